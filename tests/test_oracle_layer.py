@@ -1,0 +1,210 @@
+"""Pins of the oracle's layer math: pure-Python loops (math module only) on tiny
+inputs, textbook special cases and invariants.
+
+Layer structure: QKV projections, attention, output projection and an MLP whose
+weights are four h x h and two h x h2 matrices (FlexGen paper explainer, "Cost Model
+and Policy Search", the 8*h1^2 + 4*h1*h2 weight term); pre-LN and ReLU come from the
+workload definition; readings R5-R10 are stated in ``oracle/layer.py``.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import fg_synth
+from oracle import layer as OL
+from oracle import quant as Q
+
+
+# ----------------------------------------------------------------------------- loops
+
+
+def ln_loop(row, g, b, eps):
+    n = len(row)
+    mu = sum(row) / n
+    var = sum((v - mu) ** 2 for v in row) / n
+    return [(v - mu) / math.sqrt(var + eps) * gg + bb for v, gg, bb in zip(row, g, b)]
+
+
+def matvec_loop(x, W, bias):
+    K, N = len(W), len(W[0])
+    return [sum(x[k] * W[k][n] for k in range(K)) + bias[n] for n in range(N)]
+
+
+def attn_loop(q, ks, vs, d):
+    """softmax over positions of q.k/sqrt(d), applied to v (one head)."""
+    sc = [sum(qi * ki for qi, ki in zip(q, k)) / math.sqrt(d) for k in ks]
+    m = max(sc)
+    e = [math.exp(s - m) for s in sc]
+    z = sum(e)
+    return [sum(e[t] * vs[t][j] for t in range(len(ks))) / z for j in range(len(vs[0]))]
+
+
+def tolist(a):
+    return np.asarray(a, dtype=np.float64).tolist()
+
+
+# ----------------------------------------------------------------------------- tests
+
+
+def test_layernorm_loop_and_moments():
+    r = np.random.Generator(np.random.PCG64(11))
+    x = r.standard_normal((3, 96)) * 3 + 1
+    g = r.standard_normal(96)
+    b = r.standard_normal(96)
+    y = OL.layernorm(x, g, b, 1e-5)
+    for i in range(3):
+        assert np.allclose(y[i], ln_loop(tolist(x[i]), tolist(g), tolist(b), 1e-5),
+                           rtol=0, atol=1e-12)
+    y1 = OL.layernorm(x, np.ones(96), np.zeros(96), 0.0)
+    assert np.allclose(y1.mean(-1), 0, atol=1e-12)
+    assert np.allclose(y1.var(-1), 1, atol=1e-12)
+
+
+def test_causal_attention_loop():
+    r = np.random.Generator(np.random.PCG64(12))
+    S, T, H, d = 2, 5, 2, 4
+    q, k, v = (r.standard_normal((S, T, H * d)) for _ in range(3))
+    o = OL.causal_attention(q, k, v, H, d)
+    for s in range(S):
+        for i in range(T):
+            for hh in range(H):
+                sl = slice(hh * d, hh * d + d)
+                ref = attn_loop(tolist(q[s, i, sl]), [tolist(k[s, j, sl]) for j in range(i + 1)],
+                                [tolist(v[s, j, sl]) for j in range(i + 1)], d)
+                assert np.allclose(o[s, i, sl], ref, rtol=0, atol=1e-12)
+
+
+def test_attention_special_cases():
+    r = np.random.Generator(np.random.PCG64(13))
+    T, H, d = 6, 2, 8
+    v = r.standard_normal((1, T, H * d))
+    k = r.standard_normal((1, T, H * d))
+    # position 0 sees only itself: output = v_0
+    o = OL.causal_attention(r.standard_normal((1, T, H * d)), k, v, H, d)
+    assert np.allclose(o[0, 0], v[0, 0], atol=1e-14)
+    # equal scores (q = 0): position i outputs the mean of v_0..v_i
+    o = OL.causal_attention(np.zeros((1, T, H * d)), k, v, H, d)
+    for i in range(T):
+        assert np.allclose(o[0, i], v[0, :i + 1].mean(0), atol=1e-14)
+    # decode over one position returns v; over equal scores returns the mean
+    od = OL.decode_attention(r.standard_normal((1, H * d)), k[:, :1], v[:, :1], H, d)
+    assert np.allclose(od[0], v[0, 0], atol=1e-14)
+    od = OL.decode_attention(np.zeros((1, H * d)), k, v, H, d)
+    assert np.allclose(od[0], v[0].mean(0), atol=1e-14)
+
+
+def test_decode_attention_loop():
+    r = np.random.Generator(np.random.PCG64(14))
+    S, T, H, d = 2, 7, 2, 4
+    q = r.standard_normal((S, H * d))
+    K, V = r.standard_normal((S, T, H * d)), r.standard_normal((S, T, H * d))
+    o = OL.decode_attention(q, K, V, H, d)
+    for s in range(S):
+        for hh in range(H):
+            sl = slice(hh * d, hh * d + d)
+            ref = attn_loop(tolist(q[s, sl]), tolist(K[s, :, sl]), tolist(V[s, :, sl]), d)
+            assert np.allclose(o[s, sl], ref, rtol=0, atol=1e-12)
+
+
+def test_relu():
+    assert OL.relu(np.array([-1.0, 0.0, 2.0])).tolist() == [0.0, 0.0, 2.0]
+
+
+def _tiny_layer(f=128, random_affine=True):
+    wl = fg_synth.WORKLOADS["tiny"].with_(h=128, H=2, d=64, f=f, s=3, n=2, g=1, m=1)
+    p = fg_synth.layer_params(wl, 0, random_affine=random_affine)
+    return wl, p, OL.QuantLayer(p, wl.H, wl.d, wl.ln_eps)
+
+
+def layer_loop(L, wl, xs, Kc, Vc):
+    """One layer on one token (pure Python) given the K/V rows it attends over."""
+    v = {k: tolist(a) for k, a in L.vec.items()}
+    W = {k: tolist(a) for k, a in L.w_hat.items()}
+    h, H, d = wl.h, wl.H, wl.d
+    a = ln_loop(xs, v["ln1_g"], v["ln1_b"], wl.ln_eps)
+    qkv = matvec_loop(a, W["wqkv"], v["bqkv"])
+    q = qkv[:h]
+    att = []
+    for hh in range(H):
+        sl = slice(hh * d, hh * d + d)
+        att += attn_loop(q[sl], [k[sl] for k in Kc], [vv[sl] for vv in Vc], d)
+    h1 = [xi + oi for xi, oi in zip(xs, matvec_loop(att, W["wo"], v["bo"]))]
+    if L.f == 0:
+        return h1, qkv
+    u = ln_loop(h1, v["ln2_g"], v["ln2_b"], wl.ln_eps)
+    mid = [max(t, 0.0) for t in matvec_loop(u, W["w1"], v["b1"])]
+    return [a_ + b_ for a_, b_ in zip(h1, matvec_loop(mid, W["w2"], v["b2"]))], qkv
+
+
+@pytest.mark.parametrize("f", [128, 0])
+def test_layer_prefill_and_decode_loop(f):
+    wl, p, L = _tiny_layer(f)
+    r = np.random.Generator(np.random.PCG64(15))
+    x = r.standard_normal((1, wl.s, wl.h)).astype(np.float16)
+    cache = OL.KVCache(1, wl.s + 2, wl.h)
+    y = OL.layer_prefill(L, x, cache)
+    h = wl.h
+    # prefill: position i attends over the fp16 K/V of positions 0..i (R5)
+    kv16 = []
+    for i in range(wl.s):
+        _, qkv = layer_loop(L, wl, tolist(x[0, i].astype(np.float64)), [[0.0] * h], [[0.0] * h])
+        kv16.append((np.array(qkv[h:2 * h]).astype(np.float16).astype(np.float64).tolist(),
+                     np.array(qkv[2 * h:]).astype(np.float16).astype(np.float64).tolist()))
+    for i in range(wl.s):
+        ref, _ = layer_loop(L, wl, tolist(x[0, i].astype(np.float64)),
+                            [kv16[j][0] for j in range(i + 1)], [kv16[j][1] for j in range(i + 1)])
+        assert np.allclose(y[0, i], ref, rtol=1e-10, atol=1e-10)
+    # the cache holds the quantised fp16 K/V of the prompt
+    kq, ka, kb = Q.quantize_g64(np.array([kv[0] for kv in kv16], np.float16))
+    assert np.array_equal(cache.qk[0, :wl.s], kq)
+    # decode at pos = s: attends over the dequantised cache including the new token (R5)
+    xd = r.standard_normal((1, wl.h)).astype(np.float16)
+    yd = OL.layer_decode(L, xd, cache, wl.s)
+    _, qkv = layer_loop(L, wl, tolist(xd[0].astype(np.float64)), [[0.0] * h], [[0.0] * h])
+    knew = np.array(qkv[h:2 * h]).astype(np.float16)[None]
+    vnew = np.array(qkv[2 * h:]).astype(np.float16)[None]
+    krows = np.concatenate([np.array([kv[0] for kv in kv16], np.float16), knew])
+    vrows = np.concatenate([np.array([kv[1] for kv in kv16], np.float16), vnew])
+    khat = Q.dequant_g64(*Q.quantize_g64(krows)).astype(np.float64)
+    vhat = Q.dequant_g64(*Q.quantize_g64(vrows)).astype(np.float64)
+    ref, _ = layer_loop(L, wl, tolist(xd[0].astype(np.float64)), tolist(khat), tolist(vhat))
+    assert np.allclose(yd[0], ref, rtol=1e-10, atol=1e-10)
+
+
+def test_run_stack_positions():
+    wl = fg_synth.WORKLOADS["tiny"].with_(h=128, H=2, d=64, f=128, s=4, n=3, g=1, m=2, L=2)
+    layers = [OL.QuantLayer(fg_synth.layer_params(wl, l, True), wl.H, wl.d) for l in range(wl.L)]
+    xp = fg_synth.prompt_states(wl)
+    xs = fg_synth.step_states(wl)
+    out = OL.run_stack(layers, xp, xs, cap=wl.cap)
+    assert out["prefill"].shape == (wl.B, wl.s, wl.h)
+    assert out["steps"].shape == (wl.n - 1, wl.B, wl.h)
+    for c in out["caches"]:
+        assert c.length == wl.s + wl.n - 1          # prefill + (n-1) appended tokens
+    # sequences are independent: the stack over one sequence equals its row in the block
+    one = OL.run_stack(layers, xp[1:2], xs[:, 1:2], cap=wl.cap)
+    assert np.allclose(one["steps"][:, 0], out["steps"][:, 1], rtol=0, atol=1e-12)
+
+
+def test_planted_layer_mistakes_are_caught():
+    """A dropped residual or a missing 1/sqrt(d) in the oracle breaks the loop pin."""
+    wl, p, L = _tiny_layer(128)
+    r = np.random.Generator(np.random.PCG64(16))
+    x = r.standard_normal((1, wl.s, wl.h)).astype(np.float16)
+    good = OL.layer_prefill(L, x, OL.KVCache(1, wl.s, wl.h))
+    orig = OL.causal_attention
+    try:
+        OL.causal_attention = (lambda q, k, v, H, d, dt=np.float64:
+                               orig(np.asarray(q) * np.sqrt(d), k, v, H, d, dt))
+        bad = OL.layer_prefill(L, x, OL.KVCache(1, wl.s, wl.h))
+    finally:
+        OL.causal_attention = orig
+    assert not np.allclose(good, bad, rtol=1e-6, atol=1e-6)
+    orig_mlp = OL._mlp_and_residual
+    try:
+        OL._mlp_and_residual = lambda L_, h1, dt: orig_mlp(L_, h1, dt) - h1
+        bad = OL.layer_prefill(L, x, OL.KVCache(1, wl.s, wl.h))
+    finally:
+        OL._mlp_and_residual = orig_mlp
+    assert not np.allclose(good, bad, rtol=1e-6, atol=1e-6)
