@@ -1,0 +1,248 @@
+// Causal prefill attention over fp16 Q/K/V (sm_103a).
+//
+// The prefill step processes every prompt token at once and builds the KV cache
+// [FlexGen paper explainer, "Problem Formulation", Figure 2].  Prefill attends over the
+// fp16 K/V the projection just produced (the cache keeps the 4-bit copy for decoding).
+//
+// Flash-style: a CTA owns 64 query rows of one (sequence, head), 4 warps x 16 rows; K/V
+// tiles of 64 keys stream through a double-buffered cp.async ring; S = Q K^T and O += P V
+// run on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with an online base-2 softmax.
+// Q, K, V are read in place from the [rows][3h] QKV buffer.
+#include <math.h>
+
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace fg {
+namespace {
+
+constexpr int kRows = 64;      // query rows per CTA
+constexpr int kKeys = 64;      // keys per tile
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D>
+struct Smem {
+  static constexpr int LD = D + 8;                  // padded row (halves)
+  static constexpr int TILE = kRows * LD;           // halves per tile
+  static constexpr int BYTES = 5 * TILE * 2;        // Q, K[2], V[2]
+};
+
+template <int D>
+__global__ void __launch_bounds__(128)
+prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_log2,
+                    uint16_t* __restrict__ out) {
+  constexpr int LD = Smem<D>::LD;
+  constexpr int TILE = Smem<D>::TILE;
+  extern __shared__ __align__(16) uint16_t sm[];
+  uint16_t* sQ = sm;
+  uint16_t* sK = sm + TILE;            // 2 tiles
+  uint16_t* sV = sm + 3 * TILE;        // 2 tiles
+
+  const int qt = blockIdx.x, hd = blockIdx.y, seq = blockIdx.z;
+  const int h = H * D;
+  const int64_t row0 = (int64_t)seq * s;       // first row of this sequence
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int q0 = qt * kRows;
+
+  // ---- async loads: a tile is 64 rows x D halves = 64 * D/8 16-byte chunks
+  auto load_tile = [&](uint16_t* dst, int col, int r0) {
+    constexpr int CPR = D / 8;
+    for (int c = threadIdx.x; c < kRows * CPR; c += 128) {
+      const int r = c / CPR, cc = c % CPR;
+      const int pos = r0 + r;
+      const bool valid = pos < s;
+      const uint16_t* src = qkv + (row0 + (valid ? pos : 0)) * (3 * h) + col + cc * 8;
+      cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * LD + cc * 8)), src,
+                 valid);
+    }
+  };
+  load_tile(sQ, hd * D, q0);
+  load_tile(sK, h + hd * D, 0);
+  load_tile(sV, 2 * h + hd * D, 0);
+  cp_commit();
+
+  const int nkt = min(qt + 1, (s + kKeys - 1) / kKeys);   // causal: tiles 0..qt
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[i][c] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  uint32_t qf[D / 16][4];
+
+  for (int kt = 0; kt < nkt; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nkt) {
+      load_tile(sK + (buf ^ 1) * TILE, h + hd * D, (kt + 1) * kKeys);
+      load_tile(sV + (buf ^ 1) * TILE, 2 * h + hd * D, (kt + 1) * kKeys);
+    }
+    cp_commit();
+    cp_wait<1>();
+    __syncthreads();
+    if (kt == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int c = ks * 16 + 8 * (lane >> 4);
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(sQ + r * LD + c)), qf[ks][0],
+                qf[ks][1], qf[ks][2], qf[ks][3]);
+      }
+    }
+    const uint16_t* kb = sK + buf * TILE;
+    const uint16_t* vb = sV + buf * TILE;
+
+    // ---- S = Q K^T for 16 rows x 64 keys
+    float sc[kKeys / 8][4];
+#pragma unroll
+    for (int nb = 0; nb < kKeys / 8; ++nb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sc[nb][c] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int nb = 0; nb < kKeys / 8; nb += 2) {
+        const int i = lane >> 3;
+        const int key = nb * 8 + (lane & 7) + 8 * (i >> 1);
+        const int c = ks * 16 + 8 * (i & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(kb + key * LD + c)), b0, b1, b2,
+                b3);
+        mma16816(sc[nb], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+        mma16816(sc[nb + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+      }
+    }
+    // ---- mask (causal and sequence tail), online softmax in base 2
+    const int qrow[2] = {q0 + warp * 16 + gid, q0 + warp * 16 + gid + 8};
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < kKeys / 8; ++nb) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = kt * kKeys + nb * 8 + 2 * tig + (c & 1);
+        const int r = c >> 1;
+        float v = sc[nb][c] * scale_log2;
+        if (key > qrow[r] || key >= s) v = -INFINITY;
+        sc[nb][c] = v;
+        mx[r] = fmaxf(mx[r], v);
+      }
+    }
+    float corr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
+      const float m_new = fmaxf(m_run[r], mx[r]);
+      corr[r] = (m_run[r] == -INFINITY) ? 0.0f : exp2f(m_run[r] - m_new);
+      m_run[r] = m_new;
+    }
+    float ls[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int nb = 0; nb < kKeys / 8; ++nb) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int r = c >> 1;
+        const float p = (m_run[r] == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - m_run[r]);
+        sc[nb][c] = p;
+        ls[r] += p;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      ls[r] += __shfl_xor_sync(0xFFFFFFFFu, ls[r], 1);
+      ls[r] += __shfl_xor_sync(0xFFFFFFFFu, ls[r], 2);
+      l_run[r] = l_run[r] * corr[r] + ls[r];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr[0]; o[i][1] *= corr[0];
+      o[i][2] *= corr[1]; o[i][3] *= corr[1];
+    }
+    // ---- O += P V
+#pragma unroll
+    for (int kk = 0; kk < kKeys / 16; ++kk) {
+      const uint32_t a0 = pack_h2(sc[2 * kk][0], sc[2 * kk][1]);
+      const uint32_t a1 = pack_h2(sc[2 * kk][2], sc[2 * kk][3]);
+      const uint32_t a2 = pack_h2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      const uint32_t a3 = pack_h2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+      for (int nb = 0; nb < D / 8; nb += 2) {
+        const int i = lane >> 3;
+        const int key = kk * 16 + (lane & 7) + 8 * (i & 1);
+        const int c = nb * 8 + 8 * (i >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(static_cast<uint32_t>(__cvta_generic_to_shared(vb + key * LD + c)), b0, b1, b2,
+                  b3);
+        mma16816(o[nb], a0, a1, a2, a3, b0, b1);
+        mma16816(o[nb + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();     // the buffer is refilled by the next iteration's loads
+  }
+
+  // ---- normalise and store
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int qr = q0 + warp * 16 + gid + 8 * r;
+    if (qr >= s) continue;
+    const float inv = (l_run[r] > 0.0f) ? 1.0f / l_run[r] : 0.0f;
+    uint16_t* op = out + (row0 + qr) * h + hd * D;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      *reinterpret_cast<uint32_t*>(op + i * 8 + 2 * tig) =
+          pack_h2(o[i][2 * r] * inv, o[i][2 * r + 1] * inv);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
+                                int32_t d, float scale, uint16_t* out, cudaStream_t st) {
+  if (nseq == 0 || s == 0) return cudaSuccess;
+  dim3 grid((unsigned)((s + kRows - 1) / kRows), (unsigned)H, (unsigned)nseq);
+  const float sl2 = scale * 1.4426950408889634f;
+  if (d == 128) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        prefill_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
+    if (attr != cudaSuccess) return attr;
+    prefill_attn_kernel<128><<<grid, 128, Smem<128>::BYTES, st>>>(qkv, s, H, sl2, out);
+  } else {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        prefill_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
+    if (attr != cudaSuccess) return attr;
+    prefill_attn_kernel<64><<<grid, 128, Smem<64>::BYTES, st>>>(qkv, s, H, sl2, out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fg

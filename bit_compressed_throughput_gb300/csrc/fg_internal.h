@@ -1,0 +1,62 @@
+// Host-side declarations shared by the translation units of libfg.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fg.h"
+
+namespace fg {
+
+// Launchers: enqueue one kernel on `st`; return cudaGetLastError().
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* codes,
+                            uint32_t* ab, cudaStream_t st);
+cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64_t cols,
+                           uint16_t* y, cudaStream_t st);
+cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
+                             int32_t T, int32_t pos, const fg_kvcache& kv, cudaStream_t st);
+cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* g,
+                             const uint16_t* b, float eps, uint16_t* y, cudaStream_t st);
+cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
+                                int32_t d, float scale, uint16_t* out, cudaStream_t st);
+
+// Decode attention: number of sequence splits used for (kv, len); workspace bytes.
+int decode_attn_splits(const fg_kvcache& kv, int32_t len, int num_sms);
+size_t decode_attn_ws_bytes(const fg_kvcache& kv, int32_t len, int num_sms);
+// Launches the split kernel and, when splits > 1, the combine kernel (recording
+// `mid_event`, when given, between the two).  `kernels_out` receives 1 or 2.
+cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
+                               int32_t len, float scale, uint16_t* out, void* ws,
+                               int num_sms, cudaStream_t st, int* kernels_out,
+                               cudaEvent_t mid_event);
+
+// Dequant-fused GEMM plan: tiles, split-K factor and workspace.
+struct GemmPlan {
+  int64_t M, N, K;
+  int tiles_m, tiles_n, kblocks, splits, kb_per_split;
+  size_t ws_bytes;
+};
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms);
+cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
+                        const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
+                        void* ws, cudaStream_t st, cudaEvent_t mid_event);
+// Device error word of the GEMM's bounded waits: read-and-clear (after a sync).
+cudaError_t gemm_read_error(unsigned int* out);
+
+// Algorithmic work of one launch (bytes for memory-bound kernels, flops for the GEMM and
+// prefill attention): 4-bit storage costs 0.5 byte per element plus one (a, b) fp16 pair
+// per group of 64, i.e. 0.5625 byte.
+inline double work_gemm(int64_t M, int64_t N, int64_t K) { return 2.0 * M * N * K; }
+inline double work_gemm_reduce(int64_t M, int64_t N, int splits) {
+  return (double)splits * M * N * 4.0 + 2.0 * M * N;
+}
+inline double work_quantize(double elems) { return elems * (2.0 + 0.5625); }
+inline double work_decode_attn(int64_t B, int64_t len, int64_t h) {
+  return 2.0 * B * len * h * 0.5625 + 4.0 * B * h;
+}
+inline double work_prefill_attn(int64_t nseq, int64_t s, int64_t h) {
+  return 2.0 * nseq * h * s * (s + 1);
+}
+inline double work_layernorm(int64_t rows, int64_t h) { return 4.0 * rows * h; }
+
+}  // namespace fg

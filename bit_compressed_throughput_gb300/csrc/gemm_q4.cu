@@ -1,0 +1,502 @@
+// Dequant-fused GEMM on the 5th-generation tensor cores (sm_103a):
+//   Y[M][N] = epi( X[M][K] * W^[K][N] + bias )
+// where W^ is restored to fp16 from 4-bit codes grouped 64 along the output channel N
+// with per-group (a, b) [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가":
+// weights grouped along the output channel, restored to FP16 before compute, no INT4
+// matmul].  The block schedule's batch reuse makes the projections and the MLP dense
+// contractions over M = g*s (prefill) or M = B (decode) rows.
+//
+// CTA tile 128 x 256, K step 64, 3-stage ring, 6 warps:
+//   warp 0     TMA producer (X tile, 128B swizzle, K-major; packed code tile, 128B
+//              swizzle) + TMEM allocation
+//   warp 1     one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into a
+//              128 x 256 fp32 accumulator in TMEM and commits to mbarriers
+//   warps 2-5  restore codes -> fp16 B tile in shared memory (MN-major, 128B swizzle: one
+//              k-row of 64 output channels = one 128-byte swizzle row = one group), then
+//              run the epilogue: tcgen05.ld, bias / ReLU / residual, fp16 store
+// Restoration per pair of codes: the nibble is OR-ed into the mantissa of 1.0h so that
+// the half equals 1 + q/4, then one HFMA2 gives (1 + q/4)*(4s) + (a - 4s) = a + q*s.
+// Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7); the epilogue
+// undoes that order when it packs the accumulator columns back to fp16.
+//
+// Small M (decode) splits K over blockIdx.z; partial fp32 tiles go to the caller's
+// workspace and a reduce kernel applies the epilogue.
+//
+// Every mbarrier wait is bounded (about 2 s); on timeout the CTA raises an abort flag,
+// sets the device error word, drains its outstanding copies and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace fg {
+
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BK * BN * 2;        // 32 KB
+constexpr int C_BYTES = BK * BN / 2;        // 8 KB of codes
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr long long kWaitCycles = 1ll << 32;
+constexpr int SWZ_GROUP_M = 8;
+
+// instruction descriptor: D f32, A f16 K-major, B f16 MN-major, N = 256, M = 128
+constexpr uint32_t IDESC = (1u << 4) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait.  Returns false (and raises the CTA abort flag) on timeout or when another
+// warp already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(&g_gemm_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x),
+      "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: start, leading / stride byte offsets (>> 4), the
+// descriptor version bit of this architecture, 128-byte swizzle layout.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t x, uint32_t s, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&s),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Restore 8 codes (one word) of one group to 4 half2 in (n0,n4),(n1,n5),(n2,n6),(n3,n7).
+__device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s4, uint32_t c) {
+  uint4 o;
+  o.x = hfma2_u32(((w << 8) & 0x0F000F00u) | 0x3C003C00u, s4, c);
+  o.y = hfma2_u32(((w << 4) & 0x0F000F00u) | 0x3C003C00u, s4, c);
+  o.z = hfma2_u32((w & 0x0F000F00u) | 0x3C003C00u, s4, c);
+  o.w = hfma2_u32(((w >> 4) & 0x0F000F00u) | 0x3C003C00u, s4, c);
+  return o;
+}
+
+struct EpiArgs {
+  const uint16_t* bias;
+  const uint16_t* residual;
+  uint16_t* Y;
+  float* partial;     // split-K: [splits][M][N] fp32, else null
+  int epi;
+};
+
+// Bias / ReLU / residual on 8 consecutive outputs and the fp16 store.
+__device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int64_t row, int n,
+                                          int N) {
+  if (ea.bias) {
+    const uint4 bu = ldg_nc_v4(ea.bias + n);
+    const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_h2(bw[i]);
+      v[2 * i] += f.x;
+      v[2 * i + 1] += f.y;
+    }
+  }
+  if (ea.epi == FG_EPI_RELU) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = fmaxf(v[i], 0.0f);
+  } else if (ea.epi == FG_EPI_RESIDUAL) {
+    const uint4 ru = *reinterpret_cast<const uint4*>(ea.residual + row * N + n);
+    const uint32_t rw[4] = {ru.x, ru.y, ru.z, ru.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_h2(rw[i]);
+      v[2 * i] += f.x;
+      v[2 * i + 1] += f.y;
+    }
+  }
+  uint4 o;
+  o.x = pack_h2(v[0], v[1]);
+  o.y = pack_h2(v[2], v[3]);
+  o.z = pack_h2(v[4], v[5]);
+  o.w = pack_h2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+                  const uint32_t* __restrict__ ab, int M, int N, int K, int tiles_m, int tiles_n,
+                  int kblocks, int kb_per_split, EpiArgs ea) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                  // STAGES x A_BYTES
+  uint8_t* sB = smem + STAGES * A_BYTES;               // STAGES x B_BYTES
+  uint8_t* sC = sB + STAGES * B_BYTES;                 // STAGES x C_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + STAGES * C_BYTES);
+  // bars: full_raw[S], full_b[S], empty[S], acc_full
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- tile coordinates (grouped raster: SWZ_GROUP_M m-tiles share a wave of n-tiles)
+  const int lin = blockIdx.x;
+  const int group_span = SWZ_GROUP_M * tiles_n;
+  const int grp = lin / group_span;
+  const int first_m = grp * SWZ_GROUP_M;
+  const int gm = min(SWZ_GROUP_M, tiles_m - first_m);
+  const int within = lin - grp * group_span;
+  const int tm = first_m + within % gm;
+  const int tn = within / gm;
+  const int m0 = tm * BM, n0 = tn * BN;
+  const int kb0 = blockIdx.z * kb_per_split;
+  const int kb1 = min(kblocks, kb0 + kb_per_split);
+  const int nkb = max(0, kb1 - kb0);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_raw = [&](int s) { return bar0 + 8u * s; };
+  auto full_b = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (3 * STAGES);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_raw(s), 1);
+      mbar_init(full_b(s), 128);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES && !mbar_wait(empty(s), ((i / STAGES) & 1) ^ 1, abort_flag)) break;
+        mbar_expect_tx(full_raw(s), A_BYTES + C_BYTES);
+        tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, (kb0 + i) * BK, m0, full_raw(s));
+        tma_load_2d(smem_u32(sC + s * C_BYTES), &tmC, n0 / 2, (kb0 + i) * BK, full_raw(s));
+        issued = i + 1;
+      }
+      // Drain: every issued load must have landed before this CTA can exit.
+      for (int i = max(0, issued - STAGES); i < issued; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_try(full_raw(i % STAGES), (i / STAGES) & 1)) {
+          if (clock64() - t0 > kWaitCycles) {
+            atomicOr(&g_gemm_error, 2u);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(full_raw(s), ph, abort_flag)) break;
+        if (!mbar_wait(full_b(s), ph, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+        const uint32_t b_base = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc(b_base + kk * 16 * 128, 64 * 128, 1024);
+          umma_f16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(empty(s));
+      }
+      umma_commit(acc_full);
+    }
+  } else {
+    // ------------------------------------------------------------ restore + epilogue
+    const int tid = threadIdx.x - 64;                 // 0..127
+    const int gpr = N / 64;                           // groups per weight row
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      const int kbase = (kb0 + i) * BK;
+      // group statistics of this thread's 4 items (plain loads; tiny and L2-resident)
+      uint32_t abw[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = it * 128 + tid;
+        const int k = (item & 7) | (((item >> 6) & 7) << 3);
+        const int c = (item >> 3) & 7;
+        const int kg = kbase + k, ng = n0 / 64 + (c >> 1);
+        abw[it] = (kg < K && ng < gpr) ? __ldg(ab + (int64_t)kg * gpr + ng) : 0u;
+      }
+      if (!mbar_wait(full_raw(s), ph, abort_flag)) break;
+      const uint8_t* cs = sC + s * C_BYTES;
+      uint8_t* bs = sB + s * B_BYTES;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = it * 128 + tid;
+        const int k = (item & 7) | (((item >> 6) & 7) << 3);
+        const int c = (item >> 3) & 7;
+        const int sw = k & 7;
+        const uint4 cw = *reinterpret_cast<const uint4*>(cs + k * 128 + ((c ^ sw) << 4));
+        const float2 abf = unpack_h2(abw[it]);
+        const float sc4 = (abf.y - abf.x) * (4.0f / 15.0f);
+        const uint32_t s4 = pack_h2(sc4, sc4);
+        const float cf = abf.x - sc4;
+        const uint32_t cc = pack_h2(cf, cf);
+        uint8_t* brow = bs + (c >> 1) * (BK * 128) + k * 128;
+        const int jc0 = (c & 1) * 4;
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s4, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s4, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s4, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s4, cc);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(full_b(s));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    const bool acc_ok = mbar_wait(acc_full, 0, abort_flag);
+    __syncwarp();
+    tc_fence_after();
+    const int lane_base = 32 * (warp & 3);       // TMEM lanes this warp may read
+    const int64_t row = (int64_t)m0 + lane_base + lane;
+    if (acc_ok && nkb > 0) {
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + cc * 32;
+        __syncwarp();
+        tmem_ld16(taddr, r);
+        tmem_ld16(taddr + 16, r + 16);
+        tmem_wait_ld();
+        if (row < M) {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const int n = n0 + cc * 32 + g8 * 8;
+            if (n < N) {
+              float v[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[i] = __uint_as_float(r[8 * g8 + 2 * i]);
+                v[i + 4] = __uint_as_float(r[8 * g8 + 2 * i + 1]);
+              }
+              if (ea.partial) {
+                float* pp = ea.partial + ((int64_t)blockIdx.z * M + row) * N + n;
+                reinterpret_cast<float4*>(pp)[0] = make_float4(v[0], v[1], v[2], v[3]);
+                reinterpret_cast<float4*>(pp)[1] = make_float4(v[4], v[5], v[6], v[7]);
+              } else {
+                epilogue8(ea, v, row, n, N);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// Sum the split-K partials and apply bias / ReLU / residual: 8 outputs per thread.
+__global__ void __launch_bounds__(256)
+gemm_reduce_kernel(const float* __restrict__ partial, int splits, int64_t M, int N, EpiArgs ea) {
+  const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t chunks = M * (N / 8);
+  if (idx >= chunks) return;
+  const int64_t row = idx / (N / 8);
+  const int n = (int)(idx - row * (N / 8)) * 8;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < splits; ++s) {
+    const float4* pp = reinterpret_cast<const float4*>(partial + ((int64_t)s * M + row) * N + n);
+    const float4 x = pp[0], y = pp[1];
+    v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+    v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+  }
+  epilogue8(ea, v, row, n, N);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                        uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
+  GemmPlan p{};
+  p.M = M; p.N = N; p.K = K;
+  p.tiles_m = (int)((M + BM - 1) / BM);
+  p.tiles_n = (int)((N + BN - 1) / BN);
+  p.kblocks = (int)((K + BK - 1) / BK);
+  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  int splits = 1;
+  // Split K only when the tile grid leaves more than a quarter of the SMs idle, keeping
+  // at least 8 k-blocks per split so the pipeline stays full.
+  if (tiles > 0 && tiles * 4 < (int64_t)nsm * 3) {
+    splits = (int)std::max<int64_t>(1, nsm / tiles);
+    splits = std::min(splits, std::max(1, p.kblocks / 8));
+  }
+  p.kb_per_split = std::max(1, (p.kblocks + splits - 1) / splits);
+  p.splits = std::max(1, (p.kblocks + p.kb_per_split - 1) / p.kb_per_split);
+  p.ws_bytes = (p.splits > 1) ? (size_t)p.splits * M * N * sizeof(float) : 0;
+  return p;
+}
+
+cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
+                        const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
+                        void* ws, cudaStream_t st, cudaEvent_t mid_event) {
+  if (p.M == 0) return cudaSuccess;
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      gemm_q4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap tmA, tmC;
+  e = make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K, (uint64_t)p.M,
+                  (uint64_t)p.K * 2, BK, BM);
+  if (e != cudaSuccess) return e;
+  e = make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(p.N / 2),
+                  (uint64_t)p.K, (uint64_t)(p.N / 2), BN / 2, BK);
+  if (e != cudaSuccess) return e;
+  const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
+  EpiArgs ea = final_ea;
+  if (p.splits > 1) ea.partial = static_cast<float*>(ws);
+  dim3 grid((unsigned)(p.tiles_m * p.tiles_n), 1, (unsigned)p.splits);
+  gemm_q4_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmC, W.ab, (int)p.M, (int)p.N,
+                                                       (int)p.K, p.tiles_m, p.tiles_n, p.kblocks,
+                                                       p.kb_per_split, ea);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  if (mid_event) cudaEventRecord(mid_event, st);
+  const int64_t chunks = p.M * (p.N / 8);
+  gemm_reduce_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, st>>>(
+      static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_read_error(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_gemm_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace fg

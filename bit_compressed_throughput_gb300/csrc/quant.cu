@@ -1,0 +1,160 @@
+// Group-wise 4-bit quantisation, restoration and KV-cache append (sm_103a).
+//
+// FlexGen stores weights and the KV cache as 4-bit codes in groups of 64 (weights along
+// the output channel, K/V along the hidden dimension) with the group min a and max b,
+// and restores FP16 values before compute [FlexGen review (jaehun.me), section
+// "4-bit 압축은 정수 연산 가속과 같은가", restating paper §5].  The code formula is the
+// library's binary32 reading documented in include/fg.h.
+//
+// Work split: 8 threads per group of 64, each owning 8 consecutive values (one 16-byte
+// load, one 4-byte code store); the group min/max is a 3-step xor shuffle inside the
+// 8-lane segment.  These kernels are HBM-bound: 2 bytes read and 0.5625 bytes written
+// per element.
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace fg {
+
+namespace {
+
+constexpr int kThreads = 256;                 // 32 groups per CTA
+constexpr int kGroupsPerCta = kThreads / 8;
+
+// Quantise the 8 values held by this thread (part of a 64-group spread over 8 lanes).
+// Returns the packed codes; *ab_out receives the group's statistics word.
+__device__ __forceinline__ uint32_t quantize8(const uint4 v, uint32_t* ab_out) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = order_key(w[i] & 0xFFFFu), hi = order_key(w[i] >> 16);
+    kmin = min(kmin, min(lo, hi));
+    kmax = max(kmax, max(lo, hi));
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  const uint32_t abits = key_to_bits(kmin), bbits = key_to_bits(kmax);
+  const float af = h2f((uint16_t)abits), bf = h2f((uint16_t)bbits);
+  const float bma = __fsub_rn(bf, af);
+  uint32_t codes = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c0 = q4_code(h2f((uint16_t)(w[i] & 0xFFFFu)), af, bma);
+    const uint32_t c1 = q4_code(h2f((uint16_t)(w[i] >> 16)), af, bma);
+    codes |= (c0 | (c1 << 4)) << (8 * i);
+  }
+  *ab_out = abits | (bbits << 16);
+  return codes;
+}
+
+__global__ void __launch_bounds__(kThreads)
+quantize_kernel(const uint16_t* __restrict__ x, int64_t ngroups, uint8_t* __restrict__ codes,
+                uint32_t* __restrict__ ab) {
+  const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  // Every lane of a warp takes part in the shuffles; lanes past the end use a dummy.
+  const bool live = grp < ngroups;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (live) v = ldg_nc_v4(x + grp * 64 + sub * 8);
+  uint32_t abw;
+  const uint32_t c = quantize8(v, &abw);
+  if (live) {
+    reinterpret_cast<uint32_t*>(codes)[grp * 8 + sub] = c;
+    if (sub == 0) ab[grp] = abw;
+  }
+}
+
+// One CTA slice covers groups of the rows (b, t) of K and V: blockIdx.y selects K (0)
+// or V (1).  Row r = b*T + t of the source lives at r*row_stride elements.
+__global__ void __launch_bounds__(kThreads)
+kv_append_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                 int64_t row_stride, int T, int pos, int H, int d, int cap, int gpr,
+                 int64_t ngroups, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                 uint32_t* __restrict__ k_ab, uint32_t* __restrict__ v_ab) {
+  const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  const bool live = grp < ngroups;
+  const uint16_t* src = blockIdx.y ? v_new : k_new;
+  int64_t row = 0;
+  int gi = 0;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (live) {
+    row = grp / gpr;
+    gi = (int)(grp - row * gpr);
+    v = ldg_nc_v4(src + row * row_stride + (int64_t)gi * 64 + sub * 8);
+  }
+  uint32_t abw;
+  const uint32_t c = quantize8(v, &abw);
+  if (live) {
+    const int gph = d >> 6;                       // groups per head
+    const int64_t b = row / T;
+    const int t = (int)(row - b * T);
+    const int head = gi / gph, gs = gi - head * gph;
+    const int64_t slot = ((b * H + head) * (int64_t)cap + pos + t);
+    uint8_t* cdst = blockIdx.y ? v_codes : k_codes;
+    uint32_t* adst = blockIdx.y ? v_ab : k_ab;
+    reinterpret_cast<uint32_t*>(cdst + slot * (d >> 1) + gs * 32)[sub] = c;
+    if (sub == 0) adst[slot * gph + gs] = abw;
+  }
+}
+
+// Standalone restoration: fp16(a + q * ((b - a) / 15)), one rounding per binary32 op.
+__global__ void __launch_bounds__(kThreads)
+dequant_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ ab,
+               int64_t ngroups, uint16_t* __restrict__ y) {
+  const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  if (grp >= ngroups) return;
+  const uint32_t c = reinterpret_cast<const uint32_t*>(codes)[grp * 8 + sub];
+  const uint32_t abw = ab[grp];
+  const float af = h2f((uint16_t)(abw & 0xFFFFu)), bf = h2f((uint16_t)(abw >> 16));
+  const float s = __fdiv_rn(__fsub_rn(bf, af), 15.0f);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float q0 = (float)((c >> (8 * i)) & 0xF), q1 = (float)((c >> (8 * i + 4)) & 0xF);
+    const float x0 = __fadd_rn(af, __fmul_rn(q0, s));
+    const float x1 = __fadd_rn(af, __fmul_rn(q1, s));
+    o[i] = (uint32_t)f2h(x0) | ((uint32_t)f2h(x1) << 16);
+  }
+  reinterpret_cast<uint4*>(y + grp * 64)[sub] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+inline unsigned grid_for(int64_t ngroups) {
+  return (unsigned)((ngroups + kGroupsPerCta - 1) / kGroupsPerCta);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* codes,
+                            uint32_t* ab, cudaStream_t st) {
+  const int64_t ng = rows * (cols / 64);
+  if (ng == 0) return cudaSuccess;
+  quantize_kernel<<<grid_for(ng), kThreads, 0, st>>>(x, ng, codes, ab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64_t cols,
+                           uint16_t* y, cudaStream_t st) {
+  const int64_t ng = rows * (cols / 64);
+  if (ng == 0) return cudaSuccess;
+  dequant_kernel<<<grid_for(ng), kThreads, 0, st>>>(codes, ab, ng, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
+                             int32_t T, int32_t pos, const fg_kvcache& kv, cudaStream_t st) {
+  const int gpr = kv.h / 64;
+  const int64_t ng = (int64_t)kv.B * T * gpr;
+  if (ng == 0) return cudaSuccess;
+  const int d = kv.h / kv.H;
+  dim3 grid(grid_for(ng), 2);
+  kv_append_kernel<<<grid, kThreads, 0, st>>>(k_new, v_new, row_stride, T, pos, kv.H, d, kv.cap,
+                                              gpr, ng, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
+  return cudaGetLastError();
+}
+
+}  // namespace fg

@@ -1,0 +1,229 @@
+/*
+ * fg.h -- C ABI of libfg, the GB300 (sm_103a) engine for one OPT-style decoder layer
+ * over 4-bit group-compressed weights and KV cache, run over a block of sequences.
+ *
+ * The method (FlexGen):
+ *  - Weights and the KV cache are stored as 4-bit codes, grouped 64 elements at a
+ *    time -- along the output channel for weights, along the hidden dimension for
+ *    K/V -- with the group minimum a and maximum b kept per group, and are restored
+ *    to FP16 before any compute; INT4 is a storage format, not an INT4 matmul.
+ *    [FlexGen review (jaehun.me), section "4-bit 압축은 정수 연산 가속과 같은가",
+ *     restating paper §5; "论文阅读：FlexGen" (blog.gzher.com) §3.4]
+ *  - One layer is applied to every GPU batch of a block (B = g*m sequences) before the
+ *    next layer's weights are used; generation is a prefill over the prompt that builds
+ *    the KV cache, then decode steps that add one token per sequence.
+ *    [FlexGen paper explainer, "Compute Schedule" and Algorithm 1; Figure 2]
+ *
+ * Storage formats (the pages leave them open; these are this library's):
+ *  - fp16 values are IEEE binary16 bit patterns (uint16_t).
+ *  - codes: element 2i in the low nibble, element 2i+1 in the high nibble of byte i,
+ *    along the grouped (contiguous) dimension.
+ *  - group statistics: one uint32_t per group of 64, the fp16 bits of a in the low
+ *    half and of b in the high half.
+ *  - code q = rint((x - a) * 15 / (b - a)) in IEEE binary32 with one rounding per
+ *    operation (subtract, multiply by 15, divide), round half to even, clamped to
+ *    [0, 15]; a and b are the group min and max (-0 ordered below +0); a constant
+ *    group (b - a == 0) stores all-zero codes.  Restoring: fp16(a + q * ((b - a) / 15)).
+ *  - weight W[K][N] (K = input channel, N = output channel): codes [K][N/2] bytes,
+ *    ab [K][N/64] words, row-major, groups of 64 consecutive n at fixed k.
+ *  - KV cache of one layer: codes [B][H][cap][d/2] bytes and ab [B][H][cap][d/64]
+ *    words for K and for V, groups of 64 consecutive hidden channels (a group never
+ *    straddles two heads since d is 64 or 128).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are device memory owned by the caller; the library
+ *    never allocates, frees or keeps them.  Work is enqueued asynchronously on
+ *    `stream` (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *  - Arguments are validated on the host before any launch; a bad argument returns a
+ *    negative fg_status and launches nothing.  Validation touches no CUDA API, so it
+ *    can be exercised on a machine without a GPU.
+ *  - Device pointers must be 16-byte aligned.
+ *  - A failed launch returns FG_ERR_CUDA; fg_last_error() gives the CUDA message
+ *    (thread-local).  FG_ERR_ARCH: the current device is not sm_103.
+ *  - Every device wait inside a kernel is bounded; a wait that runs out sets a device
+ *    error word that fg_check_device_error() reads (FG_ERR_TIMEOUT).
+ */
+#ifndef FG_H_
+#define FG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FG_OK = 0,
+  FG_ERR_ARG = -1,        /* null pointer, misaligned pointer, bad enum */
+  FG_ERR_SHAPE = -2,      /* a dimension outside the supported set */
+  FG_ERR_WORKSPACE = -3,  /* workspace smaller than the matching *_workspace_bytes() */
+  FG_ERR_CUDA = -4,       /* a CUDA call or launch failed (see fg_last_error) */
+  FG_ERR_ARCH = -5,       /* current device is not compute capability 10.3 */
+  FG_ERR_CAPACITY = -6,   /* KV cache position out of range */
+  FG_ERR_TIMEOUT = -7     /* a bounded device wait ran out (kernel result invalid) */
+} fg_status;
+
+/* A 4-bit group-compressed weight W[K][N]. codes: device [K][N/2]; ab: device [K][N/64]. */
+typedef struct {
+  const uint8_t* codes;
+  const uint32_t* ab;
+  int64_t K;
+  int64_t N;
+} fg_q4mat;
+
+/* The INT4 KV cache of one layer (device buffers, layout above). */
+typedef struct {
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  uint32_t* k_ab;
+  uint32_t* v_ab;
+  int32_t B;    /* sequences */
+  int32_t cap;  /* positions per sequence */
+  int32_t h;    /* hidden size */
+  int32_t H;    /* heads; d = h / H must be 64 or 128 */
+} fg_kvcache;
+
+typedef struct {
+  int32_t h;      /* hidden size, multiple of 64, at most 16384 */
+  int32_t H;      /* heads */
+  int32_t d;      /* head dim, 64 or 128, h == H*d */
+  int32_t f;      /* FFN width, multiple of 64; 0 = attention block without the MLP */
+  float ln_eps;   /* LayerNorm epsilon */
+} fg_dims;
+
+/* One pre-LN decoder layer: h1 = x + Attn(LN1(x)) Wo + bo; y = h1 + ReLU(LN2(h1) W1 + b1) W2 + b2
+ * with [Q|K|V] = LN1(x) Wqkv + bqkv. Weights K-major (W[in][out]); wqkv is [h][3h] with
+ * columns q | k | v. All vectors fp16, device; biases may be NULL (zero).
+ * w1/w2/b1/b2/ln2_* unused when f == 0. */
+typedef struct {
+  fg_q4mat wqkv, wo, w1, w2;
+  const uint16_t *bqkv, *bo, *b1, *b2;
+  const uint16_t *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} fg_layer;
+
+/* Epilogues of fg_dequant_gemm_q4. */
+enum { FG_EPI_NONE = 0, FG_EPI_RELU = 1, FG_EPI_RESIDUAL = 2 };
+
+/* ---------------------------------------------------------------------- quantise */
+
+/* Group-wise 4-bit quantisation of fp16 x[rows][cols] (groups of 64 along cols), as
+ * defined above.  x, codes [rows][cols/2], ab [rows][cols/64]: device.
+ * cols % 64 == 0, rows >= 0 (rows == 0 is a no-op).  Bit-exact with the definition.
+ * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가"] */
+int fg_quantize_g64(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* codes,
+                    uint32_t* ab, void* stream);
+
+/* Restore fp16 y[rows][cols] = fp16(a + q * ((b - a) / 15)) (binary32, one rounding per
+ * operation).  The standalone restore; the GEMM and attention restore in registers.
+ * [same passage: values are restored to FP16 before compute] */
+int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64_t cols,
+                   uint16_t* y, void* stream);
+
+/* ---------------------------------------------------------------------- GEMM */
+
+/* Y[M][N] = epi(X[M][K] * W^ + bias) with W^ the fp16 restoration of W, fp32 accumulate.
+ * epi: FG_EPI_NONE; FG_EPI_RELU (max(.,0)); FG_EPI_RESIDUAL (+ residual[M][N]).
+ * X, bias (nullable, [N]), residual (FG_EPI_RESIDUAL only), Y: device fp16, row-major,
+ * leading dimensions K (X) and N (Y, residual).  K % 16 == 0, N % 64 == 0, M >= 0.
+ * Y may alias residual.  ws: device scratch of at least fg_gemm_workspace_bytes(M,K,N)
+ * bytes (split-K partial sums when M is small); NULL allowed when that is 0.
+ * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": restore to FP16
+ *  before compute, not an INT4 matmul; FlexGen paper explainer, "Cost Model and Policy
+ *  Search": the four h x h and two h x h2 weight matrices of a layer] */
+int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
+                       int epilogue, const uint16_t* residual, uint16_t* Y, void* ws,
+                       size_t ws_bytes, void* stream);
+size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* ---------------------------------------------------------------------- KV cache */
+
+/* Quantise new keys and values into the cache at positions pos .. pos+T-1 of every
+ * sequence.  k_new, v_new: device fp16, row (b, t) at (b*T + t) * row_stride elements,
+ * h contiguous values per row (row_stride >= h, a multiple of 8; lets K/V be read in
+ * place from a [rows][3h] QKV buffer).  T >= 0; pos >= 0; pos + T <= cap.
+ * Codes and statistics are bit-exact with fg_quantize_g64 on the same rows.
+ * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": KV grouped
+ *  along the hidden dimension; FlexGen paper explainer, Figure 2: each decode step
+ *  extends the cache] */
+int fg_kv_append_q4(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
+                    int32_t T, int32_t pos, const fg_kvcache* kv, void* stream);
+
+/* ---------------------------------------------------------------------- attention */
+
+/* Decode attention of one new token per sequence over cache positions 0 .. len-1:
+ * out[b][hd*d + j] = sum_t softmax_t(scale * q_b,hd . K^_b,hd,t) V^_b,hd,t,j with K^, V^
+ * the fp16 restorations of the cached codes.  q: device fp16, row b at b*q_stride
+ * elements; out: device fp16 [B][h].  1 <= len <= cap.  ws: device scratch of at least
+ * fg_decode_attn_workspace_bytes(kv, len) bytes (split-sequence partials).
+ * [FlexGen paper explainer, "Computation Delegation": decoding attention is I/O bound
+ *  over the KV cache] */
+int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,
+                        float scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len);
+
+/* Causal prefill attention over fp16 Q/K/V read from a QKV buffer qkv[nseq*s][3h]
+ * (columns q | k | v, head hd at hd*d): out[nseq*s][h] fp16, position i attends over
+ * positions 0..i of its own sequence, scores scaled by `scale`.  d in {64, 128}.
+ * [FlexGen paper explainer, Figure 2: the prefill step processes all prompt tokens] */
+int fg_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, int32_t d,
+                    float scale, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------- LayerNorm */
+
+/* y[rows][h] = (x - mean) / sqrt(var + eps) * gamma + beta, fp32 statistics (population
+ * variance), fp16 in and out.  h % 64 == 0, h <= 16384.  (Pre-LN of the OPT layer.) */
+int fg_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* gamma,
+                 const uint16_t* beta, float eps, uint16_t* y, void* stream);
+
+/* ---------------------------------------------------------------------- layer */
+
+/* Prefill of one layer over a block of m GPU batches of g sequences each, prompt length s:
+ * x, y: device fp16 [m][g][s][h] (y may alias x).  GPU batch k is processed in full
+ * (M = g*s rows per GEMM) before batch k+1; its K/V are quantised into `kv` positions
+ * 0..s-1 of sequences k*g .. k*g+g-1.  kv->B == g*m, s <= kv->cap.
+ * ws: device scratch of at least fg_layer_workspace_bytes(dims, g, m, s) bytes.
+ * [FlexGen paper explainer, Algorithm 1 (a layer over every GPU batch of the block);
+ *  Figure 2 (prefill builds the cache)] */
+int fg_layer_prefill(const fg_dims* dims, const fg_layer* layer, fg_kvcache* kv,
+                     const uint16_t* x, uint16_t* y, int32_t g, int32_t m, int32_t s,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* One decode step of one layer for the whole block: x, y: device fp16 [m][g][h] = [B][h]
+ * (y may alias x), one launch per operation with M = B rows so each weight is read once
+ * per step.  pos is the cache length before the step: the new K/V are appended at pos
+ * and attention runs over positions 0..pos.  pos + 1 <= kv->cap.
+ * [FlexGen paper explainer, Algorithm 1 and Figure 2] */
+int fg_layer_decode(const fg_dims* dims, const fg_layer* layer, fg_kvcache* kv,
+                    const uint16_t* x, uint16_t* y, int32_t g, int32_t m, int32_t pos,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace for fg_layer_prefill with prompts up to s_max, and for fg_layer_decode with
+ * caches up to s_max positions (the larger of the two uses). */
+size_t fg_layer_workspace_bytes(const fg_dims* dims, int32_t g, int32_t m, int32_t s_max);
+
+/* ---------------------------------------------------------------------- runtime */
+
+const char* fg_status_string(int status);
+const char* fg_last_error(void);
+/* Synchronise `stream`, read and clear the device error word: FG_OK or FG_ERR_TIMEOUT. */
+int fg_check_device_error(void* stream);
+
+/* Per-kernel timing with CUDA events recorded around every launch on its stream.
+ * kind: one of FG_K_* below.  fg_prof_query synchronises the recorded events and
+ * returns the launch count, total milliseconds and the algorithmic work of those
+ * launches (bytes for HBM-bound kinds, flops for the GEMM and prefill attention). */
+enum {
+  FG_K_QUANT = 0, FG_K_DEQUANT = 1, FG_K_GEMM = 2, FG_K_GEMM_REDUCE = 3,
+  FG_K_KV_APPEND = 4, FG_K_DECODE_ATTN = 5, FG_K_DECODE_COMBINE = 6,
+  FG_K_PREFILL_ATTN = 7, FG_K_LAYERNORM = 8, FG_K_COUNT = 9
+};
+int fg_prof_enable(int on);
+int fg_prof_reset(void);
+int fg_prof_query(int kind, int64_t* launches, double* ms, double* work);
+const char* fg_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FG_H_ */
