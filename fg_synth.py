@@ -186,3 +186,33 @@ def adversarial_groups_fp16(seed: int = 7) -> np.ndarray:
         rows.append((r.standard_normal(64).astype(np.float32)
                      * np.float32(10.0 ** r.uniform(-6, 4))).astype(np.float16))
     return np.stack(rows)
+
+
+def random_fp16(shape, seed: int, scale: float = 1.0, offset: float = 0.0) -> np.ndarray:
+    """Generic seeded N(offset, scale) fp16 array for kernel-level tests."""
+    r = np.random.Generator(np.random.PCG64(np.random.SeedSequence([9000, int(seed)])))
+    x = r.standard_normal(size=shape, dtype=np.float32) * np.float32(scale) + np.float32(offset)
+    return x.astype(np.float16)
+
+
+def random_q4_cache_torch(B: int, H: int, cap: int, d: int, seed: int, device="cuda"):
+    """Seeded random contents of one layer's 4-bit KV cache, drawn on the device with
+    torch (for workloads too large to draw on the host): codes uniform in 0..15 packed two
+    per byte, group minimum a ~ N(0, 1) and maximum b = a + |N(0, 2)|, stored as the fp16
+    bit pairs (a low, b high).  Returns (k_codes, v_codes, k_ab, v_ab) shaped like the
+    library's cache: [B][H][cap][d/2] uint8 and [B][H][cap][d/64] int32."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = []
+    for _ in range(2):
+        codes = torch.randint(0, 256, (B, H, cap, d // 2), generator=g, device=device,
+                              dtype=torch.int32).to(torch.uint8)
+        out.append(codes)
+    for _ in range(2):
+        a = torch.randn((B, H, cap, d // 64), generator=g, device=device)
+        b = a + torch.randn((B, H, cap, d // 64), generator=g, device=device).abs() * 2.0
+        ab = (a.half().view(torch.int16).to(torch.int32) & 0xFFFF) | \
+             (b.half().view(torch.int16).to(torch.int32) << 16)
+        out.append(ab)
+    return out[0], out[1], out[2], out[3]

@@ -1,0 +1,132 @@
+"""The C-ABI library builds, loads and exports every symbol include/fg.h declares, and
+its host-side argument validation rejects bad calls before touching CUDA (so these run
+on a machine without a GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fg():
+    import __graft_entry__ as g
+    g.build()
+    from bit_compressed_throughput_gb300 import fg as mod
+    return mod
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "fg.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fg_\w+)\s*\(", hdr, re.M)))
+
+
+def test_exports_every_declared_symbol(fg):
+    names = declared_symbols()
+    assert len(names) >= 19
+    missing = [n for n in names if not hasattr(fg.lib, n)]
+    assert missing == []
+
+
+def test_status_strings(fg):
+    for s in range(0, -8, -1):
+        assert fg.lib.fg_status_string(s).decode() not in ("", "unknown status")
+    assert fg.lib.fg_status_string(-99).decode() == "unknown status"
+
+
+FAKE = 0x10000          # aligned, never dereferenced: validation fails before any use
+MISALIGNED = 0x10008
+
+
+def q4(K, N, codes=FAKE, ab=FAKE):
+    from bit_compressed_throughput_gb300 import fg
+    return fg.fg_q4mat(codes, ab, K, N)
+
+
+def test_quantize_validation(fg):
+    L = fg.lib
+    assert L.fg_quantize_g64(FAKE, 4, 63, FAKE, FAKE, None) == fg.FG_ERR_SHAPE
+    assert L.fg_quantize_g64(FAKE, -1, 64, FAKE, FAKE, None) == fg.FG_ERR_SHAPE
+    assert L.fg_quantize_g64(None, 4, 64, FAKE, FAKE, None) == fg.FG_ERR_ARG
+    assert L.fg_quantize_g64(MISALIGNED, 4, 64, FAKE, FAKE, None) == fg.FG_ERR_ARG
+    assert L.fg_quantize_g64(None, 0, 64, None, None, None) == fg.FG_OK     # empty: no-op
+    assert L.fg_dequant_g64(FAKE, FAKE, 4, 96, FAKE, None) == fg.FG_ERR_SHAPE
+
+
+def test_gemm_validation(fg):
+    L = fg.lib
+    call = lambda W, M=8, bias=None, epi=0, res=None, ws=None, wsb=0, X=FAKE, Y=FAKE: \
+        L.fg_dequant_gemm_q4(X, M, C.byref(W), bias, epi, res, Y, ws, wsb, None)
+    assert call(q4(40, 256)) == fg.FG_ERR_SHAPE                 # K % 16
+    assert call(q4(64, 96)) == fg.FG_ERR_SHAPE                  # N % 64
+    assert call(q4(64, 256, codes=None)) == fg.FG_ERR_ARG
+    assert call(q4(64, 256), epi=3) == fg.FG_ERR_ARG
+    assert call(q4(64, 256), epi=fg.FG_EPI_RESIDUAL) == fg.FG_ERR_ARG   # residual missing
+    assert call(q4(64, 256), X=MISALIGNED) == fg.FG_ERR_ARG
+    assert call(q4(64, 256), M=0, X=None, Y=None) == fg.FG_OK
+    need = fg.fg_gemm_workspace_bytes(64, 4096, 256)
+    assert need > 0                                  # one tile of 256: split K
+    assert call(q4(4096, 256), M=64, ws=FAKE, wsb=need - 1) == fg.FG_ERR_WORKSPACE
+    assert fg.fg_gemm_workspace_bytes(8192, 4096, 12288) == 0      # full grid: no split
+
+
+def kvs(B=2, cap=32, h=256, H=2):
+    from bit_compressed_throughput_gb300 import fg
+    return fg.fg_kvcache(FAKE, FAKE, FAKE, FAKE, B, cap, h, H)
+
+
+def test_kv_and_attention_validation(fg):
+    L = fg.lib
+    kv = kvs()
+    assert L.fg_kv_append_q4(FAKE, FAKE, 256, 4, 30, C.byref(kv), None) == fg.FG_ERR_CAPACITY
+    assert L.fg_kv_append_q4(FAKE, FAKE, 100, 1, 0, C.byref(kv), None) == fg.FG_ERR_SHAPE
+    bad = kvs(h=256, H=8)                                        # d = 32
+    assert L.fg_kv_append_q4(FAKE, FAKE, 256, 1, 0, C.byref(bad), None) == fg.FG_ERR_SHAPE
+    assert L.fg_decode_attn_q4kv(FAKE, 256, C.byref(kv), 33, 0.1, FAKE, None, 0, None) \
+        == fg.FG_ERR_CAPACITY
+    assert L.fg_decode_attn_q4kv(FAKE, 256, C.byref(kv), 0, 0.1, FAKE, None, 0, None) \
+        == fg.FG_ERR_SHAPE
+    assert L.fg_decode_attn_q4kv(FAKE, 256, C.byref(kv), 4, -1.0, FAKE, None, 0, None) \
+        == fg.FG_ERR_ARG
+    small = kvs(B=1, cap=1024, h=256, H=2)
+    need = L.fg_decode_attn_workspace_bytes(C.byref(small), 1024)
+    assert need > 0                                   # 2 heads: split the sequence
+    assert L.fg_decode_attn_q4kv(FAKE, 256, C.byref(small), 1024, 0.1, FAKE, FAKE, need - 1,
+                                 None) == fg.FG_ERR_WORKSPACE
+    assert L.fg_prefill_attn(FAKE, 2, 16, 4, 32, 0.1, FAKE, None) == fg.FG_ERR_SHAPE
+    assert L.fg_layernorm(FAKE, 4, 100, FAKE, FAKE, 1e-5, FAKE, None) == fg.FG_ERR_SHAPE
+
+
+def test_layer_validation(fg):
+    L = fg.lib
+    dm = fg.fg_dims(256, 4, 64, 1024, 1e-5)
+    lay = fg.fg_layer(q4(256, 768), q4(256, 256), q4(256, 1024), q4(1024, 256),
+                      None, None, None, None, FAKE, FAKE, FAKE, FAKE)
+    kv = kvs(B=4, cap=20, h=256, H=4)
+    wsb = L.fg_layer_workspace_bytes(C.byref(dm), 2, 2, 20)
+    assert wsb > 0
+    pre = lambda g=2, m=2, s=16, ws=FAKE, n=wsb, d=dm, k=kv: L.fg_layer_prefill(
+        C.byref(d), C.byref(lay), C.byref(k), FAKE, FAKE, g, m, s, ws, n, None)
+    assert pre(n=wsb // 4) == fg.FG_ERR_WORKSPACE
+    assert pre(g=3) == fg.FG_ERR_SHAPE                       # kv.B != g*m
+    assert pre(s=21) == fg.FG_ERR_CAPACITY
+    assert pre(d=fg.fg_dims(256, 4, 64, 1000, 1e-5)) == fg.FG_ERR_SHAPE
+    assert pre(d=fg.fg_dims(256, 2, 128, 1024, 1e-5)) == fg.FG_ERR_SHAPE   # kv.H mismatch
+    lay_bad = fg.fg_layer(q4(256, 512), q4(256, 256), q4(256, 1024), q4(1024, 256),
+                          None, None, None, None, FAKE, FAKE, FAKE, FAKE)
+    assert L.fg_layer_prefill(C.byref(dm), C.byref(lay_bad), C.byref(kv), FAKE, FAKE, 2, 2, 16,
+                              FAKE, wsb, None) == fg.FG_ERR_SHAPE
+    assert L.fg_layer_decode(C.byref(dm), C.byref(lay), C.byref(kv), FAKE, FAKE, 2, 2, 20,
+                             FAKE, wsb, None) == fg.FG_ERR_CAPACITY
+
+
+def test_workspace_sizes_monotone(fg):
+    L = fg.lib
+    dm = fg.fg_dims(4096, 32, 128, 16384, 1e-5)
+    a = L.fg_layer_workspace_bytes(C.byref(dm), 16, 4, 512)
+    b = L.fg_layer_workspace_bytes(C.byref(dm), 16, 4, 544)
+    assert 0 < a <= b
+    # prefill buffers of one GPU batch: LN, QKV, attention, h1 and the FFN activation
+    assert a >= 16 * 512 * (4096 * 6 + 16384) * 2

@@ -1,0 +1,296 @@
+"""Kernel-level parity of libfg against the CPU oracle, through the C ABI.
+
+Integer outputs (codes, group statistics) must be bit-exact; floating outputs must meet
+max |err| <= 2e-2 * max |ref| + 1e-3.  Cases span several tiles, ragged tails, the
+degenerate sizes and, on sampled rows / sequences, the full workload sizes.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fg_synth
+from oracle import layer as OL
+from oracle import quant as OQ
+from parity_util import assert_close, cache_codes_to_rows, dev, f16, host, lib, rows_to_cache
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fg():
+    return lib()
+
+
+def gpu_quantize(fg, x16):
+    x = dev(x16)
+    R, Cc = x16.shape
+    codes = torch.empty((R, Cc // 2), dtype=torch.uint8, device="cuda")
+    ab = torch.empty((R, Cc // 64), dtype=torch.int32, device="cuda")
+    fg.fg_quantize_g64(x, codes, ab)
+    return codes, ab
+
+
+def oracle_packed(x16):
+    q, a, b = OQ.quantize_g64(x16)
+    return OQ.pack_nibbles(q), OQ.ab_pack_u32(a, b)
+
+
+# ----------------------------------------------------------------------------- quantise
+
+
+@pytest.mark.parametrize("shape,scale", [((1, 64), 1.0), ((7, 192), 0.02), ((300, 4160), 3.0),
+                                         ((1025, 128), 1e-4), ((33, 64 * 37), 100.0)])
+def test_quantize_bit_exact(fg, shape, scale):
+    x16 = fg_synth.random_fp16(shape, seed=shape[0] * 7 + shape[1], scale=scale, offset=scale / 3)
+    codes, ab = gpu_quantize(fg, x16)
+    c_ref, ab_ref = oracle_packed(x16)
+    assert np.array_equal(host(codes), c_ref)
+    assert np.array_equal(host(ab).view(np.uint32), ab_ref)
+
+
+def test_quantize_adversarial_groups(fg):
+    x16 = fg_synth.adversarial_groups_fp16()
+    codes, ab = gpu_quantize(fg, x16)
+    c_ref, ab_ref = oracle_packed(x16)
+    assert np.array_equal(host(codes), c_ref)
+    assert np.array_equal(host(ab).view(np.uint32), ab_ref)
+
+
+def test_quantize_empty_is_noop(fg):
+    codes = torch.full((4, 32), 7, dtype=torch.uint8, device="cuda")
+    ab = torch.zeros((4, 1), dtype=torch.int32, device="cuda")
+    fg.fg_quantize_g64(torch.empty((0, 64), dtype=torch.float16, device="cuda"), codes, ab)
+    torch.cuda.synchronize()
+    assert int(codes.min()) == 7
+
+
+@pytest.mark.parametrize("wl_name,which", [("opt-30b", "w1"), ("opt-175b", "w1")])
+def test_quantize_full_size_sampled_rows(fg, wl_name, which):
+    """A full weight of the workload (30B: with outlier input channels), quantised on the
+    device; sampled rows checked bit-exact against the oracle."""
+    wl = fg_synth.WORKLOADS[wl_name]
+    w = fg_synth.weight_fp16(wl.h, wl.f, wl, 0, fg_synth.T_W1)
+    codes, ab = gpu_quantize(fg, w)
+    rows = np.unique(np.r_[0, wl.h - 1, np.random.Generator(np.random.PCG64(1)).integers(
+        0, wl.h, 30)])
+    c_ref, ab_ref = oracle_packed(w[rows])
+    assert np.array_equal(host(codes[torch.from_numpy(rows).cuda()]), c_ref)
+    assert np.array_equal(host(ab[torch.from_numpy(rows).cuda()]).view(np.uint32), ab_ref)
+
+
+def test_dequant_bit_exact(fg):
+    x16 = np.concatenate([fg_synth.random_fp16((40, 256), 5, 2.0),
+                          fg_synth.adversarial_groups_fp16().reshape(4, 256)])
+    codes, ab = gpu_quantize(fg, x16)
+    y = torch.empty(x16.shape, dtype=torch.float16, device="cuda")
+    fg.fg_dequant_g64(codes, ab, x16.shape[0], x16.shape[1], y)
+    q, a, b = OQ.quantize_g64(x16)
+    ref = OQ.dequant_g64(q, a, b)
+    assert np.array_equal(host(y).view(np.uint16), ref.view(np.uint16))
+
+
+# ----------------------------------------------------------------------------- KV append
+
+
+@pytest.mark.parametrize("B,T,pos,h,H,cap", [(3, 5, 2, 256, 4, 9), (2, 1, 15, 512, 4, 16),
+                                              (4, 33, 0, 1024, 8, 40)])
+def test_kv_append_bit_exact(fg, B, T, pos, h, H, cap):
+    qkv16 = fg_synth.random_fp16((B * T, 3 * h), seed=B * 100 + T, scale=2.0)
+    qkv = dev(qkv16)
+    cache = fg.KVCacheQ4(B, cap, h, H)
+    fg.fg_kv_append_q4(qkv[:, h:], qkv[:, 2 * h:], 3 * h, T, pos, cache)
+    for src, codes_t, ab_t in ((qkv16[:, h:2 * h], cache.k_codes, cache.k_ab),
+                               (qkv16[:, 2 * h:], cache.v_codes, cache.v_ab)):
+        c_ref, ab_ref = oracle_packed(np.ascontiguousarray(src))
+        got_c = cache_codes_to_rows(host(codes_t))
+        got_ab = cache_codes_to_rows(host(ab_t)).view(np.uint32)
+        assert np.array_equal(got_c[:, pos:pos + T].reshape(B * T, h // 2), c_ref)
+        assert np.array_equal(got_ab[:, pos:pos + T].reshape(B * T, h // 64), ab_ref)
+        untouched = np.ones(cap, bool)
+        untouched[pos:pos + T] = False
+        assert not got_c[:, untouched].any() and not got_ab[:, untouched].any()
+
+
+# ----------------------------------------------------------------------------- LayerNorm
+
+
+@pytest.mark.parametrize("rows,h", [(1, 256), (37, 4096), (5, 7168), (3, 12288), (2, 16384)])
+def test_layernorm(fg, rows, h):
+    x16 = fg_synth.random_fp16((rows, h), seed=rows + h, scale=3.0, offset=1.0)
+    g16 = fg_synth.random_fp16((h,), seed=h + 1, scale=0.1, offset=1.0)
+    b16 = fg_synth.random_fp16((h,), seed=h + 2, scale=0.1)
+    y = torch.empty((rows, h), dtype=torch.float16, device="cuda")
+    fg.fg_layernorm(dev(x16), dev(g16), dev(b16), 1e-5, y)
+    ref = OL.layernorm(x16, g16, b16, 1e-5)
+    assert_close(f16(y), ref, f"layernorm {rows}x{h}")
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+
+def gemm_case(fg, M, K, N, epi, with_bias, seed, alias=False):
+    x16 = fg_synth.random_fp16((M, K), seed, 1.0)
+    w16 = fg_synth.random_fp16((K, N), seed + 1, 0.02)
+    bias16 = fg_synth.random_fp16((N,), seed + 2, 0.1) if with_bias else None
+    res16 = fg_synth.random_fp16((M, N), seed + 3, 1.0) if epi == 2 else None
+    W = fg.Q4Weight.from_fp16(dev(w16))
+    # the device quantiser is bit-exact with the oracle (checked above); re-check here
+    c_ref, ab_ref = oracle_packed(w16)
+    assert np.array_equal(host(W.codes), c_ref)
+    X = dev(x16)
+    bias = dev(bias16) if with_bias else None
+    res = dev(res16) if res16 is not None else None
+    Y = res if alias else torch.empty((M, N), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+    fg.fg_dequant_gemm_q4(X, W, bias, epi, res, Y, ws)
+    fg.fg_check_device_error()
+    q, a, b = OQ.quantize_g64(w16)
+    what = OQ.dequant_g64(q, a, b).astype(np.float64)
+    ref = x16.astype(np.float64) @ what
+    if with_bias:
+        ref += bias16.astype(np.float64)
+    if epi == 1:
+        ref = np.maximum(ref, 0)
+    elif epi == 2:
+        ref += res16.astype(np.float64)
+    got = f16(Y)
+    assert_close(got, ref, f"gemm M={M} K={K} N={N} epi={epi}")
+    # a tighter statistical check: relative RMS error at fp16 output precision
+    rms = np.sqrt(np.mean((got - ref) ** 2)) / max(np.sqrt(np.mean(ref ** 2)), 1e-30)
+    assert rms < 3e-3, f"relative rms error {rms:.3g}"
+    return wsb
+
+
+@pytest.mark.parametrize("M,K,N,epi,bias", [
+    (1, 64, 256, 0, False),         # single row, single tile
+    (4, 256, 768, 0, True),         # tiny decode QKV (split K)
+    (32, 256, 1024, 1, True),       # tiny prefill FC1
+    (200, 1024, 320, 2, True),      # ragged M, N tail of 64
+    (130, 80, 512, 0, False),       # K ragged inside a 64-block
+    (300, 512, 2048, 1, False),     # several m tiles in one raster group
+    (1100, 256, 256, 0, True),      # 9 m tiles (two raster groups)
+])
+def test_gemm_small(fg, M, K, N, epi, bias):
+    gemm_case(fg, M, K, N, epi, bias, seed=M * 31 + K + N)
+
+
+def test_gemm_split_k(fg):
+    wsb = gemm_case(fg, 64, 4096, 512, 2, True, seed=77)
+    assert wsb > 0                                        # the split-K path ran
+
+
+def test_gemm_inplace_residual(fg):
+    gemm_case(fg, 96, 512, 768, 2, True, seed=91, alias=True)
+
+
+@pytest.mark.parametrize("M,K,N,epi", [
+    (8192, 4096, 12288, 0),        # 6.7B prefill QKV, one GPU batch (g*s = 16*512)
+    (64, 4096, 16384, 1),          # 6.7B decode FC1 (M = B)
+    (144, 28672, 7168, 2),         # 30B decode FC2
+    (18432, 12288, 4096, 0),       # 175B prefill, one GPU batch, N reduced to 4096
+])
+def test_gemm_full_size_sampled(fg, M, K, N, epi):
+    """Workload-sized launches; the oracle computes sampled rows only."""
+    seed = M + K + N
+    x16 = fg_synth.random_fp16((M, K), seed, 1.0)
+    w16 = fg_synth.random_fp16((K, N), seed + 1, 0.02)
+    res16 = fg_synth.random_fp16((M, N), seed + 3, 1.0) if epi == 2 else None
+    W = fg.Q4Weight.from_fp16(dev(w16))
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    res = dev(res16) if res16 is not None else None
+    fg.fg_dequant_gemm_q4(dev(x16), W, None, epi, res, Y, ws)
+    fg.fg_check_device_error()
+    rows = np.unique(np.r_[0, M - 1, np.random.Generator(np.random.PCG64(seed)).integers(0, M, 6)])
+    q, a, b = OQ.quantize_g64(w16)
+    what = OQ.dequant_g64(q, a, b).astype(np.float32)
+    ref = (x16[rows].astype(np.float32) @ what).astype(np.float64)
+    if epi == 1:
+        ref = np.maximum(ref, 0)
+    elif epi == 2:
+        ref += res16[rows].astype(np.float64)
+    got = f16(Y[torch.from_numpy(rows).cuda()])
+    assert_close(got, ref, f"gemm full M={M} K={K} N={N}")
+
+
+# ----------------------------------------------------------------------------- decode attention
+
+
+def oracle_cache_from_rows(fg, k16, v16, cap, H):
+    """Quantise K/V rows [B][T][h] with the oracle and place the codes in a device cache."""
+    B, T, h = k16.shape
+    cache = fg.KVCacheQ4(B, cap, h, H)
+    hats = []
+    for src, codes_t, ab_t in ((k16, cache.k_codes, cache.k_ab), (v16, cache.v_codes, cache.v_ab)):
+        q, a, b = OQ.quantize_g64(src.reshape(B * T, h))
+        codes = OQ.pack_nibbles(q).reshape(B, T, h // 2)
+        abw = OQ.ab_pack_u32(a, b).reshape(B, T, h // 64).view(np.int32)
+        codes_t[:, :, :T] = dev(rows_to_cache(codes, H))
+        ab_t[:, :, :T] = dev(rows_to_cache(abw, H))
+        hats.append(OQ.dequant_g64(q, a, b).reshape(B, T, h))
+    return cache, hats[0], hats[1]
+
+
+@pytest.mark.parametrize("B,H,d,T,length,stride3", [
+    (3, 4, 128, 100, 1, False), (3, 4, 128, 100, 17, True), (3, 4, 128, 100, 100, False),
+    (2, 4, 64, 40, 37, True), (1, 2, 128, 600, 600, False), (64, 32, 128, 530, 530, True)])
+def test_decode_attention(fg, B, H, d, T, length, stride3):
+    h = H * d
+    k16 = fg_synth.random_fp16((B, T, h), seed=B * 1000 + T, scale=1.5)
+    v16 = fg_synth.random_fp16((B, T, h), seed=B * 1000 + T + 1, scale=1.0, offset=0.2)
+    cache, khat, vhat = oracle_cache_from_rows(fg, k16, v16, T + 3, H)
+    qbuf16 = fg_synth.random_fp16((B, 3 * h if stride3 else h), seed=T + 5, scale=1.5)
+    q16 = qbuf16[:, :h]
+    out = torch.empty((B, h), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_decode_attn_workspace_bytes(cache, length)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    scale = 1.0 / math.sqrt(d)
+    fg.fg_decode_attn_q4kv(dev(qbuf16), qbuf16.shape[1], cache, length, scale, out, ws)
+    ref = OL.decode_attention(q16, khat[:, :length], vhat[:, :length], H, d)
+    assert_close(f16(out), ref, f"decode attn B={B} H={H} d={d} len={length}")
+
+
+def test_decode_attention_full_kv_workload_sampled(fg):
+    """The KV-dominated workload's cache (512 sequences x 56 heads x 1056 positions) filled
+    with seeded random codes on the device; two sequences checked against the oracle."""
+    wl = fg_synth.WORKLOADS["kv-decode"]
+    B, H, d, cap = wl.B, wl.H, wl.d, wl.cap
+    kc, vc, ka, va = fg_synth.random_q4_cache_torch(B, H, cap, d, seed=4)
+    cache = fg.KVCacheQ4.__new__(fg.KVCacheQ4)
+    cache.B, cache.cap, cache.h, cache.H, cache.d = B, cap, wl.h, H, d
+    cache.k_codes, cache.v_codes, cache.k_ab, cache.v_ab = kc, vc, ka, va
+    q16 = fg_synth.random_fp16((B, wl.h), seed=44, scale=1.5)
+    out = torch.empty((B, wl.h), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_decode_attn_workspace_bytes(cache, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    fg.fg_decode_attn_q4kv(dev(q16), wl.h, cache, cap, 1.0 / math.sqrt(d), out, ws)
+    for b in (0, B - 1):
+        hats = []
+        for codes_t, ab_t in ((kc, ka), (vc, va)):
+            codes = cache_codes_to_rows(host(codes_t[b:b + 1]))[0]          # [cap][h/2]
+            abw = cache_codes_to_rows(host(ab_t[b:b + 1]))[0].view(np.uint32)
+            q = OQ.unpack_nibbles(codes)
+            a = (abw & 0xFFFF).astype(np.uint16).view(np.float16)
+            bb = (abw >> 16).astype(np.uint16).view(np.float16)
+            hats.append(OQ.dequant_g64(q, a, bb))
+        ref = OL.decode_attention(q16[b:b + 1], hats[0][None], hats[1][None], H, d)
+        assert_close(f16(out[b:b + 1]), ref, f"kv workload seq {b}")
+
+
+# ----------------------------------------------------------------------------- prefill attention
+
+
+@pytest.mark.parametrize("nseq,s,H,d", [(2, 16, 4, 64), (3, 100, 2, 128), (1, 513, 2, 128),
+                                        (2, 64, 3, 64), (1, 1, 2, 128)])
+def test_prefill_attention(fg, nseq, s, H, d):
+    h = H * d
+    qkv16 = fg_synth.random_fp16((nseq * s, 3 * h), seed=nseq * 10 + s, scale=1.5)
+    out = torch.empty((nseq * s, h), dtype=torch.float16, device="cuda")
+    fg.fg_prefill_attn(dev(qkv16), nseq, s, H, d, 1.0 / math.sqrt(d), out)
+    x = qkv16.reshape(nseq, s, 3 * h)
+    ref = OL.causal_attention(x[..., :h], x[..., h:2 * h], x[..., 2 * h:], H, d)
+    assert_close(f16(out).reshape(nseq, s, h), ref, f"prefill attn {nseq}x{s} H={H} d={d}")
