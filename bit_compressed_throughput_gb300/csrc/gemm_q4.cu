@@ -14,8 +14,8 @@
 //   warps 2-5  restore codes -> fp16 B tile in shared memory (MN-major, 128B swizzle: one
 //              k-row of 64 output channels = one 128-byte swizzle row = one group), then
 //              run the epilogue: tcgen05.ld, bias / ReLU / residual, fp16 store
-// Restoration per pair of codes: the nibble is OR-ed into the mantissa of 1.0h so that
-// the half equals 1 + q/4, then one HFMA2 gives (1 + q/4)*(4s) + (a - 4s) = a + q*s.
+// Restoration per pair of codes: the nibble is OR-ed into mantissa bits 6..9 of 1.0h so
+// that the half equals 1 + q/16, then one HFMA2 gives (1 + q/16)*(16s) + (a - 16s) = a + q*s.
 // Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7); the epilogue
 // undoes that order when it packs the accumulator columns back to fp16.
 //
@@ -146,12 +146,12 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t x, uint32_t s, uint32_t c
 }
 
 // Restore 8 codes (one word) of one group to 4 half2 in (n0,n4),(n1,n5),(n2,n6),(n3,n7).
-__device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s4, uint32_t c) {
+__device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s16, uint32_t c) {
   uint4 o;
-  o.x = hfma2_u32(((w << 8) & 0x0F000F00u) | 0x3C003C00u, s4, c);
-  o.y = hfma2_u32(((w << 4) & 0x0F000F00u) | 0x3C003C00u, s4, c);
-  o.z = hfma2_u32((w & 0x0F000F00u) | 0x3C003C00u, s4, c);
-  o.w = hfma2_u32(((w >> 4) & 0x0F000F00u) | 0x3C003C00u, s4, c);
+  o.x = hfma2_u32(((w << 6) & 0x03C003C0u) | 0x3C003C00u, s16, c);
+  o.y = hfma2_u32(((w << 2) & 0x03C003C0u) | 0x3C003C00u, s16, c);
+  o.z = hfma2_u32(((w >> 2) & 0x03C003C0u) | 0x3C003C00u, s16, c);
+  o.w = hfma2_u32(((w >> 6) & 0x03C003C0u) | 0x3C003C00u, s16, c);
   return o;
 }
 
@@ -329,16 +329,16 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int sw = k & 7;
         const uint4 cw = *reinterpret_cast<const uint4*>(cs + k * 128 + ((c ^ sw) << 4));
         const float2 abf = unpack_h2(abw[it]);
-        const float sc4 = (abf.y - abf.x) * (4.0f / 15.0f);
-        const uint32_t s4 = pack_h2(sc4, sc4);
-        const float cf = abf.x - sc4;
+        const float sc16 = (abf.y - abf.x) * (16.0f / 15.0f);
+        const uint32_t s16 = pack_h2(sc16, sc16);
+        const float cf = abf.x - sc16;
         const uint32_t cc = pack_h2(cf, cf);
         uint8_t* brow = bs + (c >> 1) * (BK * 128) + k * 128;
         const int jc0 = (c & 1) * 4;
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s4, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s4, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s4, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s4, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s16, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s16, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s16, cc);
+        *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s16, cc);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(full_b(s));

@@ -23,7 +23,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float t = (l < kThreads / 32) ? red[l] : 0.0f;
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
   return t;                           // every lane of every warp holds the total
 }
 
