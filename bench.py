@@ -37,6 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import fg_synth  # noqa: E402
+from bit_compressed_throughput_gb300 import replicas  # noqa: E402
 
 METRIC = "generated tokens/s per OPT-shaped layer stack at 1 GB300; decode-attn HBM GB/s % peak"
 UNIT = "tokens/s"
@@ -191,13 +192,7 @@ def time_region(fn, steps, dist=None):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        import torch.distributed as D
-        t = torch.tensor([ms], device="cuda")
-        D.all_reduce(t, op=D.ReduceOp.MAX)
-        ms = float(t.item())
-    return ms
+    return replicas.max_over_ranks(e0.elapsed_time(e1), dist, device="cuda")
 
 
 def run_gpu(args, wl):
@@ -270,7 +265,7 @@ def run_gpu(args, wl):
     a_ = prof["q4kv_decode_attn"]
     attn_gbs = a_["work"] / (a_["ms"] * 1e-3) / 1e9 if a_["ms"] else None
     total_kernel_ms = sum(p["ms"] for p in prof.values())
-    value = world * tokens_per_step * args.steps / (ms * 1e-3)
+    value = replicas.total_tokens(world, wl.B, wl.n, args.steps) / (ms * 1e-3)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
@@ -300,7 +295,8 @@ def run_gpu(args, wl):
                     for k, v in prof.items() if v["launches"]},
         "eager_ms_per_step": round(ms_eager / args.steps, 3),
         "gpu_launches": launches,
-        "e2e": {"value": round(world * tokens_per_step * args.steps / (ms_e2e * 1e-3), 2),
+        "e2e": {"value": round(replicas.total_tokens(world, wl.B, wl.n, args.steps)
+                               / (ms_e2e * 1e-3), 2),
                 "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
     }
