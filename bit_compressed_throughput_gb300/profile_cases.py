@@ -1,0 +1,83 @@
+"""Single-kernel cases for profiler captures: one warm-up launch, then `--reps` launches of
+one hot-path kernel at a workload's shape, inputs larger than L2 and a few GB at most.
+
+    python -m bit_compressed_throughput_gb300.profile_cases gemm-fc1-opt67b
+    python -m bit_compressed_throughput_gb300.profile_cases decode-attn-opt67b
+    python -m bit_compressed_throughput_gb300.profile_cases decode-attn-kv
+
+Inputs are seeded random device tensors (no parity check here; the tests do that).
+"""
+from __future__ import annotations
+
+import argparse
+import math
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def gemm_case(M, K, N, epi, reps):
+    import torch
+    from bit_compressed_throughput_gb300 import fg
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    X = torch.randn((M, K), generator=g, device="cuda").half()
+    W = fg.Q4Weight.from_fp16((torch.randn((K, N), generator=g, device="cuda") * 0.02).half())
+    bias = torch.zeros(N, dtype=torch.float16, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    for _ in range(1 + reps):
+        fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
+    fg.fg_check_device_error()
+
+
+def attn_case(B, H, d, length, reps):
+    import torch
+    import fg_synth
+    from bit_compressed_throughput_gb300 import fg
+    kc, vc, ka, va = fg_synth.random_q4_cache_torch(B, H, length, d, seed=3)
+    cache = fg.KVCacheQ4.__new__(fg.KVCacheQ4)
+    cache.B, cache.cap, cache.h, cache.H, cache.d = B, length, H * d, H, d
+    cache.k_codes, cache.v_codes, cache.k_ab, cache.v_ab = kc, vc, ka, va
+    q = torch.randn((B, H * d), device="cuda").half()
+    out = torch.empty_like(q)
+    wsb = fg.fg_decode_attn_workspace_bytes(cache, length)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    for _ in range(1 + reps):
+        fg.fg_decode_attn_q4kv(q, H * d, cache, length, 1.0 / math.sqrt(d), out, ws)
+    torch.cuda.synchronize()
+
+
+CASES = {
+    # 6.7B prefill FC1 of one GPU batch: M = 16*512, K = 4096, N = 16384, ReLU
+    "gemm-fc1-opt67b": lambda r: gemm_case(8192, 4096, 16384, 1, r),
+    # 6.7B prefill QKV: N = 3*4096
+    "gemm-qkv-opt67b": lambda r: gemm_case(8192, 4096, 12288, 0, r),
+    # 6.7B decode FC1 (M = B = 64, split K)
+    "gemm-fc1-decode-opt67b": lambda r: gemm_case(64, 4096, 16384, 1, r),
+    # 6.7B decode attention at the last step: 64 sequences x 32 heads x 543 positions
+    "decode-attn-opt67b": lambda r: attn_case(64, 32, 128, 543, r),
+    # KV-dominated workload: 512 sequences x 56 heads x 1056 positions (4.3 GB of cache)
+    "decode-attn-kv": lambda r: attn_case(512, 56, 128, 1056, r),
+}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=2)
+    a = ap.parse_args()
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    CASES[a.case](a.reps)
+    torch.cuda.synchronize()
+    print(f"{a.case}: ok")
+
+
+if __name__ == "__main__":
+    main()
