@@ -277,6 +277,9 @@ LayerWs layer_ws(const fg_dims& dm, int64_t M, const fg_kvcache* kv_for_decode, 
 }
 
 }  // namespace
+
+void set_last_error(const std::string& msg) { t_last_error = msg; }
+
 }  // namespace fg
 
 using namespace fg;

@@ -4,6 +4,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "../../include/fg.h"
 
 namespace fg {
@@ -19,6 +21,9 @@ cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const u
                              const uint16_t* b, float eps, uint16_t* y, cudaStream_t st);
 cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
                                 int32_t d, float scale, uint16_t* out, cudaStream_t st);
+
+// Message returned by fg_last_error() on this thread.
+void set_last_error(const std::string& msg);
 
 // Decode attention: number of sequence splits used for (kv, len); workspace bytes.
 int decode_attn_splits(const fg_kvcache& kv, int32_t len, int num_sms);

@@ -61,6 +61,7 @@ _SIGS = {
     "fg_decode_attn_q4kv": ([_P, _I64, C.POINTER(fg_kvcache), _I32, _F, _P, _P, _SZ, _P],
                             C.c_int),
     "fg_decode_attn_workspace_bytes": ([C.POINTER(fg_kvcache), _I32], _SZ),
+    "fg_decode_attn_q4kv_static": ([_P, _I64, C.POINTER(fg_kvcache), _I32, _F, _P, _P], C.c_int),
     "fg_prefill_attn": ([_P, _I32, _I32, _I32, _I32, _F, _P, _P], C.c_int),
     "fg_layernorm": ([_P, _I64, _I32, _P, _P, _F, _P, _P], C.c_int),
     "fg_layer_prefill": ([C.POINTER(fg_dims), C.POINTER(fg_layer), C.POINTER(fg_kvcache), _P, _P,
@@ -232,6 +233,19 @@ def fg_decode_attn_q4kv(q, q_stride: int, cache: KVCacheQ4, length: int, scale: 
     _check("fg_decode_attn_q4kv",
            lib.fg_decode_attn_q4kv(_ptr(q), q_stride, C.byref(st), length, scale, _ptr(out),
                                    _ptr(ws), wsb, _stream(stream)))
+
+
+DECODE_ATTN_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def fg_decode_attn_q4kv_static(q, q_stride: int, cache: KVCacheQ4, length: int, scale: float,
+                               out, stream=None):
+    """Decode attention for callers that cannot allocate: the split scratch is the
+    library's own static device array (4 MiB), so no workspace is passed."""
+    st = cache.struct()
+    _check("fg_decode_attn_q4kv_static",
+           lib.fg_decode_attn_q4kv_static(_ptr(q), q_stride, C.byref(st), length, scale,
+                                          _ptr(out), _stream(stream)))
 
 
 def fg_prefill_attn(qkv, nseq: int, s: int, H: int, d: int, scale: float, out, stream=None):

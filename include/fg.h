@@ -162,6 +162,23 @@ int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* k
                         float scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len);
 
+/* Decode attention exactly as fg_decode_attn_q4kv, for callers that cannot allocate
+ * device memory -- code that must not call cudaMalloc (a region that forbids allocation,
+ * an external allocator that owns all device memory, a host runtime that can only pass
+ * existing buffers through) and so cannot supply the split-sequence workspace.  Its
+ * scratch is a fixed array of FG_DECODE_ATTN_STATIC_SCRATCH_BYTES in device global
+ * memory defined by the library itself (held on every GPU that loads the library until
+ * the process exits); the call allocates nothing.  The caller still passes q, the cache
+ * and out.  A call whose split scratch (fg_decode_attn_workspace_bytes) would exceed the
+ * array returns FG_ERR_WORKSPACE without launching, and fg_last_error() says so.
+ * The first call on a device looks up the array's device address for that device; make
+ * that first call before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU race on it.  No part of it needs to start at zero; each call writes
+ * every byte it reads.  The paper has no counterpart of this entry point. */
+#define FG_DECODE_ATTN_STATIC_SCRATCH_BYTES (4u << 20)
+int fg_decode_attn_q4kv_static(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv,
+                               int32_t len, float scale, uint16_t* out, void* stream);
+
 /* Causal prefill attention over fp16 Q/K/V read from a QKV buffer qkv[nseq*s][3h]
  * (columns q | k | v, head hd at hd*d): out[nseq*s][h] fp16, position i attends over
  * positions 0..i of its own sequence, scores scaled by `scale`.  d in {64, 128}.
