@@ -147,7 +147,8 @@ void prof_drain_locked() {
 int check_q4mat(const fg_q4mat* W) {
   if (!W || !W->codes || !W->ab) return FG_ERR_ARG;
   if (!aligned16(W->codes) || !aligned16(W->ab)) return FG_ERR_ARG;
-  if (W->K <= 0 || W->K % 16 != 0 || W->N <= 0 || W->N % 64 != 0) return FG_ERR_SHAPE;
+  // N % 256: the group statistics of one 256-column tile are one 16-byte TMA row
+  if (W->K <= 0 || W->K % 16 != 0 || W->N <= 0 || W->N % 256 != 0) return FG_ERR_SHAPE;
   if (W->K > (1ll << 31) - 1 || W->N > (1ll << 31) - 1) return FG_ERR_SHAPE;
   return FG_OK;
 }
@@ -167,8 +168,8 @@ int check_kv(const fg_kvcache* kv) {
 
 int check_dims(const fg_dims* dm) {
   if (!dm) return FG_ERR_ARG;
-  if (dm->h <= 0 || dm->h % 64 != 0 || dm->h > 16384 || dm->H <= 0 || dm->h != dm->H * dm->d ||
-      (dm->d != 64 && dm->d != 128) || dm->f < 0 || dm->f % 64 != 0 || !(dm->ln_eps > 0.0f))
+  if (dm->h <= 0 || dm->h % 256 != 0 || dm->h > 16384 || dm->H <= 0 || dm->h != dm->H * dm->d ||
+      (dm->d != 64 && dm->d != 128) || dm->f < 0 || dm->f % 256 != 0 || !(dm->ln_eps > 0.0f))
     return FG_ERR_SHAPE;
   return FG_OK;
 }

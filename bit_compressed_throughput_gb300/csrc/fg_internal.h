@@ -39,6 +39,8 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
 struct GemmPlan {
   int64_t M, N, K;
   int tiles_m, tiles_n, kblocks, splits, kb_per_split;
+  int64_t units;   // (split, tile) work units
+  int grid;        // persistent CTAs: min(units, SMs)
   size_t ws_bytes;
 };
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms);

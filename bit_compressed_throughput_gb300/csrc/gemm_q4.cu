@@ -6,21 +6,27 @@
 // matmul].  The block schedule's batch reuse makes the projections and the MLP dense
 // contractions over M = g*s (prefill) or M = B (decode) rows.
 //
-// CTA tile 128 x 256, K step 64, 3-stage ring, 6 warps:
-//   warp 0     TMA producer (X tile, 128B swizzle, K-major; packed code tile, 128B
-//              swizzle) + TMEM allocation
-//   warp 1     one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into a
-//              128 x 256 fp32 accumulator in TMEM and commits to mbarriers
-//   warps 2-5  restore codes -> fp16 B tile in shared memory (MN-major, 128B swizzle: one
-//              k-row of 64 output channels = one 128-byte swizzle row = one group), then
-//              run the epilogue: tcgen05.ld, bias / ReLU / residual, fp16 store
+// Persistent kernel: one CTA per SM loops over output tiles 128 x 256 (K step 64).
+//   warp 0      TMA producer: X tile (128B swizzle, K-major), packed code tile (128B
+//               swizzle) and the tile's group statistics, one transaction per stage, into a
+//               6-deep ring; owns the TMEM allocation (512 columns)
+//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into one of
+//               two double-buffered 128 x 256 fp32 accumulators and commits to mbarriers
+//   warps 2-9   restore codes -> fp16 B tile in a 2-deep shared-memory ring (MN-major,
+//               128B swizzle: one k-row of 64 output channels = one 128-byte swizzle row =
+//               one group); two restore warps per SM sub-partition hide each other's
+//               latency
+//   warps 10-13 epilogue of the previous tile (tcgen05.ld, bias / ReLU / residual, fp16
+//               store) while the other accumulator fills
+// The restore, not the MMA, bounds this kernel: with the restore skipped the same
+// pipeline runs at about 84% of the measured dense fp16 peak.
 // Restoration per pair of codes: the nibble is OR-ed into mantissa bits 6..9 of 1.0h so
 // that the half equals 1 + q/16, then one HFMA2 gives (1 + q/16)*(16s) + (a - 16s) = a + q*s.
 // Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7); the epilogue
 // undoes that order when it packs the accumulator columns back to fp16.
 //
-// Small M (decode) splits K over blockIdx.z; partial fp32 tiles go to the caller's
-// workspace and a reduce kernel applies the epilogue.
+// Small M (decode) also splits K: work units are (split, tile); partial fp32 tiles go to
+// the caller's workspace and a reduce kernel applies the epilogue.
 //
 // Every mbarrier wait is bounded (about 2 s); on timeout the CTA raises an abort flag,
 // sets the device error word, drains its outstanding copies and exits.
@@ -39,20 +45,31 @@ __device__ unsigned int g_gemm_error = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
-constexpr int THREADS = 192;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int UM = 128;                     // rows per MMA
+constexpr int RS = 6;                       // raw ring: X tile + code tile
+constexpr int BS = 2;                       // restored B ring
+constexpr int RW = 8;                       // restore warps
+constexpr int RT = RW * 32;                 // restore threads
+constexpr int EW0 = 2 + RW;                 // first epilogue warp
+constexpr int THREADS = (EW0 + 4) * 32;
+constexpr int ITEMS = BK * BN / 32 / RT;    // 16-byte code chunks per restore thread
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int B_BYTES = BK * BN * 2;        // 32 KB
-constexpr int C_BYTES = BK * BN / 2;        // 8 KB of codes
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int C_BYTES = BK * BN / 2;        // 8 KB of codes (128-byte rows)
+constexpr int S_BYTES = BK * (BN / 64) * 4;  // 1 KB of (a, b) words
+constexpr int SMEM_BYTES = RS * (A_BYTES + C_BYTES + S_BYTES) + BS * B_BYTES +
+                           1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t TMEM_COLS = 2 * (BM / UM) * BN;   // two accumulator buffers
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(TMEM_COLS == 512, "TMEM budget");
+static_assert(ITEMS * RT * 32 == BK * BN, "restore coverage");
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int SWZ_GROUP_M = 8;
 
 // instruction descriptor: D f32, A f16 K-major, B f16 MN-major, N = 256, M = 128
 constexpr uint32_t IDESC = (1u << 4) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+                           ((uint32_t)(UM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -197,50 +214,62 @@ __device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int6
   *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
-gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
-                  const uint32_t* __restrict__ ab, int M, int N, int K, int tiles_m, int tiles_n,
-                  int kblocks, int kb_per_split, EpiArgs ea) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* sA = smem;                                  // STAGES x A_BYTES
-  uint8_t* sB = smem + STAGES * A_BYTES;               // STAGES x B_BYTES
-  uint8_t* sC = sB + STAGES * B_BYTES;                 // STAGES x C_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + STAGES * C_BYTES);
-  // bars: full_raw[S], full_b[S], empty[S], acc_full
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- tile coordinates (grouped raster: SWZ_GROUP_M m-tiles share a wave of n-tiles)
-  const int lin = blockIdx.x;
+__device__ __forceinline__ void unit_coords(int u, int tiles_m, int tiles_n, int kblocks,
+                                            int kb_per_split, int& m0, int& n0, int& split,
+                                            int& kb_begin, int& kb_end) {
+  const int tiles = tiles_m * tiles_n;
+  split = u / tiles;
+  const int lin = u - split * tiles;
+  // grouped raster: SWZ_GROUP_M m-tiles share a wave of n-tiles
   const int group_span = SWZ_GROUP_M * tiles_n;
   const int grp = lin / group_span;
   const int first_m = grp * SWZ_GROUP_M;
   const int gm = min(SWZ_GROUP_M, tiles_m - first_m);
   const int within = lin - grp * group_span;
-  const int tm = first_m + within % gm;
-  const int tn = within / gm;
-  const int m0 = tm * BM, n0 = tn * BN;
-  const int kb0 = blockIdx.z * kb_per_split;
-  const int kb1 = min(kblocks, kb0 + kb_per_split);
-  const int nkb = max(0, kb1 - kb0);
+  m0 = (first_m + within % gm) * BM;
+  n0 = (within / gm) * BN;
+  kb_begin = split * kb_per_split;
+  kb_end = min(kblocks, kb_begin + kb_per_split);
+}
 
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+                  const __grid_constant__ CUtensorMap tmS, int M, int N, int K, int tiles_m, int tiles_n,
+                  int kblocks, int kb_per_split, int units, EpiArgs ea) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                  // RS x A_BYTES
+  uint8_t* sC = sA + RS * A_BYTES;                     // RS x C_BYTES
+  uint8_t* sB = sC + RS * C_BYTES;                     // BS x B_BYTES
+  uint32_t* sS = reinterpret_cast<uint32_t*>(sB + BS * B_BYTES);    // RS x 256 words
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + BS * B_BYTES + RS * S_BYTES);
+  // bars: full_raw[RS], empty_raw[RS], full_b[BS], empty_b[BS], acc_full[2], acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RS + 2 * BS + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
   auto full_raw = [&](int s) { return bar0 + 8u * s; };
-  auto full_b = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  const uint32_t acc_full = bar0 + 8u * (3 * STAGES);
+  auto empty_raw = [&](int s) { return bar0 + 8u * (RS + s); };
+  auto full_b = [&](int s) { return bar0 + 8u * (2 * RS + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * (2 * RS + BS + s); };
+  auto acc_full = [&](int s) { return bar0 + 8u * (2 * RS + 2 * BS + s); };
+  auto acc_empty = [&](int s) { return bar0 + 8u * (2 * RS + 2 * BS + 2 + s); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < RS; ++s) {
       mbar_init(full_raw(s), 1);
-      mbar_init(full_b(s), 128);
-      mbar_init(empty(s), 1);
+      mbar_init(empty_raw(s), 1);
     }
-    mbar_init(acc_full, 1);
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(full_b(s), RT);                    // every restore thread arrives
+      mbar_init(empty_b(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(acc_full(s), 1);
+      mbar_init(acc_empty(s), 4);                  // one arrival per epilogue warp
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -259,19 +288,27 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        if (i >= STAGES && !mbar_wait(empty(s), ((i / STAGES) & 1) ^ 1, abort_flag)) break;
-        mbar_expect_tx(full_raw(s), A_BYTES + C_BYTES);
-        tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, (kb0 + i) * BK, m0, full_raw(s));
-        tma_load_2d(smem_u32(sC + s * C_BYTES), &tmC, n0 / 2, (kb0 + i) * BK, full_raw(s));
-        issued = i + 1;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int m0, n0, split, kbb, kbe;
+        unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+        for (int kb = kbb; kb < kbe; ++kb, ++it) {
+          const int s = it % RS;
+          if (it >= RS && !mbar_wait(empty_raw(s), ((it / RS) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full_raw(s), A_BYTES + C_BYTES + S_BYTES);
+          tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, kb * BK, m0, full_raw(s));
+          tma_load_2d(smem_u32(sC + s * C_BYTES), &tmC, n0 / 2, kb * BK, full_raw(s));
+          tma_load_2d(smem_u32(sS + s * (S_BYTES / 4)), &tmS, n0 / 64, kb * BK, full_raw(s));
+        }
       }
       // Drain: every issued load must have landed before this CTA can exit.
-      for (int i = max(0, issued - STAGES); i < issued; ++i) {
+      for (int i = max(0, it - RS); i < it; ++i) {
         const long long t0 = clock64();
-        while (!mbar_try(full_raw(i % STAGES), (i / STAGES) & 1)) {
+        while (!mbar_try(full_raw(i % RS), (i / RS) & 1)) {
           if (clock64() - t0 > kWaitCycles) {
             atomicOr(&g_gemm_error, 2u);
             break;
@@ -282,104 +319,166 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(full_raw(s), ph, abort_flag)) break;
-        if (!mbar_wait(full_b(s), ph, abort_flag)) break;
+      int it = 0, tl = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tl) {
+        int m0, n0, split, kbb, kbe;
+        unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+        const int acc = tl & 1;
+        if (tl >= 2 && !mbar_wait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + s * A_BYTES);
-        const uint32_t b_base = smem_u32(sB + s * B_BYTES);
+        const uint32_t tacc = tmem + acc * ((BM / UM) * BN);
+        for (int kb = kbb; kb < kbe; ++kb, ++it) {
+          const int s = it % RS, bs = it % BS;
+          if (!mbar_wait(full_raw(s), (it / RS) & 1, abort_flag) ||
+              !mbar_wait(full_b(bs), (it / BS) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + bs * B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024);
-          const uint64_t bd = smem_desc(b_base + kk * 16 * 128, 64 * 128, 1024);
-          umma_f16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bd = smem_desc(b_base + kk * 16 * 128, 64 * 128, 1024);
+            const uint32_t accum = (kb > kbb || kk > 0) ? 1u : 0u;
+#pragma unroll
+            for (int hh = 0; hh < BM / UM; ++hh) {
+              if (m0 + hh * UM >= M) break;         // rows past M: nothing to compute
+              const uint64_t ad = smem_desc(a_base + hh * (UM * 128) + kk * 32, 16, 1024);
+              umma_f16(tacc + hh * BN, ad, bd, accum);
+            }
+          }
+          umma_commit(empty_raw(s));
+          umma_commit(empty_b(bs));
         }
-        umma_commit(empty(s));
+        umma_commit(acc_full(acc));
       }
-      umma_commit(acc_full);
+    }
+  } else if (warp < EW0) {
+    // ------------------------------------------------------------ restore codes -> B
+    const int tid = threadIdx.x - 64;                 // 0 .. RT-1
+    // items of this thread: k-row and 16-byte code chunk c (32 output channels) of the
+    // 64 x 256 tile; 8 consecutive lanes take 8 consecutive k at one c, which keeps the
+    // swizzled code loads, the statistics loads and the swizzled B stores free of bank
+    // conflicts
+    int ik[ITEMS], ic[ITEMS];
+#pragma unroll
+    for (int t = 0; t < ITEMS; ++t) {
+      const int item = t * RT + tid;
+      ik[t] = (item & 7) | (((item >> 6) & 7) << 3);
+      ic[t] = (item >> 3) & 7;
+    }
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      int m0, n0, split, kbb, kbe;
+      unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+      for (int kb = kbb; kb < kbe; ++kb, ++it) {
+        const int s = it % RS, bs = it % BS;
+        if (!mbar_wait(full_raw(s), (it / RS) & 1, abort_flag) ||
+            (it >= BS && !mbar_wait(empty_b(bs), ((it / BS) & 1) ^ 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* cs = sC + s * C_BYTES;
+        const uint32_t* ss = sS + s * (S_BYTES / 4);
+        uint8_t* bsm = sB + bs * B_BYTES;
+#pragma unroll
+        for (int t = 0; t < ITEMS; ++t) {
+          const int k = ik[t], c = ic[t], sw = k & 7;
+          const uint4 cw = *reinterpret_cast<const uint4*>(cs + k * 128 + ((c ^ sw) << 4));
+          const float2 abf = unpack_h2(ss[k * (BN / 64) + (c >> 1)]);
+          const float sc16 = (abf.y - abf.x) * (16.0f / 15.0f);
+          const uint32_t s16 = pack_h2(sc16, sc16);
+          const float cf = abf.x - sc16;
+          const uint32_t cc = pack_h2(cf, cf);
+          uint8_t* brow = bsm + (c >> 1) * (BK * 128) + k * 128;
+          const int jc0 = (c & 1) * 4;
+          *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s16, cc);
+          *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s16, cc);
+          *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s16, cc);
+          *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s16, cc);
+        }
+        // make the stores visible to the tensor core's (async) proxy, then arrive
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(full_b(bs));
+      }
     }
   } else {
-    // ------------------------------------------------------------ restore + epilogue
-    const int tid = threadIdx.x - 64;                 // 0..127
-    const int gpr = N / 64;                           // groups per weight row
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = (i / STAGES) & 1;
-      const int kbase = (kb0 + i) * BK;
-      // group statistics of this thread's 4 items (plain loads; tiny and L2-resident)
-      uint32_t abw[4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = it * 128 + tid;
-        const int k = (item & 7) | (((item >> 6) & 7) << 3);
-        const int c = (item >> 3) & 7;
-        const int kg = kbase + k, ng = n0 / 64 + (c >> 1);
-        abw[it] = (kg < K && ng < gpr) ? __ldg(ab + (int64_t)kg * gpr + ng) : 0u;
-      }
-      if (!mbar_wait(full_raw(s), ph, abort_flag)) break;
-      const uint8_t* cs = sC + s * C_BYTES;
-      uint8_t* bs = sB + s * B_BYTES;
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = it * 128 + tid;
-        const int k = (item & 7) | (((item >> 6) & 7) << 3);
-        const int c = (item >> 3) & 7;
-        const int sw = k & 7;
-        const uint4 cw = *reinterpret_cast<const uint4*>(cs + k * 128 + ((c ^ sw) << 4));
-        const float2 abf = unpack_h2(abw[it]);
-        const float sc16 = (abf.y - abf.x) * (16.0f / 15.0f);
-        const uint32_t s16 = pack_h2(sc16, sc16);
-        const float cf = abf.x - sc16;
-        const uint32_t cc = pack_h2(cf, cf);
-        uint8_t* brow = bs + (c >> 1) * (BK * 128) + k * 128;
-        const int jc0 = (c & 1) * 4;
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s16, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s16, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s16, cc);
-        *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s16, cc);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(full_b(s));
-    }
-
-    // ---------------------------------------------------------------- epilogue
-    const bool acc_ok = mbar_wait(acc_full, 0, abort_flag);
-    __syncwarp();
-    tc_fence_after();
-    const int lane_base = 32 * (warp & 3);       // TMEM lanes this warp may read
-    const int64_t row = (int64_t)m0 + lane_base + lane;
-    if (acc_ok && nkb > 0) {
+    // ------------------------------------------------------------ epilogue
+    const int lane_base = 32 * (warp & 3);            // TMEM lanes this warp may read
+    int tl = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
+      int m0, n0, split, kbb, kbe;
+      unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+      const int acc = tl & 1;
+      if (!mbar_wait(acc_full(acc), (tl >> 1) & 1, abort_flag)) break;
+      __syncwarp();
+      tc_fence_after();
+      for (int hh = 0; hh < BM / UM; ++hh) {
+      const int64_t row = (int64_t)m0 + hh * UM + lane_base + lane;
+      const bool row_ok = row < M;
       for (int cc = 0; cc < BN / 32; ++cc) {
+        const int nb = n0 + cc * 32;
+        // loads that do not depend on the accumulator go first
+        uint4 bias4[4], res4[4];
+        if (!ea.partial && nb < N) {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            bias4[g8] = ea.bias ? ldg_nc_v4(ea.bias + nb + g8 * 8) : make_uint4(0, 0, 0, 0);
+            res4[g8] = (ea.epi == FG_EPI_RESIDUAL && row_ok)
+                           ? *reinterpret_cast<const uint4*>(ea.residual + row * N + nb + g8 * 8)
+                           : make_uint4(0, 0, 0, 0);
+          }
+        }
         uint32_t r[32];
-        const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + cc * 32;
+        const uint32_t taddr =
+            tmem + ((uint32_t)lane_base << 16) + acc * ((BM / UM) * BN) + hh * BN + cc * 32;
         __syncwarp();
         tmem_ld16(taddr, r);
         tmem_ld16(taddr + 16, r + 16);
         tmem_wait_ld();
-        if (row < M) {
+        if (!row_ok || nb >= N) continue;
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            const int n = n0 + cc * 32 + g8 * 8;
-            if (n < N) {
-              float v[8];
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int n = nb + g8 * 8;
+          float v[8];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                v[i] = __uint_as_float(r[8 * g8 + 2 * i]);
-                v[i + 4] = __uint_as_float(r[8 * g8 + 2 * i + 1]);
-              }
-              if (ea.partial) {
-                float* pp = ea.partial + ((int64_t)blockIdx.z * M + row) * N + n;
-                reinterpret_cast<float4*>(pp)[0] = make_float4(v[0], v[1], v[2], v[3]);
-                reinterpret_cast<float4*>(pp)[1] = make_float4(v[4], v[5], v[6], v[7]);
-              } else {
-                epilogue8(ea, v, row, n, N);
-              }
-            }
+          for (int i = 0; i < 4; ++i) {
+            v[i] = __uint_as_float(r[8 * g8 + 2 * i]);
+            v[i + 4] = __uint_as_float(r[8 * g8 + 2 * i + 1]);
           }
+          if (ea.partial) {
+            float* pp = ea.partial + ((int64_t)split * M + row) * N + n;
+            reinterpret_cast<float4*>(pp)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4*>(pp)[1] = make_float4(v[4], v[5], v[6], v[7]);
+            continue;
+          }
+          const uint32_t bw[4] = {bias4[g8].x, bias4[g8].y, bias4[g8].z, bias4[g8].w};
+          const uint32_t rw[4] = {res4[g8].x, res4[g8].y, res4[g8].z, res4[g8].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 fb = unpack_h2(bw[i]), fr = unpack_h2(rw[i]);
+            v[2 * i] += fb.x + fr.x;
+            v[2 * i + 1] += fb.y + fr.y;
+          }
+          if (ea.epi == FG_EPI_RELU) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = fmaxf(v[i], 0.0f);
+          }
+          uint4 o;
+          o.x = pack_h2(v[0], v[1]);
+          o.y = pack_h2(v[2], v[3]);
+          o.z = pack_h2(v[4], v[5]);
+          o.w = pack_h2(v[6], v[7]);
+          *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
         }
       }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(acc));
     }
   }
 
@@ -427,13 +526,13 @@ cudaError_t get_encode() {
 
 cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                        uint32_t box_outer) {
+                        uint32_t box_outer, CUtensorMapSwizzle swz) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -457,6 +556,8 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
   p.kb_per_split = std::max(1, (p.kblocks + splits - 1) / splits);
   p.splits = std::max(1, (p.kblocks + p.kb_per_split - 1) / p.kb_per_split);
   p.ws_bytes = (p.splits > 1) ? (size_t)p.splits * M * N * sizeof(float) : 0;
+  p.units = tiles * p.splits;
+  p.grid = (int)std::min<int64_t>(p.units, nsm);
   return p;
 }
 
@@ -469,20 +570,23 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   static cudaError_t attr_err = cudaFuncSetAttribute(
       gemm_q4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
-  CUtensorMap tmA, tmC;
+  CUtensorMap tmA, tmC, tmS;
   e = make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K, (uint64_t)p.M,
-                  (uint64_t)p.K * 2, BK, BM);
+                  (uint64_t)p.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(p.N / 2),
-                  (uint64_t)p.K, (uint64_t)(p.N / 2), BN / 2, BK);
+                  (uint64_t)p.K, (uint64_t)(p.N / 2), BN / 2, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT32, W.ab, (uint64_t)(p.N / 64),
+                  (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, BN / 64, BK,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
-  dim3 grid((unsigned)(p.tiles_m * p.tiles_n), 1, (unsigned)p.splits);
-  gemm_q4_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmC, W.ab, (int)p.M, (int)p.N,
-                                                       (int)p.K, p.tiles_m, p.tiles_n, p.kblocks,
-                                                       p.kb_per_split, ea);
+  gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(
+      tmA, tmC, tmS, (int)p.M, (int)p.N, (int)p.K, p.tiles_m, p.tiles_n, p.kblocks,
+      p.kb_per_split, (int)p.units, ea);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   if (mid_event) cudaEventRecord(mid_event, st);

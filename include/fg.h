@@ -85,10 +85,10 @@ typedef struct {
 } fg_kvcache;
 
 typedef struct {
-  int32_t h;      /* hidden size, multiple of 64, at most 16384 */
+  int32_t h;      /* hidden size, multiple of 256, at most 16384 */
   int32_t H;      /* heads */
   int32_t d;      /* head dim, 64 or 128, h == H*d */
-  int32_t f;      /* FFN width, multiple of 64; 0 = attention block without the MLP */
+  int32_t f;      /* FFN width, multiple of 256; 0 = attention block without the MLP */
   float ln_eps;   /* LayerNorm epsilon */
 } fg_dims;
 
@@ -125,7 +125,8 @@ int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64
 /* Y[M][N] = epi(X[M][K] * W^ + bias) with W^ the fp16 restoration of W, fp32 accumulate.
  * epi: FG_EPI_NONE; FG_EPI_RELU (max(.,0)); FG_EPI_RESIDUAL (+ residual[M][N]).
  * X, bias (nullable, [N]), residual (FG_EPI_RESIDUAL only), Y: device fp16, row-major,
- * leading dimensions K (X) and N (Y, residual).  K % 16 == 0, N % 64 == 0, M >= 0.
+ * leading dimensions K (X) and N (Y, residual).  K % 16 == 0, N % 256 == 0 (one output tile
+ * of group statistics is one 16-byte row), M >= 0.
  * Y may alias residual.  ws: device scratch of at least fg_gemm_workspace_bytes(M,K,N)
  * bytes (split-K partial sums when M is small); NULL allowed when that is 0.
  * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": restore to FP16

@@ -61,6 +61,7 @@ def test_gemm_validation(fg):
         L.fg_dequant_gemm_q4(X, M, C.byref(W), bias, epi, res, Y, ws, wsb, None)
     assert call(q4(40, 256)) == fg.FG_ERR_SHAPE                 # K % 16
     assert call(q4(64, 96)) == fg.FG_ERR_SHAPE                  # N % 64
+    assert call(q4(64, 320)) == fg.FG_ERR_SHAPE                 # N % 256
     assert call(q4(64, 256, codes=None)) == fg.FG_ERR_ARG
     assert call(q4(64, 256), epi=3) == fg.FG_ERR_ARG
     assert call(q4(64, 256), epi=fg.FG_EPI_RESIDUAL) == fg.FG_ERR_ARG   # residual missing
@@ -113,6 +114,7 @@ def test_layer_validation(fg):
     assert pre(g=3) == fg.FG_ERR_SHAPE                       # kv.B != g*m
     assert pre(s=21) == fg.FG_ERR_CAPACITY
     assert pre(d=fg.fg_dims(256, 4, 64, 1000, 1e-5)) == fg.FG_ERR_SHAPE
+    assert pre(d=fg.fg_dims(256, 4, 64, 960, 1e-5)) == fg.FG_ERR_SHAPE     # f % 256
     assert pre(d=fg.fg_dims(256, 2, 128, 1024, 1e-5)) == fg.FG_ERR_SHAPE   # kv.H mismatch
     lay_bad = fg.fg_layer(q4(256, 512), q4(256, 256), q4(256, 1024), q4(1024, 256),
                           None, None, None, None, FAKE, FAKE, FAKE, FAKE)

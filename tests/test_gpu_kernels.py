@@ -168,7 +168,7 @@ def gemm_case(fg, M, K, N, epi, with_bias, seed, alias=False):
     (1, 64, 256, 0, False),         # single row, single tile
     (4, 256, 768, 0, True),         # tiny decode QKV (split K)
     (32, 256, 1024, 1, True),       # tiny prefill FC1
-    (200, 1024, 320, 2, True),      # ragged M, N tail of 64
+    (200, 1024, 768, 2, True),      # ragged M, three n tiles
     (130, 80, 512, 0, False),       # K ragged inside a 64-block
     (300, 512, 2048, 1, False),     # several m tiles in one raster group
     (1100, 256, 256, 0, True),      # 9 m tiles (two raster groups)
