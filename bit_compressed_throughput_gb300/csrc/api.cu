@@ -158,8 +158,9 @@ int check_kv(const fg_kvcache* kv) {
   if (!aligned16(kv->k_codes) || !aligned16(kv->v_codes) || !aligned16(kv->k_ab) ||
       !aligned16(kv->v_ab))
     return FG_ERR_ARG;
-  if (kv->B < 0 || kv->cap <= 0 || kv->h <= 0 || kv->H <= 0 || kv->h % 64 != 0 ||
-      kv->h % kv->H != 0)
+  // cap % 16: decode attention streams whole 16-position tiles of a head's region
+  if (kv->B < 0 || kv->cap <= 0 || kv->cap % 16 != 0 || kv->h <= 0 || kv->H <= 0 ||
+      kv->h % 64 != 0 || kv->h % kv->H != 0)
     return FG_ERR_SHAPE;
   const int d = kv->h / kv->H;
   if (d != 64 && d != 128) return FG_ERR_SHAPE;
@@ -306,11 +307,14 @@ const char* fg_last_error(void) { return t_last_error.c_str(); }
 int fg_check_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return set_cuda_error(e);
-  unsigned int flag = 0;
+  unsigned int flag = 0, aflag = 0;
   e = gemm_read_error(&flag);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if (flag) {
-    t_last_error = "GEMM mbarrier wait timed out (flag " + std::to_string(flag) + ")";
+  e = attn_read_error(&aflag);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (flag || aflag) {
+    t_last_error = "bounded device wait timed out (GEMM flag " + std::to_string(flag) +
+                   ", decode attention flag " + std::to_string(aflag) + ")";
     return FG_ERR_TIMEOUT;
   }
   return FG_OK;

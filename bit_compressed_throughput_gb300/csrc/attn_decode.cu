@@ -10,41 +10,73 @@
 // Algebra per group g of 64 channels (a = min, s = (b - a)/15, c = code):
 //   q . k^  = sum_g ( s_g * sum_{j in g} c_j q_j  +  a_g * Q_g ),  Q_g = sum_{j in g} q_j
 //   sum_t p_t v^_tj = sum_t (p_t s_tg) c_tj + sum_t p_t a_tg
-// so the per-element work is a dot product of integer codes with fp16 weights.  The codes
-// become exact fp16 integers by OR-ing the nibble into the mantissa of 1024.0 and
-// subtracting 1024 (exact), and the dot products run on mma.sync m16n8k16 with fp32
-// accumulation (the product of a 4-bit integer and an fp16 value is exact in fp32).
+// so the per-element work is a dot product of integer codes with fp16 weights.  A nibble
+// OR-ed into the mantissa of 1024.0h gives the exact half 1024 + c (nibble at bit 0) or
+// 1024 + 16c (nibble at bit 4), so one shift per 32-bit word of codes suffices; the 16 is
+// folded into q (K side) or into the epilogue (V side), and the 1024 offsets are removed
+// algebraically: 1024 * sum(q) per group on the K side and 1024 * sum_t w_t on the V side.
+// The dot products run on mma.sync m16n8k16 with fp32 accumulation (the products are
+// exact in fp32).
 //
-// One warp owns (b, hd, split): 16 positions per tile, lane (gid, tig) loads positions
-// gid and gid+8 of the tile, 16 bytes of codes each for K and V (d = 128: 32 channels
-// per lane).  The dot-product index order inside a tile is permuted to match what each
-// lane loaded; q (K side) is permuted the same way, and the V side is transposed in
-// registers with movmatrix.  Online softmax (base 2) across tiles; split-sequence
-// partials are combined by a second kernel when one (b, hd) per warp would leave SMs idle.
+// Memory pipeline: a warp owns a flattened stream of 16-position tiles over its work
+// items (b, hd, split).  Lane 0 keeps kRing tiles in flight with 1-D bulk async copies
+// (K codes, V codes, K and V group statistics of one tile: four contiguous runs in the
+// head-major cache) into a per-warp shared-memory ring, completing on one mbarrier per
+// slot; the warp computes on slot i while slots i+1 .. i+kRing-1 land.  The stream runs
+// across item boundaries, so the ring never drains between items.  Tiles are whole 16
+// positions (the cache capacity is a multiple of 16), positions at or past the end are
+// masked with selects, so never-written cache slots cannot leak into the result.
+//
+// Inside a tile, lane (gid, tig) reads positions gid and gid+8 (16 bytes of codes each
+// for K and V when d = 128).  The dot-product index order is permuted to match what each
+// lane holds; q (K side) is permuted the same way, and the V side is transposed in
+// registers with movmatrix.  Online softmax (base 2) per item; split items write
+// (m, l, unnormalised o) partials that a second kernel combines.
+//
+// Every mbarrier wait is bounded; on timeout the warp sets the device error word read by
+// fg_check_device_error, drains its copies and stops.
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "fg_common.cuh"
 #include "fg_internal.h"
 
 namespace fg {
+
+__device__ unsigned int g_attn_error = 0;
+
 namespace {
 
 constexpr int kWarps = 4;
 constexpr int kTile = 16;
+constexpr int kRing = 4;                  // tiles in flight per warp
+constexpr int kPlanWarpsPerSm = 16;       // resident warps per SM assumed by the split plan
+constexpr long long kWaitCycles = 1ll << 32;
 
-__device__ __forceinline__ uint32_t hsub_1024(uint32_t x) {
-  __half2 a = *reinterpret_cast<__half2*>(&x);
-  const uint32_t k = 0x64006400u;
-  __half2 b = *reinterpret_cast<const __half2*>(&k);
-  __half2 r = __hsub2(a, b);
-  return *reinterpret_cast<uint32_t*>(&r);
+template <int D>
+struct Ring {
+  static constexpr int NG = D / 64;                     // groups per head
+  static constexpr int CODE_BYTES = kTile * (D / 2);    // one tile of K (or V) codes
+  static constexpr int AB_BYTES = kTile * NG * 4;       // one tile of K (or V) statistics
+  static constexpr int SLOT = 2 * CODE_BYTES + 2 * AB_BYTES;
+  static constexpr int WARP_BYTES = kRing * SLOT;
+  static constexpr int CTA_BYTES = kWarps * WARP_BYTES + kWarps * kRing * 8;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Pair i (0..3) of a code word as exact fp16 integers (c_i, c_{i+4}).
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
-  return hsub_1024(((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u);
+// The four pairs (c_i, c_{i+4}) of a code word as halves: pairs 0 and 2 hold 1024 + c,
+// pairs 1 and 3 hold 1024 + 16c (factor kPairScale[i]).
+__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t w8 = w >> 8;
+  p[0] = (w & 0x000F000Fu) | 0x64006400u;
+  p[1] = (w & 0x00F000F0u) | 0x64006400u;
+  p[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+  p[3] = (w8 & 0x00F000F0u) | 0x64006400u;
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -62,241 +94,366 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   return r;
 }
 
-template <int NW>
-struct TileRegs {
-  uint32_t k[2][NW], v[2][NW];   // codes of rows gid, gid+8
-  uint32_t ka[2][2], va[2][2];   // (a,b) words of rows gid, gid+8, groups 0..NG-1
+__device__ __forceinline__ void bar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait; false (and the device error word set) if it ran out.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!bar_try(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_attn_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+// One contiguous run global -> shared through the bulk-copy engine, completing on `bar`.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Work item -> (b, hd, position range).
+struct Item {
+  int b, hd, split, t_begin, t_end, ntiles;
 };
+__device__ __forceinline__ Item item_of(int item, int H, int len, int splits, int tps) {
+  Item it;
+  const int bh = item / splits;
+  it.split = item - bh * splits;
+  it.b = bh / H;
+  it.hd = bh - it.b * H;
+  it.t_begin = it.split * tps * kTile;
+  it.t_end = min(len, it.t_begin + tps * kTile);
+  it.ntiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
+  return it;
+}
 
 // D = head dim; NW = 32-bit code words per lane per row (D/32); NG = groups per head.
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 4)
 decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
                    const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc,
                    const uint32_t* __restrict__ kab, const uint32_t* __restrict__ vab, int B,
-                   int H, int cap, int len, int splits, int tiles_per_split, float scale_log2,
+                   int H, int cap, int len, int splits, int tps, float scale_log2,
                    uint16_t* __restrict__ out, float* __restrict__ partial) {
+  using R = Ring<D>;
   constexpr int NW = D / 32;
   constexpr int NG = D / 64;
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int64_t item = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (item >= (int64_t)B * H * splits) return;
-  const int split = (int)(item % splits);
-  const int64_t bh = item / splits;
-  const int b = (int)(bh / H), hd = (int)(bh % H);
-  const int t_begin = split * tiles_per_split * kTile;
-  const int t_end = min(len, t_begin + tiles_per_split * kTile);
+  uint8_t* ring = smem + warp * R::WARP_BYTES;
+  const uint32_t bar0 = smem_u32(smem + kWarps * R::WARP_BYTES) + warp * kRing * 8;
+  const int items = B * H * splits;                     // < 2^31 (checked on the host)
+  const int nwarps = gridDim.x * kWarps;
+  const int first = blockIdx.x * kWarps + warp;
 
-  // ---- q: this lane's channels j = tig*8*NW + 8w + i + 4e, permuted into B fragments.
-  const uint16_t* qh = q + (int64_t)b * q_stride + (int64_t)hd * D + tig * 8 * NW;
-  uint32_t qw[NW * 4];
-#pragma unroll
-  for (int c = 0; c < NW; ++c) {
-    const uint4 u = ldg_nc_v4(qh + 8 * c);
-    qw[4 * c] = u.x; qw[4 * c + 1] = u.y; qw[4 * c + 2] = u.z; qw[4 * c + 3] = u.w;
+  if (lane == 0) {
+    for (int s = 0; s < kRing; ++s) bar_init(bar0 + 8 * s);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // fp16 bits of channel 8w+i of this lane's chunk
-  auto qval = [&](int w, int i) -> uint32_t {
-    const uint32_t word = qw[4 * w + (i >> 1)];
-    return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
-  };
-  const int my_group = (NG == 2) ? (tig >> 1) : 0;
-  float qsum = 0.0f;
-#pragma unroll
-  for (int w = 0; w < NW; ++w)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qsum += h2f((uint16_t)qval(w, i));
-  // Sum over the lanes sharing this group: tig pairs (NG == 2) or all four (NG == 1).
-  qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
-  if (NG == 1) qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
-  const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3);
-  const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) : 0.0f;
+  __syncwarp();
 
-  uint32_t bq[2 * NW][2];
-#pragma unroll
-  for (int s = 0; s < 2 * NW; ++s) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int p = 2 * s + r, w = p >> 2, i = p & 3;
-      const uint32_t v = qval(w, i) | (qval(w, i + 4) << 16);
-      bq[s][r] = (gid == my_group) ? v : 0u;
-    }
-  }
-
-  // ---- stream the tiles
-  const int64_t head_row0 = ((int64_t)b * H + hd) * cap;      // slot of position 0
-  const uint8_t* kbase = kc + head_row0 * (D / 2) + tig * 4 * NW;
-  const uint8_t* vbase = vc + head_row0 * (D / 2) + tig * 4 * NW;
-  const uint32_t* kabase = kab + head_row0 * NG;
-  const uint32_t* vabase = vab + head_row0 * NG;
-
-  auto load_tile = [&](int t0, TileRegs<NW>& R) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = t0 + gid + 8 * r;
-      if (t < t_end) {
-        if (NW == 4) {
-          const uint4 uk = ldg_nc_v4(kbase + (int64_t)t * (D / 2));
-          const uint4 uv = ldg_nc_v4(vbase + (int64_t)t * (D / 2));
-          R.k[r][0] = uk.x; R.k[r][1] = uk.y; R.k[r][2 % NW] = uk.z; R.k[r][3 % NW] = uk.w;
-          R.v[r][0] = uv.x; R.v[r][1] = uv.y; R.v[r][2 % NW] = uv.z; R.v[r][3 % NW] = uv.w;
-        } else {
-          const uint2 uk = *reinterpret_cast<const uint2*>(kbase + (int64_t)t * (D / 2));
-          const uint2 uv = *reinterpret_cast<const uint2*>(vbase + (int64_t)t * (D / 2));
-          R.k[r][0] = uk.x; R.k[r][1 % NW] = uk.y;
-          R.v[r][0] = uv.x; R.v[r][1 % NW] = uv.y;
-        }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          R.ka[r][g] = kabase[(int64_t)t * NG + g];
-          R.va[r][g] = vabase[(int64_t)t * NG + g];
-        }
-      } else {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) { R.k[r][w] = 0u; R.v[r][w] = 0u; }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) { R.ka[r][g] = 0u; R.va[r][g] = 0u; }
-      }
+  // ---- issue cursor (used by lane 0 only): kRing tiles ahead of the compute cursor
+  int ii = first;
+  int itile = 0;
+  Item iitem = item_of(ii < items ? ii : 0, H, len, splits, tps);
+  int64_t gi = 0;
+  auto issue = [&]() {
+    if (ii >= items) return;
+    const int s = (int)(gi % kRing);
+    const uint32_t bar = bar0 + 8 * s;
+    uint8_t* slot = ring + s * R::SLOT;
+    const int t0 = iitem.t_begin + itile * kTile;
+    const int64_t row0 = ((int64_t)iitem.b * H + iitem.hd) * cap + t0;
+    // the slot was last read through the generic proxy; order that before the copy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bar_expect_tx(bar, R::SLOT);
+    bulk_copy(smem_u32(slot), kc + row0 * (D / 2), R::CODE_BYTES, bar);
+    bulk_copy(smem_u32(slot + R::CODE_BYTES), vc + row0 * (D / 2), R::CODE_BYTES, bar);
+    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES), kab + row0 * NG, R::AB_BYTES, bar);
+    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES + R::AB_BYTES), vab + row0 * NG, R::AB_BYTES,
+              bar);
+    ++gi;
+    if (++itile == iitem.ntiles) {
+      ii += nwarps;
+      itile = 0;
+      if (ii < items) iitem = item_of(ii, H, len, splits, tps);
     }
   };
+  if (lane == 0)
+    for (int r = 0; r < kRing; ++r) issue();
 
-  float m_run = -INFINITY, l_run = 0.0f;
-  float acc[2 * NW][4];
-#pragma unroll
-  for (int u = 0; u < 2 * NW; ++u)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-  float asum[NG];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) asum[g] = 0.0f;
+  int64_t gc = 0;
+  bool ok = true;
+  for (int ci = first; ci < items && ok; ci += nwarps) {
+    const Item it = item_of(ci, H, len, splits, tps);
 
-  TileRegs<NW> cur, nxt;
-  if (t_begin < t_end) load_tile(t_begin, cur);
-  for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
-    if (t0 + kTile < t_end) load_tile(t0 + kTile, nxt);
-
-    // ---- scores: K codes (rows t) x permuted q, one column per group
-    float dk[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- q: this lane's channels j = tig*8*NW + 8w + i + 4e, permuted into B fragments
+    const uint16_t* qh = q + (int64_t)it.b * q_stride + (int64_t)it.hd * D + tig * 8 * NW;
+    uint32_t qw[NW * 4];
+#pragma unroll
+    for (int c = 0; c < NW; ++c) {
+      const uint4 u = ldg_nc_v4(qh + 8 * c);
+      qw[4 * c] = u.x; qw[4 * c + 1] = u.y; qw[4 * c + 2] = u.z; qw[4 * c + 3] = u.w;
+    }
+    auto qval = [&](int w, int i) -> uint32_t {     // fp16 bits of channel 8w+i of the chunk
+      const uint32_t word = qw[4 * w + (i >> 1)];
+      return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
+    };
+    const int my_group = (NG == 2) ? (tig >> 1) : 0;
+    // B fragments: q for pairs with factor 1, q/16 (exact) for pairs with factor 16;
+    // qsum = sum of q, qoff = 1024 * sum of the B values (the codes' 1024 offset)
+    float qsum = 0.0f, qoff = 0.0f;
+    uint32_t bq[2 * NW][2];
 #pragma unroll
     for (int s = 0; s < 2 * NW; ++s) {
-      const int p0 = 2 * s, p1 = 2 * s + 1;
-      const uint32_t a0 = code_pair(cur.k[0][p0 >> 2], p0 & 3);
-      const uint32_t a1 = code_pair(cur.k[1][p0 >> 2], p0 & 3);
-      const uint32_t a2 = code_pair(cur.k[0][p1 >> 2], p1 & 3);
-      const uint32_t a3 = code_pair(cur.k[1][p1 >> 2], p1 & 3);
-      mma16816(dk, a0, a1, a2, a3, bq[s][0], bq[s][1]);
-    }
-    // lanes with tig == 0 hold D[t][0..1] for t = gid (dk[0], dk[1]) and gid+8 (dk[2], dk[3])
-    float sc[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float2 ab0 = unpack_h2(cur.ka[r][0]);
-      float v = (ab0.y - ab0.x) * (1.0f / 15.0f) * dk[2 * r] + ab0.x * Q0;
-      if (NG == 2) {
-        const float2 ab1 = unpack_h2(cur.ka[r][NG - 1]);
-        v += (ab1.y - ab1.x) * (1.0f / 15.0f) * dk[2 * r + 1] + ab1.x * Q1;
+      for (int r = 0; r < 2; ++r) {
+        const int p = 2 * s + r, w = p >> 2, i = p & 3;
+        uint32_t v = qval(w, i) | (qval(w, i + 4) << 16);
+        const float2 fq = unpack_h2(v);
+        qsum += fq.x + fq.y;
+        if (i & 1) {
+          const uint32_t k16 = 0x2C002C00u;             // half2(1/16, 1/16)
+          __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), *reinterpret_cast<const __half2*>(&k16));
+          v = *reinterpret_cast<uint32_t*>(&h);
+        }
+        const float2 fb = unpack_h2(v);
+        qoff += 1024.0f * (fb.x + fb.y);
+        bq[s][r] = (gid == my_group) ? v : 0u;
       }
-      v = __shfl_sync(0xFFFFFFFFu, v, lane & ~3);
-      const int t = t0 + gid + 8 * r;
-      sc[r] = (t < t_end) ? v * scale_log2 : -INFINITY;
     }
-    float mx = fmaxf(sc[0], sc[1]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-    const float m_new = fmaxf(m_run, mx);
-    const float corr = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new);
-    const float p0 = exp2f(sc[0] - m_new), p1 = exp2f(sc[1] - m_new);
-    float ps = p0 + p1;
-    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
-    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 8);
-    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
-    if (m_new != m_run) {
-      l_run *= corr;
-#pragma unroll
-      for (int u = 0; u < 2 * NW; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) asum[g] *= corr;
-      m_run = m_new;
+    // sum over the lanes sharing this group: tig pairs (NG == 2) or all four (NG == 1)
+    qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
+    qoff += __shfl_xor_sync(0xFFFFFFFFu, qoff, 1);
+    if (NG == 1) {
+      qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
+      qoff += __shfl_xor_sync(0xFFFFFFFFu, qoff, 2);
     }
-    l_run += ps;
+    const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3);
+    const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) : 0.0f;
+    const float O0 = __shfl_sync(0xFFFFFFFFu, qoff, lane & ~3);
+    const float O1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qoff, (lane & ~3) | 2) : 0.0f;
 
-    // ---- V weights w_tg = p_t * s_tg (fp16) and the offset term sum_t p_t a_tg
-    uint32_t wrow[2];
+    float m_run = -INFINITY, l_run = 0.0f;
+    float acc[2 * NW][4];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float p = r ? p1 : p0;
-      const float2 ab0 = unpack_h2(cur.va[r][0]);
-      const float w0 = p * (ab0.y - ab0.x) * (1.0f / 15.0f);
-      asum[0] += p * ab0.x;
-      float w1 = 0.0f;
-      if (NG == 2) {
-        const float2 ab1 = unpack_h2(cur.va[r][NG - 1]);
-        w1 = p * (ab1.y - ab1.x) * (1.0f / 15.0f);
-        asum[NG - 1] += p * ab1.x;
+    for (int u = 0; u < 2 * NW; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
+    float asum[NG], wsum[NG];           // sum_t p_t a_tg and sum_t w_tg (1024 offset)
+#pragma unroll
+    for (int g = 0; g < NG; ++g) asum[g] = wsum[g] = 0.0f;
+
+    for (int j = 0; j < it.ntiles; ++j, ++gc) {
+      const int s = (int)(gc % kRing);
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(bar0 + 8 * s, (uint32_t)((gc / kRing) & 1)));
+      if (!ok) break;
+      const uint8_t* slot = ring + s * R::SLOT;
+      // ---- this lane's rows gid and gid+8 of the tile, from shared memory
+      uint32_t kw[2][NW], vw[2][NW], ka[2][NG], va[2][NG];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = gid + 8 * r;
+        const uint8_t* kp = slot + row * (D / 2) + tig * 4 * NW;
+        const uint8_t* vp = slot + R::CODE_BYTES + row * (D / 2) + tig * 4 * NW;
+        if (NW == 4) {
+          const uint4 uk = *reinterpret_cast<const uint4*>(kp);
+          const uint4 uv = *reinterpret_cast<const uint4*>(vp);
+          kw[r][0] = uk.x; kw[r][1] = uk.y; kw[r][2 % NW] = uk.z; kw[r][3 % NW] = uk.w;
+          vw[r][0] = uv.x; vw[r][1] = uv.y; vw[r][2 % NW] = uv.z; vw[r][3 % NW] = uv.w;
+        } else {
+          const uint2 uk = *reinterpret_cast<const uint2*>(kp);
+          const uint2 uv = *reinterpret_cast<const uint2*>(vp);
+          kw[r][0] = uk.x; kw[r][1 % NW] = uk.y;
+          vw[r][0] = uv.x; vw[r][1 % NW] = uv.y;
+        }
+        const uint32_t* kap = reinterpret_cast<const uint32_t*>(slot + 2 * R::CODE_BYTES);
+        const uint32_t* vap = reinterpret_cast<const uint32_t*>(slot + 2 * R::CODE_BYTES +
+                                                                R::AB_BYTES);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          ka[r][g] = kap[row * NG + g];
+          va[r][g] = vap[row * NG + g];
+        }
       }
-      wrow[r] = pack_h2(w0, w1);
-    }
-    // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid (group n)
-    const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
-    const uint32_t wb = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig + 4);
-    const uint32_t wc = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig);
-    const uint32_t wd = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig + 4);
-    uint32_t bv0 = 0u, bv1 = 0u;
-    if (gid < NG) {
-      const uint32_t sel = gid ? 0x7632u : 0x5410u;   // pick the high or low halves
-      bv0 = __byte_perm(wa, wb, sel);
-      bv1 = __byte_perm(wc, wd, sel);
-    }
-    // ---- V codes transposed to (channel rows, position columns)
+      __syncwarp();                       // every lane is done with this slot
+      if (lane == 0) issue();             // refill it kRing tiles ahead
+      const int t0 = it.t_begin + j * kTile;
+
+      // ---- scores: K codes (rows t) x permuted q, one column per group
+      float dk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < 2 * NW; ++u) {
-      const int px = 2 * u, py = 2 * u + 1;
-      const uint32_t x0 = movtrans(code_pair(cur.v[0][px >> 2], px & 3));
-      const uint32_t y0 = movtrans(code_pair(cur.v[0][py >> 2], py & 3));
-      const uint32_t x1 = movtrans(code_pair(cur.v[1][px >> 2], px & 3));
-      const uint32_t y1 = movtrans(code_pair(cur.v[1][py >> 2], py & 3));
-      mma16816(acc[u], x0, y0, x1, y1, bv0, bv1);
+      for (int w = 0; w < NW; ++w) {
+        uint32_t c0[4], c1[4];                       // rows gid and gid+8
+        code_pairs(kw[0][w], c0);
+        code_pairs(kw[1][w], c1);
+        mma16816(dk, c0[0], c1[0], c0[1], c1[1], bq[2 * w][0], bq[2 * w][1]);
+        mma16816(dk, c0[2], c1[2], c0[3], c1[3], bq[2 * w + 1][0], bq[2 * w + 1][1]);
+      }
+      // lanes with tig == 0 hold D[t][0..1] for t = gid (dk[0], dk[1]) and gid+8 (dk[2], dk[3])
+      bool valid[2];
+      float sc[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float2 ab0 = unpack_h2(ka[r][0]);
+        float v = (ab0.y - ab0.x) * (1.0f / 15.0f) * (dk[2 * r] - O0) + ab0.x * Q0;
+        if (NG == 2) {
+          const float2 ab1 = unpack_h2(ka[r][NG - 1]);
+          v += (ab1.y - ab1.x) * (1.0f / 15.0f) * (dk[2 * r + 1] - O1) + ab1.x * Q1;
+        }
+        v = __shfl_sync(0xFFFFFFFFu, v, lane & ~3);
+        valid[r] = t0 + gid + 8 * r < it.t_end;
+        sc[r] = valid[r] ? v * scale_log2 : -INFINITY;
+      }
+      float mx = fmaxf(sc[0], sc[1]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      // lazy rescaling: the reference maximum moves only when a score exceeds it by more
+      // than 2^8, so p stays <= 256 and the accumulators rarely need scaling
+      if (mx > m_run + 8.0f) {
+        const float corr = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
+        l_run *= corr;
+#pragma unroll
+        for (int u = 0; u < 2 * NW; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          asum[g] *= corr;
+          wsum[g] *= corr;
+        }
+        m_run = mx;
+      }
+      const float p0 = valid[0] ? exp2f(sc[0] - m_run) : 0.0f;
+      const float p1 = valid[1] ? exp2f(sc[1] - m_run) : 0.0f;
+      float ps = p0 + p1;
+      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
+      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 8);
+      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
+      l_run += ps;
+
+      // ---- V weights w_tg = p_t * s_tg (fp16) and the offset term sum_t p_t a_tg; rows
+      // past the end contribute exact zeros whatever their (never written) bytes hold
+      uint32_t wrow[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float p = r ? p1 : p0;
+        const float2 ab0 = unpack_h2(va[r][0]);
+        const float w0 = valid[r] ? p * (ab0.y - ab0.x) * (1.0f / 15.0f) : 0.0f;
+        asum[0] += valid[r] ? p * ab0.x : 0.0f;
+        float w1 = 0.0f;
+        if (NG == 2) {
+          const float2 ab1 = unpack_h2(va[r][NG - 1]);
+          w1 = valid[r] ? p * (ab1.y - ab1.x) * (1.0f / 15.0f) : 0.0f;
+          asum[NG - 1] += valid[r] ? p * ab1.x : 0.0f;
+        }
+        wrow[r] = pack_h2(w0, w1);
+        const float2 wr = unpack_h2(wrow[r]);       // the fp16 values the MMA uses
+        wsum[0] += wr.x;
+        if (NG == 2) wsum[NG - 1] += wr.y;
+      }
+      // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid (group n)
+      const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
+      const uint32_t wb = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig + 4);
+      const uint32_t wc = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig);
+      const uint32_t wd = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig + 4);
+      uint32_t bv0 = 0u, bv1 = 0u;
+      if (gid < NG) {
+        const uint32_t sel = gid ? 0x7632u : 0x5410u;   // pick the high or low halves
+        bv0 = __byte_perm(wa, wb, sel);
+        bv1 = __byte_perm(wc, wd, sel);
+      }
+      // ---- V codes transposed to (channel rows, position columns)
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        uint32_t c0[4], c1[4];
+        code_pairs(vw[0][w], c0);
+        code_pairs(vw[1][w], c1);
+        mma16816(acc[2 * w], movtrans(c0[0]), movtrans(c0[1]), movtrans(c1[0]), movtrans(c1[1]),
+                 bv0, bv1);
+        mma16816(acc[2 * w + 1], movtrans(c0[2]), movtrans(c0[3]), movtrans(c1[2]),
+                 movtrans(c1[3]), bv0, bv1);
+      }
     }
-    cur = nxt;
+    if (!ok) break;
+
+    // ---- epilogue of the item: o_j = (acc + sum_t p_t a_tg) / l
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 4);
+      asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
+      asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
+      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 4);
+      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 8);
+      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 16);
+    }
+    if (tig == 0) {
+      const int g_lo = (NG == 2) ? (gid >> 2) : 0;      // group of channel row gid
+      const float A = (NG == 2 && g_lo) ? asum[NG - 1] : asum[0];
+      const float W1024 = 1024.0f * ((NG == 2 && g_lo) ? wsum[NG - 1] : wsum[0]);
+      // channel rows of mma u: pair 2u has factor 1, pair 2u+1 factor 16
+      auto vx_of = [&](int u) { return (g_lo ? acc[u][1] : acc[u][0]) - W1024 + A; };
+      auto vy_of = [&](int u) {
+        return ((g_lo ? acc[u][3] : acc[u][2]) - W1024) * (1.0f / 16.0f) + A;
+      };
+      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const int jbase = (gid >> 1) * 8 * NW + 4 * (gid & 1);
+      if (splits == 1) {
+        uint16_t* o = out + (int64_t)it.b * H * D + (int64_t)it.hd * D;
+#pragma unroll
+        for (int u = 0; u < 2 * NW; ++u) {
+          const int px = 2 * u, py = 2 * u + 1;
+          o[jbase + 8 * (px >> 2) + (px & 3)] = f2h(vx_of(u) * inv_l);
+          o[jbase + 8 * (py >> 2) + (py & 3)] = f2h(vy_of(u) * inv_l);
+        }
+      } else {
+        float* pp = partial + (int64_t)ci * (D + 2);
+#pragma unroll
+        for (int u = 0; u < 2 * NW; ++u) {
+          const int px = 2 * u, py = 2 * u + 1;
+          pp[jbase + 8 * (px >> 2) + (px & 3)] = vx_of(u);
+          pp[jbase + 8 * (py >> 2) + (py & 3)] = vy_of(u);
+        }
+        if (gid == 0) {
+          pp[D] = m_run;
+          pp[D + 1] = l_run;
+        }
+      }
+    }
+    __syncwarp();
   }
 
-  // ---- epilogue: o_j = (acc + sum_t p_t a_tg) / l
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 4);
-    asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
-    asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
-  }
-  if (tig != 0) return;
-  const int g_lo = (NG == 2) ? (gid >> 2) : 0;        // group of channel row gid
-  const float A = (NG == 2 && g_lo) ? asum[NG - 1] : asum[0];
-  const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-  const int jbase = (gid >> 1) * 8 * NW + 4 * (gid & 1);
-  if (splits == 1) {
-    uint16_t* o = out + (int64_t)b * H * D + (int64_t)hd * D;
-#pragma unroll
-    for (int u = 0; u < 2 * NW; ++u) {
-      const int px = 2 * u, py = 2 * u + 1;
-      const float vx = (g_lo ? acc[u][1] : acc[u][0]) + A;
-      const float vy = (g_lo ? acc[u][3] : acc[u][2]) + A;
-      o[jbase + 8 * (px >> 2) + (px & 3)] = f2h(vx * inv_l);
-      o[jbase + 8 * (py >> 2) + (py & 3)] = f2h(vy * inv_l);
-    }
-  } else {
-    float* pp = partial + (bh * splits + split) * (int64_t)(D + 2);
-#pragma unroll
-    for (int u = 0; u < 2 * NW; ++u) {
-      const int px = 2 * u, py = 2 * u + 1;
-      pp[jbase + 8 * (px >> 2) + (px & 3)] = (g_lo ? acc[u][1] : acc[u][0]) + A;
-      pp[jbase + 8 * (py >> 2) + (py & 3)] = (g_lo ? acc[u][3] : acc[u][2]) + A;
-    }
-    if (gid == 0) {
-      pp[D] = m_run;
-      pp[D + 1] = l_run;
+  // ---- drain: every issued copy must land before the warp's shared memory is released
+  if (lane == 0) {
+    for (int64_t g = gc; g < gi; ++g) {
+      const uint32_t bar = bar0 + 8 * (uint32_t)(g % kRing);
+      const long long t0 = clock64();
+      while (!bar_try(bar, (uint32_t)((g / kRing) & 1))) {
+        if (clock64() - t0 > kWaitCycles) {
+          atomicOr(&g_attn_error, 2u);
+          break;
+        }
+      }
     }
   }
 }
@@ -330,18 +487,30 @@ decode_combine_kernel(const float* __restrict__ partial, int64_t nbh, int H, int
   for (int c = 0; c < D / 32; ++c) op[c * 32 + lane] = f2h(o[c] * inv);
 }
 
-constexpr int kTargetWarpsPerSm = 32;   // two waves of 16 resident warps
+template <int D>
+int resident_ctas() {
+  static int occ = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<D>, kWarps * 32,
+                                                      Ring<D>::CTA_BYTES) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    return n;
+  }();
+  return occ;
+}
 
 }  // namespace
 
+// Sequence splits: enough work items (b, hd, split) for about two per resident warp, each
+// split at least 4 tiles long, no empty split.
 int decode_attn_splits(const fg_kvcache& kv, int32_t len, int nsm) {
   const int64_t bh = (int64_t)kv.B * kv.H;
   if (bh == 0) return 1;
   const int ntiles = (len + kTile - 1) / kTile;
-  const int64_t target = (int64_t)nsm * kTargetWarpsPerSm;
+  const int64_t target = 2ll * nsm * kPlanWarpsPerSm;
   int64_t splits = (target + bh - 1) / bh;
-  const int min_tiles = 4;
-  splits = std::min<int64_t>(splits, std::max(1, ntiles / min_tiles));
+  splits = std::min<int64_t>(splits, std::max(1, ntiles / 4));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, ntiles));
   const int tps = (int)((ntiles + splits - 1) / splits);
   return (ntiles + tps - 1) / tps;
@@ -362,17 +531,21 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
   const int ntiles = (len + kTile - 1) / kTile;
   const int tps = (ntiles + splits - 1) / splits;
   const int64_t items = (int64_t)kv.B * kv.H * splits;
-  const unsigned grid = (unsigned)((items + kWarps - 1) / kWarps);
+  if (items >= (1ll << 31)) return cudaErrorInvalidValue;   // work items are 32-bit
   const float sl2 = scale * 1.4426950408889634f;
   float* partial = static_cast<float*>(ws);
-  if (d == 128)
-    decode_attn_kernel<128><<<grid, kWarps * 32, 0, st>>>(
+  const int64_t want = (items + kWarps - 1) / kWarps;
+  if (d == 128) {
+    const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<128>());
+    decode_attn_kernel<128><<<grid, kWarps * 32, Ring<128>::CTA_BYTES, st>>>(
         q, q_stride, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits,
         tps, sl2, out, partial);
-  else
-    decode_attn_kernel<64><<<grid, kWarps * 32, 0, st>>>(
+  } else {
+    const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<64>());
+    decode_attn_kernel<64><<<grid, kWarps * 32, Ring<64>::CTA_BYTES, st>>>(
         q, q_stride, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits,
         tps, sl2, out, partial);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *kernels_out = 1;
@@ -388,6 +561,13 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
     *kernels_out = 2;
   }
   return e;
+}
+
+cudaError_t attn_read_error(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_attn_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_attn_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace fg

@@ -47,8 +47,9 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms);
 cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
                         void* ws, cudaStream_t st, cudaEvent_t mid_event);
-// Device error word of the GEMM's bounded waits: read-and-clear (after a sync).
+// Device error words of the bounded waits (GEMM, decode attention): read-and-clear.
 cudaError_t gemm_read_error(unsigned int* out);
+cudaError_t attn_read_error(unsigned int* out);
 
 // Algorithmic work of one launch (bytes for memory-bound kernels, flops for the GEMM and
 // prefill attention): 4-bit storage costs 0.5 byte per element plus one (a, b) fp16 pair

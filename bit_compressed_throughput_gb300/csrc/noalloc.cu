@@ -86,8 +86,8 @@ extern "C" int fg_decode_attn_q4kv_static(const uint16_t* q, int64_t q_stride,
   if (!aligned16(kv->k_codes) || !aligned16(kv->v_codes) || !aligned16(kv->k_ab) ||
       !aligned16(kv->v_ab))
     return FG_ERR_ARG;
-  if (kv->B < 0 || kv->cap <= 0 || kv->h <= 0 || kv->H <= 0 || kv->h % 64 != 0 ||
-      kv->h % kv->H != 0)
+  if (kv->B < 0 || kv->cap <= 0 || kv->cap % 16 != 0 || kv->h <= 0 || kv->H <= 0 ||
+      kv->h % 64 != 0 || kv->h % kv->H != 0)
     return FG_ERR_SHAPE;
   const int d = kv->h / kv->H;
   if (d != 64 && d != 128) return FG_ERR_SHAPE;

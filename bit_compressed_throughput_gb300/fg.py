@@ -132,10 +132,11 @@ class Q4Weight:
 
 class KVCacheQ4:
     """One layer's 4-bit KV cache: codes [B][H][cap][d/2] uint8, ab [B][H][cap][d/64]
-    int32, for K and V."""
+    int32, for K and V.  ``cap`` is rounded up to a multiple of 16 positions."""
 
     def __init__(self, B: int, cap: int, h: int, H: int, device="cuda"):
         import torch
+        cap = (int(cap) + 15) // 16 * 16
         d = h // H
         self.B, self.cap, self.h, self.H, self.d = B, cap, h, H, d
         self.k_codes = torch.zeros((B, H, cap, d // 2), dtype=torch.uint8, device=device)

@@ -39,9 +39,10 @@ def attn_case(B, H, d, length, reps):
     import torch
     import fg_synth
     from bit_compressed_throughput_gb300 import fg
-    kc, vc, ka, va = fg_synth.random_q4_cache_torch(B, H, length, d, seed=3)
+    cap = (length + 15) // 16 * 16
+    kc, vc, ka, va = fg_synth.random_q4_cache_torch(B, H, cap, d, seed=3)
     cache = fg.KVCacheQ4.__new__(fg.KVCacheQ4)
-    cache.B, cache.cap, cache.h, cache.H, cache.d = B, length, H * d, H, d
+    cache.B, cache.cap, cache.h, cache.H, cache.d = B, cap, H * d, H, d
     cache.k_codes, cache.v_codes, cache.k_ab, cache.v_ab = kc, vc, ka, va
     q = torch.randn((B, H * d), device="cuda").half()
     out = torch.empty_like(q)

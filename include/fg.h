@@ -79,7 +79,7 @@ typedef struct {
   uint32_t* k_ab;
   uint32_t* v_ab;
   int32_t B;    /* sequences */
-  int32_t cap;  /* positions per sequence */
+  int32_t cap;  /* positions per sequence, a multiple of 16 (whole 16-position tiles) */
   int32_t h;    /* hidden size */
   int32_t H;    /* heads; d = h / H must be 64 or 128 */
 } fg_kvcache;

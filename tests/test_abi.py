@@ -105,14 +105,15 @@ def test_layer_validation(fg):
     dm = fg.fg_dims(256, 4, 64, 1024, 1e-5)
     lay = fg.fg_layer(q4(256, 768), q4(256, 256), q4(256, 1024), q4(1024, 256),
                       None, None, None, None, FAKE, FAKE, FAKE, FAKE)
-    kv = kvs(B=4, cap=20, h=256, H=4)
-    wsb = L.fg_layer_workspace_bytes(C.byref(dm), 2, 2, 20)
+    kv = kvs(B=4, cap=32, h=256, H=4)
+    wsb = L.fg_layer_workspace_bytes(C.byref(dm), 2, 2, 32)
     assert wsb > 0
     pre = lambda g=2, m=2, s=16, ws=FAKE, n=wsb, d=dm, k=kv: L.fg_layer_prefill(
         C.byref(d), C.byref(lay), C.byref(k), FAKE, FAKE, g, m, s, ws, n, None)
     assert pre(n=wsb // 4) == fg.FG_ERR_WORKSPACE
     assert pre(g=3) == fg.FG_ERR_SHAPE                       # kv.B != g*m
-    assert pre(s=21) == fg.FG_ERR_CAPACITY
+    assert pre(s=33) == fg.FG_ERR_CAPACITY
+    assert pre(k=kvs(B=4, cap=20, h=256, H=4)) == fg.FG_ERR_SHAPE      # cap % 16
     assert pre(d=fg.fg_dims(256, 4, 64, 1000, 1e-5)) == fg.FG_ERR_SHAPE
     assert pre(d=fg.fg_dims(256, 4, 64, 960, 1e-5)) == fg.FG_ERR_SHAPE     # f % 256
     assert pre(d=fg.fg_dims(256, 2, 128, 1024, 1e-5)) == fg.FG_ERR_SHAPE   # kv.H mismatch
@@ -120,7 +121,7 @@ def test_layer_validation(fg):
                           None, None, None, None, FAKE, FAKE, FAKE, FAKE)
     assert L.fg_layer_prefill(C.byref(dm), C.byref(lay_bad), C.byref(kv), FAKE, FAKE, 2, 2, 16,
                               FAKE, wsb, None) == fg.FG_ERR_SHAPE
-    assert L.fg_layer_decode(C.byref(dm), C.byref(lay), C.byref(kv), FAKE, FAKE, 2, 2, 20,
+    assert L.fg_layer_decode(C.byref(dm), C.byref(lay), C.byref(kv), FAKE, FAKE, 2, 2, 32,
                              FAKE, wsb, None) == fg.FG_ERR_CAPACITY
 
 

@@ -108,7 +108,7 @@ def test_kv_append_bit_exact(fg, B, T, pos, h, H, cap):
         got_ab = cache_codes_to_rows(host(ab_t)).view(np.uint32)
         assert np.array_equal(got_c[:, pos:pos + T].reshape(B * T, h // 2), c_ref)
         assert np.array_equal(got_ab[:, pos:pos + T].reshape(B * T, h // 64), ab_ref)
-        untouched = np.ones(cap, bool)
+        untouched = np.ones(cache.cap, bool)
         untouched[pos:pos + T] = False
         assert not got_c[:, untouched].any() and not got_ab[:, untouched].any()
 
@@ -243,6 +243,11 @@ def test_decode_attention(fg, B, H, d, T, length, stride3):
     k16 = fg_synth.random_fp16((B, T, h), seed=B * 1000 + T, scale=1.5)
     v16 = fg_synth.random_fp16((B, T, h), seed=B * 1000 + T + 1, scale=1.0, offset=0.2)
     cache, khat, vhat = oracle_cache_from_rows(fg, k16, v16, T + 3, H)
+    # positions the call must not read (or must mask): garbage codes, NaN statistics
+    cache.k_codes[:, :, T:] = 0x5A
+    cache.v_codes[:, :, T:] = 0xA5
+    cache.k_ab[:, :, T:] = 0x7E007E00
+    cache.v_ab[:, :, T:] = 0x7E007E00
     qbuf16 = fg_synth.random_fp16((B, 3 * h if stride3 else h), seed=T + 5, scale=1.5)
     q16 = qbuf16[:, :h]
     out = torch.empty((B, h), dtype=torch.float16, device="cuda")
