@@ -35,10 +35,12 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
                                int num_sms, cudaStream_t st, int* kernels_out,
                                cudaEvent_t mid_event);
 
-// Dequant-fused GEMM plan: tiles, split-K factor and workspace.
+// Dequant-fused GEMM plan: tn tokens x 128 channels per tile, split-K factor and
+// workspace.
 struct GemmPlan {
   int64_t M, N, K;
-  int tiles_m, tiles_n, kblocks, splits, kb_per_split;
+  int tn;                  // tokens per tile: a multiple of 16 in [16, 256]
+  int tiles_t, tiles_c, kblocks, splits, kb_per_split;
   int64_t units;   // (split, tile) work units
   int grid;        // persistent CTAs: min(units, SMs)
   size_t ws_bytes;

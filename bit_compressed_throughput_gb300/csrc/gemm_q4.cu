@@ -6,27 +6,36 @@
 // matmul].  The block schedule's batch reuse makes the projections and the MLP dense
 // contractions over M = g*s (prefill) or M = B (decode) rows.
 //
-// Persistent kernel: one CTA per SM loops over output tiles 128 x 256 (K step 64).
-//   warp 0      TMA producer: X tile (128B swizzle, K-major), packed code tile (128B
-//               swizzle) and the tile's group statistics, one transaction per stage, into a
-//               6-deep ring; owns the TMEM allocation (512 columns)
-//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) into one of
-//               two double-buffered 128 x 256 fp32 accumulators and commits to mbarriers
-//   warps 2-9   restore codes -> fp16 B tile in a 2-deep shared-memory ring (MN-major,
-//               128B swizzle: one k-row of 64 output channels = one 128-byte swizzle row =
-//               one group); two restore warps per SM sub-partition hide each other's
-//               latency
-//   warps 10-13 epilogue of the previous tile (tcgen05.ld, bias / ReLU / residual, fp16
-//               store) while the other accumulator fills
-// The restore, not the MMA, bounds this kernel: with the restore skipped the same
-// pipeline runs at about 84% of the measured dense fp16 peak.
+// The tensor core computes the transposed product Y^T = W^T X^T: the restored weights are
+// the MMA's A operand (M = 128 output channels) and the activations its B operand
+// (N = up to 256 tokens).  Against the straight orientation (tokens as M, channels as N)
+// this halves the codes restored per MMA cycle at 256 tokens per tile, needs no padding
+// when the token count is small (decode: N = B), and keeps the restored tile in the
+// layout the codes already have: one k-row of 64 output channels is one 128-byte swizzle
+// row of an MN-major operand, one quantisation group.
+//
+// Persistent kernel: one CTA per SM loops over (split, token tile, channel tile) units,
+// K step 64.
+//   warp 0      TMA producer: X tile (tn x 64, 128B swizzle, K-major), the 128-channel
+//               code tile (64B swizzle) and the group statistics of the aligned 256-channel
+//               block, one transaction per stage, into a ring sized to the shared memory
+//               left (4 stages at tn = 256, 13 at tn = 64); owns the TMEM allocation
+//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=tn, K=16) into one of
+//               two double-buffered fp32 accumulators; one commit per k-block frees both
+//               its raw stage and its restored slot
+//   warps 2-9   two groups of four warps restore alternate k-blocks: codes -> fp16 A tile
+//               in a 3-slot shared-memory ring (MN-major, 128B swizzle), two 16-byte code
+//               chunks (32 channels each) per thread per k-block
+//   warps 10-13 epilogue of the previous tile (tcgen05.ld: one TMEM lane per output
+//               channel, 32 tokens per batch; bias / ReLU / residual, fp16 store); with a
+//               residual the tile's rows are prefetched to L2 while the accumulator fills
 // Restoration per pair of codes: the nibble is OR-ed into mantissa bits 6..9 of 1.0h so
 // that the half equals 1 + q/16, then one HFMA2 gives (1 + q/16)*(16s) + (a - 16s) = a + q*s.
-// Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7); the epilogue
-// undoes that order when it packs the accumulator columns back to fp16.
+// Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7), so accumulator
+// lane 8u+p holds channel 8u+kPerm[p]; the epilogue maps lanes back to channels.
 //
-// Small M (decode) also splits K: work units are (split, tile); partial fp32 tiles go to
-// the caller's workspace and a reduce kernel applies the epilogue.
+// Few work units (decode) split K: partial fp32 tiles go to the caller's workspace and a
+// reduce kernel applies the epilogue.
 //
 // Every mbarrier wait is bounded (about 2 s); on timeout the CTA raises an abort flag,
 // sets the device error word, drains its outstanding copies and exits.
@@ -45,31 +54,40 @@ __device__ unsigned int g_gemm_error = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int UM = 128;                     // rows per MMA
-constexpr int RS = 6;                       // raw ring: X tile + code tile
-constexpr int BS = 2;                       // restored B ring
+constexpr int TCH = 128;                    // output channels per tile (MMA M)
+constexpr int TN_MAX = 256;                 // tokens per tile (MMA N), runtime tn <= 256
+constexpr int BK = 64;
+constexpr int RS_MAX = 16;                 // raw ring stages (X tile + codes + statistics)
+constexpr int BS = 3;                       // restored-weight ring (fewer than the raw stages)
 constexpr int RW = 8;                       // restore warps
 constexpr int RT = RW * 32;                 // restore threads
+constexpr int RG = 2;                       // restore groups: k-blocks restored concurrently
+constexpr int RTG = RT / RG;                // threads per restore group
+constexpr int ITEMS = RG;                   // 16-byte code chunks per thread per k-block
 constexpr int EW0 = 2 + RW;                 // first epilogue warp
 constexpr int THREADS = (EW0 + 4) * 32;
-constexpr int ITEMS = BK * BN / 32 / RT;    // 16-byte code chunks per restore thread
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = BK * BN * 2;        // 32 KB
-constexpr int C_BYTES = BK * BN / 2;        // 8 KB of codes (128-byte rows)
-constexpr int S_BYTES = BK * (BN / 64) * 4;  // 1 KB of (a, b) words
-constexpr int SMEM_BYTES = RS * (A_BYTES + C_BYTES + S_BYTES) + BS * B_BYTES +
-                           1024 /*align*/ + 256 /*barriers*/;
-constexpr uint32_t TMEM_COLS = 2 * (BM / UM) * BN;   // two accumulator buffers
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int X_BYTES = TN_MAX * BK * 2;    // 32 KB at tn = 256
+constexpr int W_BYTES = TCH * BK * 2;       // 16 KB restored
+constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
+constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
+constexpr int SMEM_BYTES = 232448;          // the whole per-CTA budget
+constexpr int BAR_BYTES = 512;
+// raw ring: stages of (tn*128 + C_BYTES + S_BYTES) bytes, as many as fit (4 at tn = 256,
+// 13 at tn = 64), so that small token tiles keep enough code bytes in flight to stream HBM
+constexpr int RING_BYTES = SMEM_BYTES - 1024 /*align*/ - BS * W_BYTES - BAR_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * TN_MAX;  // two accumulator buffers
+// the ring arithmetic of the restorers needs more raw stages than A slots
+static_assert(RING_BYTES / (X_BYTES + C_BYTES + S_BYTES) > BS, "raw stages > A slots at tn = 256");
+static_assert((2 * RS_MAX + BS + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
 static_assert(TMEM_COLS == 512, "TMEM budget");
-static_assert(ITEMS * RT * 32 == BK * BN, "restore coverage");
+static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
 constexpr long long kWaitCycles = 1ll << 32;
-constexpr int SWZ_GROUP_M = 8;
+constexpr int SWZ_GROUP = 8;                // token tiles per raster group
 
-// instruction descriptor: D f32, A f16 K-major, B f16 MN-major, N = 256, M = 128
-constexpr uint32_t IDESC = (1u << 4) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(UM >> 4) << 24);
+// instruction descriptor: D f32, A and B f16, A MN-major, B K-major, M = 128, N = tn
+__host__ __device__ constexpr uint32_t make_idesc(int tn) {
+  return (1u << 4) | (1u << 15) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(TCH >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -95,6 +113,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait.  Returns false (and raises the CTA abort flag) on timeout or when another
 // warp already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try(bar, parity)) return true;             // fast path: phase already complete
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (*abort_flag) return false;
@@ -124,11 +143,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -151,6 +170,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -180,7 +202,7 @@ struct EpiArgs {
   int epi;
 };
 
-// Bias / ReLU / residual on 8 consecutive outputs and the fp16 store.
+// Bias / ReLU / residual on 8 consecutive outputs and the fp16 store (reduce kernel).
 __device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int64_t row, int n,
                                           int N) {
   if (ea.bias) {
@@ -214,58 +236,71 @@ __device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int6
   *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
 }
 
-__device__ __forceinline__ void unit_coords(int u, int tiles_m, int tiles_n, int kblocks,
-                                            int kb_per_split, int& m0, int& n0, int& split,
-                                            int& kb_begin, int& kb_end) {
-  const int tiles = tiles_m * tiles_n;
-  split = u / tiles;
-  const int lin = u - split * tiles;
-  // grouped raster: SWZ_GROUP_M m-tiles share a wave of n-tiles
-  const int group_span = SWZ_GROUP_M * tiles_n;
+struct Unit {
+  int t0, c0, split, kb_begin, kb_end;
+};
+
+// Work unit u -> token tile, channel tile and k-block range.  Grouped raster: SWZ_GROUP
+// token tiles share a wave of channel tiles, so a wave of CTAs touches few X tiles.
+__device__ __forceinline__ Unit unit_coords(int u, int tn, int tiles_t, int tiles_c,
+                                            int kblocks, int kb_per_split) {
+  Unit r;
+  const int tiles = tiles_t * tiles_c;
+  r.split = u / tiles;
+  const int lin = u - r.split * tiles;
+  const int group_span = SWZ_GROUP * tiles_c;
   const int grp = lin / group_span;
-  const int first_m = grp * SWZ_GROUP_M;
-  const int gm = min(SWZ_GROUP_M, tiles_m - first_m);
+  const int first_t = grp * SWZ_GROUP;
+  const int gt = min(SWZ_GROUP, tiles_t - first_t);
   const int within = lin - grp * group_span;
-  m0 = (first_m + within % gm) * BM;
-  n0 = (within / gm) * BN;
-  kb_begin = split * kb_per_split;
-  kb_end = min(kblocks, kb_begin + kb_per_split);
+  r.t0 = (first_t + within % gt) * tn;
+  r.c0 = (within / gt) * TCH;
+  r.kb_begin = r.split * kb_per_split;
+  r.kb_end = min(kblocks, r.kb_begin + kb_per_split);
+  return r;
 }
 
+struct KArgs {
+  int M, N, K, tn;
+  uint32_t idesc;
+  int tiles_t, tiles_c, kblocks, kb_per_split, units;
+  int rs;              // raw ring stages
+  int stage_bytes;     // tn*128 + C_BYTES + S_BYTES (a multiple of 1024)
+};
+
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
-                  const __grid_constant__ CUtensorMap tmS, int M, int N, int K, int tiles_m, int tiles_n,
-                  int kblocks, int kb_per_split, int units, EpiArgs ea) {
+gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
+                  const __grid_constant__ CUtensorMap tmS, const KArgs ka, const EpiArgs ea) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;                                  // RS x A_BYTES
-  uint8_t* sC = sA + RS * A_BYTES;                     // RS x C_BYTES
-  uint8_t* sB = sC + RS * C_BYTES;                     // BS x B_BYTES
-  uint32_t* sS = reinterpret_cast<uint32_t*>(sB + BS * B_BYTES);    // RS x 256 words
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + BS * B_BYTES + RS * S_BYTES);
-  // bars: full_raw[RS], empty_raw[RS], full_b[BS], empty_b[BS], acc_full[2], acc_empty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RS + 2 * BS + 4);
+  uint8_t* sW = smem;                                  // BS x W_BYTES (restored weights)
+  uint8_t* ring = sW + BS * W_BYTES;                   // rs stages: X | codes | statistics
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + RING_BYTES);
+  // bars: full_raw[RS_MAX], mma_done[RS_MAX], full_w[BS], acc_full[2], acc_empty[2].
+  // mma_done(s) completes when the MMAs of the k-block held in raw stage s are done: the
+  // producer may then refill the stage and the restorers reuse that k-block's A slot.
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RS_MAX + BS + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
   auto full_raw = [&](int s) { return bar0 + 8u * s; };
-  auto empty_raw = [&](int s) { return bar0 + 8u * (RS + s); };
-  auto full_b = [&](int s) { return bar0 + 8u * (2 * RS + s); };
-  auto empty_b = [&](int s) { return bar0 + 8u * (2 * RS + BS + s); };
-  auto acc_full = [&](int s) { return bar0 + 8u * (2 * RS + 2 * BS + s); };
-  auto acc_empty = [&](int s) { return bar0 + 8u * (2 * RS + 2 * BS + 2 + s); };
+  auto mma_done = [&](int s) { return bar0 + 8u * (RS_MAX + s); };
+  auto full_w = [&](int s) { return bar0 + 8u * (2 * RS_MAX + s); };
+  auto acc_full = [&](int s) { return bar0 + 8u * (2 * RS_MAX + BS + s); };
+  auto acc_empty = [&](int s) { return bar0 + 8u * (2 * RS_MAX + BS + 2 + s); };
+  const int tn = ka.tn, RS = ka.rs, SB = ka.stage_bytes, XB = tn * 128;
+  auto stage_x = [&](int s) { return ring + s * SB; };
+  auto stage_c = [&](int s) { return ring + s * SB + XB; };
+  auto stage_s = [&](int s) { return reinterpret_cast<const uint32_t*>(ring + s * SB + XB + C_BYTES); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init(full_raw(s), 1);
-      mbar_init(empty_raw(s), 1);
+      mbar_init(mma_done(s), 1);
     }
-    for (int s = 0; s < BS; ++s) {
-      mbar_init(full_b(s), RT);                    // every restore thread arrives
-      mbar_init(empty_b(s), 1);
-    }
+    for (int s = 0; s < BS; ++s) mbar_init(full_w(s), RTG);   // one restore group arrives
     for (int s = 0; s < 2; ++s) {
       mbar_init(acc_full(s), 1);
       mbar_init(acc_empty(s), 4);                  // one arrival per epilogue warp
@@ -288,21 +323,25 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int it = 0;
+      const uint32_t stage_tx = (uint32_t)SB;
+      int it = 0, s = 0;
+      uint32_t ph = 0;                                // lap parity of stage s
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        int m0, n0, split, kbb, kbe;
-        unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
-        for (int kb = kbb; kb < kbe; ++kb, ++it) {
-          const int s = it % RS;
-          if (it >= RS && !mbar_wait(empty_raw(s), ((it / RS) & 1) ^ 1, abort_flag)) {
+      for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x) {
+        const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+          if (it >= RS && !mbar_wait(mma_done(s), ph ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(full_raw(s), A_BYTES + C_BYTES + S_BYTES);
-          tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, kb * BK, m0, full_raw(s));
-          tma_load_2d(smem_u32(sC + s * C_BYTES), &tmC, n0 / 2, kb * BK, full_raw(s));
-          tma_load_2d(smem_u32(sS + s * (S_BYTES / 4)), &tmS, n0 / 64, kb * BK, full_raw(s));
+          mbar_expect_tx(full_raw(s), stage_tx);
+          tma_load_2d(smem_u32(stage_x(s)), &tmX, kb * BK, w.t0, full_raw(s));
+          tma_load_2d(smem_u32(stage_c(s)), &tmC, w.c0 / 2, kb * BK, full_raw(s));
+          tma_load_2d(smem_u32(stage_s(s)), &tmS, (w.c0 / 256) * 4, kb * BK, full_raw(s));
+          if (++s == RS) {
+            s = 0;
+            ph ^= 1;
+          }
         }
       }
       // Drain: every issued load must have landed before this CTA can exit.
@@ -319,162 +358,169 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int it = 0, tl = 0;
+      // descriptors of slot 0 / stage 0; a slot or stage offset, and the K16 step, add
+      // (bytes >> 4) to the start-address field (all addresses are below 256 KB)
+      const uint64_t adesc0 = smem_desc(smem_u32(sW), 64 * 128, 1024);
+      const uint64_t bdesc0 = smem_desc(smem_u32(ring), 16, 1024);
+      int tl = 0, s = 0, ws = 0;
+      uint32_t ph_w = 0;                              // lap parity of A slot ws
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tl) {
-        int m0, n0, split, kbb, kbe;
-        unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+      for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x, ++tl) {
+        const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
         const int acc = tl & 1;
         if (tl >= 2 && !mbar_wait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t tacc = tmem + acc * ((BM / UM) * BN);
-        for (int kb = kbb; kb < kbe; ++kb, ++it) {
-          const int s = it % RS, bs = it % BS;
-          if (!mbar_wait(full_raw(s), (it / RS) & 1, abort_flag) ||
-              !mbar_wait(full_b(bs), (it / BS) & 1, abort_flag)) {
+        const uint32_t tacc = tmem + acc * TN_MAX;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          // the restorers of this k-block waited for its raw stage before arriving
+          if (!mbar_wait(full_w(ws), ph_w, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * A_BYTES);
-          const uint32_t b_base = smem_u32(sB + bs * B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bd = smem_desc(b_base + kk * 16 * 128, 64 * 128, 1024);
-            const uint32_t accum = (kb > kbb || kk > 0) ? 1u : 0u;
-#pragma unroll
-            for (int hh = 0; hh < BM / UM; ++hh) {
-              if (m0 + hh * UM >= M) break;         // rows past M: nothing to compute
-              const uint64_t ad = smem_desc(a_base + hh * (UM * 128) + kk * 32, 16, 1024);
-              umma_f16(tacc + hh * BN, ad, bd, accum);
-            }
+          const uint64_t ad = adesc0 + (uint64_t)(ws * (W_BYTES >> 4));
+          const uint64_t bd = bdesc0 + (uint64_t)(s * (SB >> 4));
+          umma_f16(tacc, ad, bd, ka.idesc, kb > w.kb_begin ? 1u : 0u);
+          umma_f16(tacc, ad + 128, bd + 2, ka.idesc, 1u);
+          umma_f16(tacc, ad + 256, bd + 4, ka.idesc, 1u);
+          umma_f16(tacc, ad + 384, bd + 6, ka.idesc, 1u);
+          umma_commit(mma_done(s));
+          if (++s == RS) s = 0;
+          if (++ws == BS) {
+            ws = 0;
+            ph_w ^= 1;
           }
-          umma_commit(empty_raw(s));
-          umma_commit(empty_b(bs));
         }
         umma_commit(acc_full(acc));
       }
     }
   } else if (warp < EW0) {
-    // ------------------------------------------------------------ restore codes -> B
+    // ------------------------------------------------------------ restore codes -> A
+    // RG groups of RTG threads; group g restores the k-blocks it == g (mod RG), so RG
+    // k-blocks are in restoration at once.  Item -> (k-row, 16-byte code chunk c = 32
+    // channels).  Each 8-lane phase takes the two chunks of one 64-channel group on four
+    // k-rows whose (k & 3) differ and whose (k & 1, k & 4) differ, which keeps the
+    // 64B-swizzled code loads and the 128B-swizzled restored stores free of bank conflicts.
     const int tid = threadIdx.x - 64;                 // 0 .. RT-1
-    // items of this thread: k-row and 16-byte code chunk c (32 output channels) of the
-    // 64 x 256 tile; 8 consecutive lanes take 8 consecutive k at one c, which keeps the
-    // swizzled code loads, the statistics loads and the swizzled B stores free of bank
-    // conflicts
-    int ik[ITEMS], ic[ITEMS];
+    const int grp = tid / RTG, tg = tid % RTG;
+    int code_off[ITEMS], stat_k[ITEMS], w_off[ITEMS], sw[ITEMS], cl4[ITEMS];
 #pragma unroll
     for (int t = 0; t < ITEMS; ++t) {
-      const int item = t * RT + tid;
-      ik[t] = (item & 7) | (((item >> 6) & 7) << 3);
-      ic[t] = (item >> 3) & 7;
+      const int item = tg + t * RTG;                  // 0 .. 255
+      const int cl = item & 1, rsel = (item >> 1) & 3, quad = (item >> 3) & 1;
+      const int j = (item >> 4) & 1;
+      const int k = (item >> 5) * 8 + (quad ? 2 + rsel : (rsel < 2 ? rsel : rsel + 4));
+      const int c = 2 * j + cl;
+      code_off[t] = k * 64 + ((c ^ ((k >> 1) & 3)) << 4);
+      stat_k[t] = k * 4 + j;
+      w_off[t] = j * (BK * 128) + k * 128;
+      sw[t] = k & 7;
+      cl4[t] = cl * 4;
     }
-    int it = 0;
+    // ring positions of k-block it (stage s, lap parity ph) and of k-block it - BS, whose
+    // MMAs must be done before its A slot is rewritten (stage so, parity pho)
+    int it = 0, s = 0, so = RS - BS, ws = 0, rg = 0;   // RS > BS
+    uint32_t ph = 0, pho = 1;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      int m0, n0, split, kbb, kbe;
-      unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
-      for (int kb = kbb; kb < kbe; ++kb, ++it) {
-        const int s = it % RS, bs = it % BS;
-        if (!mbar_wait(full_raw(s), (it / RS) & 1, abort_flag) ||
-            (it >= BS && !mbar_wait(empty_b(bs), ((it / BS) & 1) ^ 1, abort_flag))) {
+    for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x) {
+      const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
+      const int g0 = (w.c0 >> 6) & 3;                 // first group of the tile in the box
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+        const int cs_ = s, cws = ws;
+        const uint32_t cph = ph, cpho = pho;
+        const int cso = so;
+        const bool mine = (rg == grp);
+        if (++s == RS) { s = 0; ph ^= 1; }
+        if (++so == RS) { so = 0; pho ^= 1; }
+        if (++ws == BS) ws = 0;
+        if (++rg == RG) rg = 0;
+        if (!mine) continue;
+        if (!mbar_wait(full_raw(cs_), cph, abort_flag) ||
+            (it >= BS && !mbar_wait(mma_done(cso), cpho, abort_flag))) {
           ok = false;
           break;
         }
-        const uint8_t* cs = sC + s * C_BYTES;
-        const uint32_t* ss = sS + s * (S_BYTES / 4);
-        uint8_t* bsm = sB + bs * B_BYTES;
+        const uint8_t* cs = stage_c(cs_);
+        const uint32_t* ss = stage_s(cs_);
+        uint8_t* wb = sW + cws * W_BYTES;
+        uint4 cw[ITEMS];
+        uint32_t abw[ITEMS];
 #pragma unroll
         for (int t = 0; t < ITEMS; ++t) {
-          const int k = ik[t], c = ic[t], sw = k & 7;
-          const uint4 cw = *reinterpret_cast<const uint4*>(cs + k * 128 + ((c ^ sw) << 4));
-          const float2 abf = unpack_h2(ss[k * (BN / 64) + (c >> 1)]);
+          cw[t] = *reinterpret_cast<const uint4*>(cs + code_off[t]);
+          abw[t] = ss[stat_k[t] + g0];
+        }
+#pragma unroll
+        for (int t = 0; t < ITEMS; ++t) {
+          const float2 abf = unpack_h2(abw[t]);
           const float sc16 = (abf.y - abf.x) * (16.0f / 15.0f);
           const uint32_t s16 = pack_h2(sc16, sc16);
           const float cf = abf.x - sc16;
           const uint32_t cc = pack_h2(cf, cf);
-          uint8_t* brow = bsm + (c >> 1) * (BK * 128) + k * 128;
-          const int jc0 = (c & 1) * 4;
-          *reinterpret_cast<uint4*>(brow + (((jc0 + 0) ^ sw) << 4)) = restore8(cw.x, s16, cc);
-          *reinterpret_cast<uint4*>(brow + (((jc0 + 1) ^ sw) << 4)) = restore8(cw.y, s16, cc);
-          *reinterpret_cast<uint4*>(brow + (((jc0 + 2) ^ sw) << 4)) = restore8(cw.z, s16, cc);
-          *reinterpret_cast<uint4*>(brow + (((jc0 + 3) ^ sw) << 4)) = restore8(cw.w, s16, cc);
+          uint8_t* wrow = wb + w_off[t];
+          const int u0 = cl4[t], z = sw[t];
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 0) ^ z) << 4)) = restore8(cw[t].x, s16, cc);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 1) ^ z) << 4)) = restore8(cw[t].y, s16, cc);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 2) ^ z) << 4)) = restore8(cw[t].z, s16, cc);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 3) ^ z) << 4)) = restore8(cw[t].w, s16, cc);
         }
         // make the stores visible to the tensor core's (async) proxy, then arrive
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(full_b(bs));
+        mbar_arrive(full_w(cws));
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // TMEM lane L holds restored row L of the tile: channel (L & ~7) + kPerm[L & 7] with
+    // kPerm = (0,4,1,5,2,6,3,7), the order restore8 leaves the pairs in.
     const int lane_base = 32 * (warp & 3);            // TMEM lanes this warp may read
+    const int L = lane_base + lane;
+    const int ch_in_tile = (L & ~7) + ((L & 7) >> 1) + ((L & 1) << 2);
+    const int64_t N = ka.N;
+    const bool add_res = !ea.partial && ea.epi == FG_EPI_RESIDUAL;
     int tl = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
-      int m0, n0, split, kbb, kbe;
-      unit_coords(u, tiles_m, tiles_n, kblocks, kb_per_split, m0, n0, split, kbb, kbe);
+    for (int u = blockIdx.x; u < ka.units; u += gridDim.x, ++tl) {
+      const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
       const int acc = tl & 1;
+      const int ntok = min(tn, ka.M - w.t0);          // valid tokens of this tile
+      if (add_res) {
+        // pull this tile's residual rows (2 x 128 bytes per token) into L2 while the
+        // accumulator fills
+        for (int i = 32 * (warp & 3) + lane; i < 2 * ntok; i += 128)
+          prefetch_l2(ea.residual + (int64_t)(w.t0 + (i >> 1)) * N + w.c0 + (i & 1) * 64);
+      }
       if (!mbar_wait(acc_full(acc), (tl >> 1) & 1, abort_flag)) break;
       __syncwarp();
       tc_fence_after();
-      for (int hh = 0; hh < BM / UM; ++hh) {
-      const int64_t row = (int64_t)m0 + hh * UM + lane_base + lane;
-      const bool row_ok = row < M;
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        const int nb = n0 + cc * 32;
+      const int64_t ch = w.c0 + ch_in_tile;
+      const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;
+      for (int cb = 0; cb < ntok; cb += 32) {
         // loads that do not depend on the accumulator go first
-        uint4 bias4[4], res4[4];
-        if (!ea.partial && nb < N) {
+        float res[32];
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            bias4[g8] = ea.bias ? ldg_nc_v4(ea.bias + nb + g8 * 8) : make_uint4(0, 0, 0, 0);
-            res4[g8] = (ea.epi == FG_EPI_RESIDUAL && row_ok)
-                           ? *reinterpret_cast<const uint4*>(ea.residual + row * N + nb + g8 * 8)
-                           : make_uint4(0, 0, 0, 0);
-          }
-        }
+        for (int i = 0; i < 32; ++i)
+          res[i] = (add_res && cb + i < ntok)
+                       ? h2f(ea.residual[(int64_t)(w.t0 + cb + i) * N + ch]) : 0.0f;
+        // columns past tn (at most cb + 31 <= 255) stay inside this accumulator's 256
         uint32_t r[32];
-        const uint32_t taddr =
-            tmem + ((uint32_t)lane_base << 16) + acc * ((BM / UM) * BN) + hh * BN + cc * 32;
         __syncwarp();
+        const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + acc * TN_MAX + cb;
         tmem_ld16(taddr, r);
         tmem_ld16(taddr + 16, r + 16);
         tmem_wait_ld();
-        if (!row_ok || nb >= N) continue;
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int n = nb + g8 * 8;
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[i] = __uint_as_float(r[8 * g8 + 2 * i]);
-            v[i + 4] = __uint_as_float(r[8 * g8 + 2 * i + 1]);
-          }
+        for (int i = 0; i < 32; ++i) {
+          if (cb + i >= ntok) break;
+          const int64_t t = w.t0 + cb + i;
+          const float a = __uint_as_float(r[i]);
           if (ea.partial) {
-            float* pp = ea.partial + ((int64_t)split * M + row) * N + n;
-            reinterpret_cast<float4*>(pp)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(pp)[1] = make_float4(v[4], v[5], v[6], v[7]);
+            ea.partial[((int64_t)w.split * ka.M + t) * N + ch] = a;
             continue;
           }
-          const uint32_t bw[4] = {bias4[g8].x, bias4[g8].y, bias4[g8].z, bias4[g8].w};
-          const uint32_t rw[4] = {res4[g8].x, res4[g8].y, res4[g8].z, res4[g8].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 fb = unpack_h2(bw[i]), fr = unpack_h2(rw[i]);
-            v[2 * i] += fb.x + fr.x;
-            v[2 * i + 1] += fb.y + fr.y;
-          }
-          if (ea.epi == FG_EPI_RELU) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = fmaxf(v[i], 0.0f);
-          }
-          uint4 o;
-          o.x = pack_h2(v[0], v[1]);
-          o.y = pack_h2(v[2], v[3]);
-          o.z = pack_h2(v[4], v[5]);
-          o.w = pack_h2(v[6], v[7]);
-          *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
+          float v = a + (bias_f + res[i]);
+          if (ea.epi == FG_EPI_RELU) v = fmaxf(v, 0.0f);
+          ea.Y[t * N + ch] = f2h(v);
         }
-      }
       }
       tc_fence_before();
       __syncwarp();
@@ -542,10 +588,13 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
   GemmPlan p{};
   p.M = M; p.N = N; p.K = K;
-  p.tiles_m = (int)((M + BM - 1) / BM);
-  p.tiles_n = (int)((N + BN - 1) / BN);
+  p.tiles_t = (int)std::max<int64_t>(1, (M + TN_MAX - 1) / TN_MAX);
+  // tokens per tile: the smallest multiple of 16 that covers M in tiles_t tiles
+  const int64_t per = (M + p.tiles_t - 1) / p.tiles_t;
+  p.tn = (int)std::min<int64_t>(TN_MAX, std::max<int64_t>(16, (per + 15) / 16 * 16));
+  p.tiles_c = (int)((N + TCH - 1) / TCH);
   p.kblocks = (int)((K + BK - 1) / BK);
-  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  const int64_t tiles = (int64_t)p.tiles_t * p.tiles_c;
   int splits = 1;
   // Split K only when the tile grid leaves more than a quarter of the SMs idle, keeping
   // at least 8 k-blocks per split so the pipeline stays full.
@@ -570,23 +619,25 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   static cudaError_t attr_err = cudaFuncSetAttribute(
       gemm_q4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
-  CUtensorMap tmA, tmC, tmS;
-  e = make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K, (uint64_t)p.M,
-                  (uint64_t)p.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  CUtensorMap tmX, tmC, tmS;
+  e = make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K, (uint64_t)p.M,
+                  (uint64_t)p.K * 2, BK, (uint32_t)p.tn, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(p.N / 2),
-                  (uint64_t)p.K, (uint64_t)(p.N / 2), BN / 2, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+                  (uint64_t)p.K, (uint64_t)(p.N / 2), TCH / 2, BK, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT32, W.ab, (uint64_t)(p.N / 64),
-                  (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, BN / 64, BK,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+                  (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
-  gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(
-      tmA, tmC, tmS, (int)p.M, (int)p.N, (int)p.K, p.tiles_m, p.tiles_n, p.kblocks,
-      p.kb_per_split, (int)p.units, ea);
+  const int stage_bytes = p.tn * 128 + C_BYTES + S_BYTES;
+  const int rs = std::min(RS_MAX, RING_BYTES / stage_bytes);
+  if (rs <= BS) return cudaErrorInvalidConfiguration;   // restorer ring needs RS > BS
+  const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
+                 p.kblocks, p.kb_per_split, (int)p.units, rs, stage_bytes};
+  gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(tmX, tmC, tmS, ka, ea);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   if (mid_event) cudaEventRecord(mid_event, st);
