@@ -15,20 +15,25 @@
 // row of an MN-major operand, one quantisation group.
 //
 // Persistent kernel: one CTA per SM loops over (split, token tile, channel tile) units,
-// K step 64.
-//   warp 0      TMA producer: X tile (tn x 64, 128B swizzle, K-major), the 128-channel
-//               code tile (64B swizzle) and the group statistics of the aligned 256-channel
-//               block, one transaction per stage, into a ring sized to the shared memory
-//               left (4 stages at tn = 256, 13 at tn = 64); owns the TMEM allocation
+// K step 64.  Two rings in shared memory: a k-block ring of R slots, each an X tile and a
+// restored A tile, freed together by one MMA commit; and a code ring of RC stages (codes +
+// group statistics), freed by the restorers once they have consumed the words.  Depths
+// follow the token tile: R = 4, RC = 6 at tn = 256; R = 6, RC = 16 at tn = 64, where the
+// codes stream from HBM and need more bytes in flight.
+//   warp 0      TMA producer of X tiles (tn x 64, 128B swizzle, K-major); owns TMEM
 //   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=tn, K=16) into one of
-//               two double-buffered fp32 accumulators; one commit per k-block frees both
-//               its raw stage and its restored slot
-//   warps 2-9   two groups of four warps restore alternate k-blocks: codes -> fp16 A tile
-//               in a 3-slot shared-memory ring (MN-major, 128B swizzle), two 16-byte code
-//               chunks (32 channels each) per thread per k-block
-//   warps 10-13 epilogue of the previous tile (tcgen05.ld: one TMEM lane per output
+//               two double-buffered fp32 accumulators; it waits once per k-block, on a
+//               barrier that completes when the A slot is restored AND the X tile landed
+//   warp 2      TMA producer of code tiles (64B swizzle) and the group statistics of the
+//               aligned 256-channel block
+//   warps 3-10  two groups of four warps restore alternate k-blocks: codes -> fp16 A tile
+//               (MN-major, 128B swizzle), two 16-byte code chunks (32 channels each) per
+//               thread per k-block
+//   warps 11-14 epilogue of the previous tile (tcgen05.ld: one TMEM lane per output
 //               channel, 32 tokens per batch; bias / ReLU / residual, fp16 store); with a
 //               residual the tile's rows are prefetched to L2 while the accumulator fills
+// Barrier polls take the non-blocking test_wait first: on the MMA issuer's path the phase
+// is nearly always complete, and test_wait returns several times sooner than try_wait.
 // Restoration per pair of codes: the nibble is OR-ed into mantissa bits 6..9 of 1.0h so
 // that the half equals 1 + q/16, then one HFMA2 gives (1 + q/16)*(16s) + (a - 16s) = a + q*s.
 // Within each 8-channel chunk the pairs land as (n0,n4,n1,n5,n2,n6,n3,n7), so accumulator
@@ -57,30 +62,28 @@ namespace {
 constexpr int TCH = 128;                    // output channels per tile (MMA M)
 constexpr int TN_MAX = 256;                 // tokens per tile (MMA N), runtime tn <= 256
 constexpr int BK = 64;
-constexpr int RS_MAX = 16;                 // raw ring stages (X tile + codes + statistics)
-constexpr int BS = 3;                       // restored-weight ring (fewer than the raw stages)
+constexpr int R_MAX = 8;                    // k-block ring: X tile + restored A slot
+constexpr int RC_MAX = 16;                  // code ring: codes + group statistics
 constexpr int RW = 8;                       // restore warps
 constexpr int RT = RW * 32;                 // restore threads
 constexpr int RG = 2;                       // restore groups: k-blocks restored concurrently
 constexpr int RTG = RT / RG;                // threads per restore group
 constexpr int ITEMS = RG;                   // 16-byte code chunks per thread per k-block
-constexpr int EW0 = 2 + RW;                 // first epilogue warp
+constexpr int RW0 = 3;                      // first restore warp
+constexpr int EW0 = RW0 + RW;               // first epilogue warp
 constexpr int THREADS = (EW0 + 4) * 32;
-constexpr int X_BYTES = TN_MAX * BK * 2;    // 32 KB at tn = 256
 constexpr int W_BYTES = TCH * BK * 2;       // 16 KB restored
 constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
+constexpr int CS_BYTES = C_BYTES + S_BYTES; // one code stage
 constexpr int SMEM_BYTES = 232448;          // the whole per-CTA budget
 constexpr int BAR_BYTES = 512;
-// raw ring: stages of (tn*128 + C_BYTES + S_BYTES) bytes, as many as fit (4 at tn = 256,
-// 13 at tn = 64), so that small token tiles keep enough code bytes in flight to stream HBM
-constexpr int RING_BYTES = SMEM_BYTES - 1024 /*align*/ - BS * W_BYTES - BAR_BYTES;
+constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * TN_MAX;  // two accumulator buffers
-// the ring arithmetic of the restorers needs more raw stages than A slots
-static_assert(RING_BYTES / (X_BYTES + C_BYTES + S_BYTES) > BS, "raw stages > A slots at tn = 256");
-static_assert((2 * RS_MAX + BS + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
+static_assert((2 * R_MAX + 2 * RC_MAX + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
 static_assert(TMEM_COLS == 512, "TMEM budget");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
+static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int SWZ_GROUP = 8;                // token tiles per raster group
 
@@ -110,10 +113,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a phase: far cheaper than try_wait when the phase is already
+// complete, which is the common case on the MMA issuer's path.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
 // Bounded wait.  Returns false (and raises the CTA abort flag) on timeout or when another
 // warp already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try(bar, parity)) return true;             // fast path: phase already complete
+  if (mbar_test(bar, parity)) return true;            // fast path: phase already complete
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (*abort_flag) return false;
@@ -264,8 +276,8 @@ struct KArgs {
   int M, N, K, tn;
   uint32_t idesc;
   int tiles_t, tiles_c, kblocks, kb_per_split, units;
-  int rs;              // raw ring stages
-  int stage_bytes;     // tn*128 + C_BYTES + S_BYTES (a multiple of 1024)
+  int r;               // k-block ring depth (X stage + A slot, freed by one MMA commit)
+  int rc;              // code ring depth
 };
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -274,36 +286,40 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sW = smem;                                  // BS x W_BYTES (restored weights)
-  uint8_t* ring = sW + BS * W_BYTES;                   // rs stages: X | codes | statistics
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + RING_BYTES);
-  // bars: full_raw[RS_MAX], mma_done[RS_MAX], full_w[BS], acc_full[2], acc_empty[2].
-  // mma_done(s) completes when the MMAs of the k-block held in raw stage s are done: the
-  // producer may then refill the stage and the restorers reuse that k-block's A slot.
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RS_MAX + BS + 4);
+  const int tn = ka.tn, R = ka.r, RC = ka.rc, XB = tn * 128;
+  uint8_t* sW = smem;                                  // R x W_BYTES (restored weights)
+  uint8_t* sX = sW + R * W_BYTES;                      // R x XB (activations)
+  uint8_t* sC = sX + R * XB;                           // RC x CS_BYTES (codes | statistics)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + POOL_BYTES);
+  // bars: full[R_MAX], mma_done[R_MAX], full_c[RC_MAX], free_c[RC_MAX], acc_full[2],
+  // acc_empty[2].  full(r) completes when the restore group has written A slot r AND the X
+  // tile of slot r has landed (the X producer's expect_tx arrival plus the TMA bytes), so
+  // the MMA issuer waits once per k-block.  mma_done(r) completes when the MMAs of slot r
+  // are done: its X stage may be refilled and its A slot rewritten.
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * R_MAX + 2 * RC_MAX + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
-  auto full_raw = [&](int s) { return bar0 + 8u * s; };
-  auto mma_done = [&](int s) { return bar0 + 8u * (RS_MAX + s); };
-  auto full_w = [&](int s) { return bar0 + 8u * (2 * RS_MAX + s); };
-  auto acc_full = [&](int s) { return bar0 + 8u * (2 * RS_MAX + BS + s); };
-  auto acc_empty = [&](int s) { return bar0 + 8u * (2 * RS_MAX + BS + 2 + s); };
-  const int tn = ka.tn, RS = ka.rs, SB = ka.stage_bytes, XB = tn * 128;
-  auto stage_x = [&](int s) { return ring + s * SB; };
-  auto stage_c = [&](int s) { return ring + s * SB + XB; };
-  auto stage_s = [&](int s) { return reinterpret_cast<const uint32_t*>(ring + s * SB + XB + C_BYTES); };
+  auto full = [&](int r) { return bar0 + 8u * r; };
+  auto mma_done = [&](int r) { return bar0 + 8u * (R_MAX + r); };
+  auto full_c = [&](int c) { return bar0 + 8u * (2 * R_MAX + c); };
+  auto free_c = [&](int c) { return bar0 + 8u * (2 * R_MAX + RC_MAX + c); };
+  auto acc_full = [&](int a) { return bar0 + 8u * (2 * R_MAX + 2 * RC_MAX + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (2 * R_MAX + 2 * RC_MAX + 2 + a); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RS; ++s) {
-      mbar_init(full_raw(s), 1);
-      mbar_init(mma_done(s), 1);
+    for (int r = 0; r < R; ++r) {
+      mbar_init(full(r), RTG + 1);                 // one restore group + the X producer
+      mbar_init(mma_done(r), 1);
     }
-    for (int s = 0; s < BS; ++s) mbar_init(full_w(s), RTG);   // one restore group arrives
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(acc_full(s), 1);
-      mbar_init(acc_empty(s), 4);                  // one arrival per epilogue warp
+    for (int c = 0; c < RC; ++c) {
+      mbar_init(full_c(c), 1);
+      mbar_init(free_c(c), RTG);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 4);                  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -320,37 +336,51 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0: X tiles into the k-block ring; warp 2: codes + statistics into the code ring
     if (lane == 0) {
-      const uint32_t stage_tx = (uint32_t)SB;
+      const bool is_x = (warp == 0);
+      const int depth = is_x ? R : RC;
       int it = 0, s = 0;
-      uint32_t ph = 0;                                // lap parity of stage s
+      uint32_t ph = 0;                                // lap parity of slot s
       bool ok = true;
       for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x) {
         const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
-          if (it >= RS && !mbar_wait(mma_done(s), ph ^ 1, abort_flag)) {
+          if (it >= depth &&
+              !mbar_wait(is_x ? mma_done(s) : free_c(s), ph ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(full_raw(s), stage_tx);
-          tma_load_2d(smem_u32(stage_x(s)), &tmX, kb * BK, w.t0, full_raw(s));
-          tma_load_2d(smem_u32(stage_c(s)), &tmC, w.c0 / 2, kb * BK, full_raw(s));
-          tma_load_2d(smem_u32(stage_s(s)), &tmS, (w.c0 / 256) * 4, kb * BK, full_raw(s));
-          if (++s == RS) {
+          if (is_x) {
+            mbar_expect_tx(full(s), (uint32_t)XB);
+            tma_load_2d(smem_u32(sX + s * XB), &tmX, kb * BK, w.t0, full(s));
+          } else {
+            uint8_t* cs = sC + s * CS_BYTES;
+            mbar_expect_tx(full_c(s), (uint32_t)CS_BYTES);
+            tma_load_2d(smem_u32(cs), &tmC, w.c0 / 2, kb * BK, full_c(s));
+            tma_load_2d(smem_u32(cs + C_BYTES), &tmS, (w.c0 / 256) * 4, kb * BK, full_c(s));
+          }
+          if (++s == depth) {
             s = 0;
             ph ^= 1;
           }
         }
       }
-      // Drain: every issued load must have landed before this CTA can exit.
-      for (int i = max(0, it - RS); i < it; ++i) {
-        const long long t0 = clock64();
-        while (!mbar_try(full_raw(i % RS), (i / RS) & 1)) {
-          if (clock64() - t0 > kWaitCycles) {
-            atomicOr(&g_gemm_error, 2u);
-            break;
+      // Drain: every issued load must have landed before this CTA can exit.  X tiles land
+      // on the k-block barriers, which the MMA issuer consumes on the normal path; after an
+      // abort their phases may also lack restore arrivals, so those waits are short.
+      if (!is_x || !ok) {
+        const long long limit = is_x ? (1ll << 26) : kWaitCycles;
+        for (int i = max(0, it - depth); i < it; ++i) {
+          const uint32_t bar = is_x ? full(i % depth) : full_c(i % depth);
+          const long long t0 = clock64();
+          while (!mbar_try(bar, (i / depth) & 1)) {
+            if (clock64() - t0 > limit) {
+              atomicOr(&g_gemm_error, 2u);
+              break;
+            }
           }
         }
       }
@@ -358,12 +388,12 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // descriptors of slot 0 / stage 0; a slot or stage offset, and the K16 step, add
-      // (bytes >> 4) to the start-address field (all addresses are below 256 KB)
+      // descriptors of slot 0; a slot offset, and the K16 step, add (bytes >> 4) to the
+      // start-address field (all addresses are below 256 KB)
       const uint64_t adesc0 = smem_desc(smem_u32(sW), 64 * 128, 1024);
-      const uint64_t bdesc0 = smem_desc(smem_u32(ring), 16, 1024);
-      int tl = 0, s = 0, ws = 0;
-      uint32_t ph_w = 0;                              // lap parity of A slot ws
+      const uint64_t bdesc0 = smem_desc(smem_u32(sX), 16, 1024);
+      int tl = 0, r = 0;
+      uint32_t ph = 0;                                // lap parity of slot r
       bool ok = true;
       for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x, ++tl) {
         const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
@@ -372,23 +402,21 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         tc_fence_after();
         const uint32_t tacc = tmem + acc * TN_MAX;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          // the restorers of this k-block waited for its raw stage before arriving
-          if (!mbar_wait(full_w(ws), ph_w, abort_flag)) {
+          if (!mbar_wait(full(r), ph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = adesc0 + (uint64_t)(ws * (W_BYTES >> 4));
-          const uint64_t bd = bdesc0 + (uint64_t)(s * (SB >> 4));
+          const uint64_t ad = adesc0 + (uint64_t)(r * (W_BYTES >> 4));
+          const uint64_t bd = bdesc0 + (uint64_t)(r * (XB >> 4));
           umma_f16(tacc, ad, bd, ka.idesc, kb > w.kb_begin ? 1u : 0u);
           umma_f16(tacc, ad + 128, bd + 2, ka.idesc, 1u);
           umma_f16(tacc, ad + 256, bd + 4, ka.idesc, 1u);
           umma_f16(tacc, ad + 384, bd + 6, ka.idesc, 1u);
-          umma_commit(mma_done(s));
-          if (++s == RS) s = 0;
-          if (++ws == BS) {
-            ws = 0;
-            ph_w ^= 1;
+          umma_commit(mma_done(r));
+          if (++r == R) {
+            r = 0;
+            ph ^= 1;
           }
         }
         umma_commit(acc_full(acc));
@@ -401,7 +429,7 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     // channels).  Each 8-lane phase takes the two chunks of one 64-channel group on four
     // k-rows whose (k & 3) differ and whose (k & 1, k & 4) differ, which keeps the
     // 64B-swizzled code loads and the 128B-swizzled restored stores free of bank conflicts.
-    const int tid = threadIdx.x - 64;                 // 0 .. RT-1
+    const int tid = threadIdx.x - 32 * RW0;           // 0 .. RT-1
     const int grp = tid / RTG, tg = tid % RTG;
     int code_off[ITEMS], stat_k[ITEMS], w_off[ITEMS], sw[ITEMS], cl4[ITEMS];
 #pragma unroll
@@ -417,32 +445,28 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       sw[t] = k & 7;
       cl4[t] = cl * 4;
     }
-    // ring positions of k-block it (stage s, lap parity ph) and of k-block it - BS, whose
-    // MMAs must be done before its A slot is rewritten (stage so, parity pho)
-    int it = 0, s = 0, so = RS - BS, ws = 0, rg = 0;   // RS > BS
-    uint32_t ph = 0, pho = 1;
+    // ring positions of k-block it: code stage c (lap parity phc) and slot r (parity phr);
+    // the slot is free once the MMAs of k-block it - R (same slot, parity phr ^ 1) are done
+    int it = 0, c = 0, r = 0, rg = 0;
+    uint32_t phc = 0, phr = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x) {
       const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
       const int g0 = (w.c0 >> 6) & 3;                 // first group of the tile in the box
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
-        const int cs_ = s, cws = ws;
-        const uint32_t cph = ph, cpho = pho;
-        const int cso = so;
+        const int cc_ = c, cr = r;
+        const uint32_t cphc = phc, cphr = phr;
         const bool mine = (rg == grp);
-        if (++s == RS) { s = 0; ph ^= 1; }
-        if (++so == RS) { so = 0; pho ^= 1; }
-        if (++ws == BS) ws = 0;
+        if (++c == RC) { c = 0; phc ^= 1; }
+        if (++r == R) { r = 0; phr ^= 1; }
         if (++rg == RG) rg = 0;
         if (!mine) continue;
-        if (!mbar_wait(full_raw(cs_), cph, abort_flag) ||
-            (it >= BS && !mbar_wait(mma_done(cso), cpho, abort_flag))) {
+        if (!mbar_wait(full_c(cc_), cphc, abort_flag)) {
           ok = false;
           break;
         }
-        const uint8_t* cs = stage_c(cs_);
-        const uint32_t* ss = stage_s(cs_);
-        uint8_t* wb = sW + cws * W_BYTES;
+        const uint8_t* cs = sC + cc_ * CS_BYTES;
+        const uint32_t* ss = reinterpret_cast<const uint32_t*>(cs + C_BYTES);
         uint4 cw[ITEMS];
         uint32_t abw[ITEMS];
 #pragma unroll
@@ -450,23 +474,30 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
           cw[t] = *reinterpret_cast<const uint4*>(cs + code_off[t]);
           abw[t] = ss[stat_k[t] + g0];
         }
+        if (it >= R && !mbar_wait(mma_done(cr), cphr ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* wb = sW + cr * W_BYTES;
 #pragma unroll
         for (int t = 0; t < ITEMS; ++t) {
           const float2 abf = unpack_h2(abw[t]);
           const float sc16 = (abf.y - abf.x) * (16.0f / 15.0f);
           const uint32_t s16 = pack_h2(sc16, sc16);
           const float cf = abf.x - sc16;
-          const uint32_t cc = pack_h2(cf, cf);
+          const uint32_t ccst = pack_h2(cf, cf);
           uint8_t* wrow = wb + w_off[t];
           const int u0 = cl4[t], z = sw[t];
-          *reinterpret_cast<uint4*>(wrow + (((u0 + 0) ^ z) << 4)) = restore8(cw[t].x, s16, cc);
-          *reinterpret_cast<uint4*>(wrow + (((u0 + 1) ^ z) << 4)) = restore8(cw[t].y, s16, cc);
-          *reinterpret_cast<uint4*>(wrow + (((u0 + 2) ^ z) << 4)) = restore8(cw[t].z, s16, cc);
-          *reinterpret_cast<uint4*>(wrow + (((u0 + 3) ^ z) << 4)) = restore8(cw[t].w, s16, cc);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 0) ^ z) << 4)) = restore8(cw[t].x, s16, ccst);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 1) ^ z) << 4)) = restore8(cw[t].y, s16, ccst);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 2) ^ z) << 4)) = restore8(cw[t].z, s16, ccst);
+          *reinterpret_cast<uint4*>(wrow + (((u0 + 3) ^ z) << 4)) = restore8(cw[t].w, s16, ccst);
         }
+        // the code stage may be refilled: its words have been consumed by the stores above
+        mbar_arrive(free_c(cc_));
         // make the stores visible to the tensor core's (async) proxy, then arrive
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(full_w(cws));
+        mbar_arrive(full(cr));
       }
     }
   } else {
@@ -632,11 +663,15 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
-  const int stage_bytes = p.tn * 128 + C_BYTES + S_BYTES;
-  const int rs = std::min(RS_MAX, RING_BYTES / stage_bytes);
-  if (rs <= BS) return cudaErrorInvalidConfiguration;   // restorer ring needs RS > BS
+  // ring depths: small token tiles (decode) keep 16 code stages (80 KB of codes from HBM
+  // in flight per SM); large ones trade code stages for k-block slots
+  const int per_k = W_BYTES + p.tn * 128;
+  const int rc_target = (p.tn <= 128) ? RC_MAX : 6;
+  const int r = std::min(R_MAX, (POOL_BYTES - rc_target * CS_BYTES) / per_k);
+  const int rc = std::min(RC_MAX, (POOL_BYTES - r * per_k) / CS_BYTES);
+  if (r < 3 || rc < 2) return cudaErrorInvalidConfiguration;
   const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
-                 p.kblocks, p.kb_per_split, (int)p.units, rs, stage_bytes};
+                 p.kblocks, p.kb_per_split, (int)p.units, r, rc};
   gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(tmX, tmC, tmS, ka, ea);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;

@@ -217,6 +217,30 @@ def test_gemm_full_size_sampled(fg, M, K, N, epi):
     assert_close(got, ref, f"gemm full M={M} K={K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N,epi", [
+    (8192, 4096, 4096, 2),         # prefill O projection with residual, 1024 tiles
+    (18432, 12288, 4096, 0),       # long K: 192 k-blocks per tile
+    (64, 16384, 4096, 2),          # decode FC2: split K + reduce
+])
+def test_gemm_repeat_bit_identical(fg, M, K, N, epi):
+    """The pipelined GEMM is deterministic: repeated launches on the same inputs give the
+    same bits, which a race between its shared-memory producers and consumers would break."""
+    seed = 7 * M + K + N
+    X = dev(fg_synth.random_fp16((M, K), seed, 1.0))
+    W = fg.Q4Weight.from_fp16(dev(fg_synth.random_fp16((K, N), seed + 1, 0.02)))
+    res = dev(fg_synth.random_fp16((M, N), seed + 3, 1.0)) if epi == 2 else None
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    outs = []
+    for _ in range(3):
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        fg.fg_dequant_gemm_q4(X, W, None, epi, res, Y, ws)
+        outs.append(Y)
+    fg.fg_check_device_error()
+    for Y in outs[1:]:
+        assert torch.equal(Y.view(torch.int16), outs[0].view(torch.int16))
+
+
 # ----------------------------------------------------------------------------- decode attention
 
 
