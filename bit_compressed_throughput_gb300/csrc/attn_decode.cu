@@ -295,8 +295,6 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           va[r][g] = vap[row * NG + g];
         }
       }
-      __syncwarp();                       // every lane is done with this slot
-      if (lane == 0) issue();             // refill it kRing tiles ahead
       const int t0 = it.t_begin + j * kTile;
 
       // ---- scores: K codes (rows t) x permuted q, one column per group
@@ -394,6 +392,10 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
         mma16816(acc[2 * w + 1], movtrans(c0[2]), movtrans(c0[3]), movtrans(c1[2]),
                  movtrans(c1[3]), bv0, bv1);
       }
+      // every lane has consumed the words it loaded from this slot: refill it kRing tiles
+      // ahead (releasing it any earlier would let the copy race the slot's last readers)
+      __syncwarp();
+      if (lane == 0) issue();
     }
     if (!ok) break;
 
