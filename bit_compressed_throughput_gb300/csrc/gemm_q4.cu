@@ -24,11 +24,14 @@
 //   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=tn, K=16) into one of
 //               two double-buffered fp32 accumulators; it waits once per k-block, on a
 //               barrier that completes when the A slot is restored AND the X tile landed
+//   warp 15     with tn <= 128, a second issuing thread: the two take alternate k-blocks
+//               into their own accumulators (one thread cannot keep the tensor pipe busy
+//               with N <= 128 MMAs); the epilogue adds the pair
 //   warp 2      TMA producer of code tiles (64B swizzle) and the group statistics of the
 //               aligned 256-channel block
-//   warps 3-10  two groups of four warps restore alternate k-blocks: codes -> fp16 A tile
-//               (MN-major, 128B swizzle), two 16-byte code chunks (32 channels each) per
-//               thread per k-block
+//   warps 3-10  four groups of two warps restore every fourth k-block: codes -> fp16 A
+//               tile (MN-major, 128B swizzle), four 16-byte code chunks (32 channels each)
+//               per thread per k-block
 //   warps 11-14 epilogue of the previous tile (tcgen05.ld: one TMEM lane per output
 //               channel, 32 tokens per batch; bias / ReLU / residual, fp16 store); with a
 //               residual the tile's rows are prefetched to L2 while the accumulator fills
@@ -66,12 +69,13 @@ constexpr int R_MAX = 8;                    // k-block ring: X tile + restored A
 constexpr int RC_MAX = 16;                  // code ring: codes + group statistics
 constexpr int RW = 8;                       // restore warps
 constexpr int RT = RW * 32;                 // restore threads
-constexpr int RG = 2;                       // restore groups: k-blocks restored concurrently
+constexpr int RG = 4;                       // restore groups: k-blocks restored concurrently
 constexpr int RTG = RT / RG;                // threads per restore group
 constexpr int ITEMS = RG;                   // 16-byte code chunks per thread per k-block
 constexpr int RW0 = 3;                      // first restore warp
 constexpr int EW0 = RW0 + RW;               // first epilogue warp
-constexpr int THREADS = (EW0 + 4) * 32;
+constexpr int MW1 = EW0 + 4;                // second MMA issuer warp (token tiles <= 128)
+constexpr int THREADS = (MW1 + 1) * 32;
 constexpr int W_BYTES = TCH * BK * 2;       // 16 KB restored
 constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
@@ -277,6 +281,7 @@ struct KArgs {
   uint32_t idesc;
   int tiles_t, tiles_c, kblocks, kb_per_split, units;
   int r;               // k-block ring depth (X stage + A slot, freed by one MMA commit)
+  int ni;              // MMA issuers: 2 for tn <= 128 (k-blocks alternate, 2 accumulators)
   int rc;              // code ring depth
 };
 
@@ -318,7 +323,7 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       mbar_init(free_c(c), RTG);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(acc_full(a), 1);
+      mbar_init(acc_full(a), ka.ni);               // one commit per MMA issuer
       mbar_init(acc_empty(a), 4);                  // one arrival per epilogue warp
     }
     *abort_flag = 0;
@@ -385,38 +390,56 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == MW1) {
+    // ------------------------------------------------------------ MMA issuers
+    // With ni = 2 (token tiles of at most 128), issuer mi takes the k-blocks it == mi
+    // (mod 2), which restore group mi restores, into its own accumulator (columns
+    // acc * 256 + mi * 128): a single issuing thread cannot keep the tensor pipe busy with
+    // N <= 128 MMAs.  The epilogue adds the two accumulators.
+    const int mi = (warp == 1) ? 0 : 1;
+    if (lane == 0 && mi < ka.ni) {
       // descriptors of slot 0; a slot offset, and the K16 step, add (bytes >> 4) to the
       // start-address field (all addresses are below 256 KB)
       const uint64_t adesc0 = smem_desc(smem_u32(sW), 64 * 128, 1024);
       const uint64_t bdesc0 = smem_desc(smem_u32(sX), 16, 1024);
+      // descriptors of the current slot advance with the ring; parity by bit test (ni is
+      // 1 or 2): this thread's bookkeeping sits on the MMA stream's critical path
+      const uint64_t a_step = W_BYTES >> 4, b_step = (uint64_t)(XB >> 4);
+      uint64_t ad = adesc0, bd = bdesc0;
       int tl = 0, r = 0;
-      uint32_t ph = 0;                                // lap parity of slot r
+      uint32_t ph = 0, par = 0;                       // lap parity of slot r; k-block parity
+      const uint32_t mask = (ka.ni == 2) ? 1u : 0u;
       bool ok = true;
       for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x, ++tl) {
         const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
         const int acc = tl & 1;
         if (tl >= 2 && !mbar_wait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t tacc = tmem + acc * TN_MAX;
+        const uint32_t tacc = tmem + acc * TN_MAX + mi * 128;
+        uint32_t accumulate = 0u;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (!mbar_wait(full(r), ph, abort_flag)) {
-            ok = false;
-            break;
+          if ((par & mask) == (uint32_t)mi) {
+            if (!mbar_wait(full(r), ph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            umma_f16(tacc, ad, bd, ka.idesc, accumulate);
+            umma_f16(tacc, ad + 128, bd + 2, ka.idesc, 1u);
+            umma_f16(tacc, ad + 256, bd + 4, ka.idesc, 1u);
+            umma_f16(tacc, ad + 384, bd + 6, ka.idesc, 1u);
+            umma_commit(mma_done(r));
+            accumulate = 1u;
           }
-          tc_fence_after();
-          const uint64_t ad = adesc0 + (uint64_t)(r * (W_BYTES >> 4));
-          const uint64_t bd = bdesc0 + (uint64_t)(r * (XB >> 4));
-          umma_f16(tacc, ad, bd, ka.idesc, kb > w.kb_begin ? 1u : 0u);
-          umma_f16(tacc, ad + 128, bd + 2, ka.idesc, 1u);
-          umma_f16(tacc, ad + 256, bd + 4, ka.idesc, 1u);
-          umma_f16(tacc, ad + 384, bd + 6, ka.idesc, 1u);
-          umma_commit(mma_done(r));
+          ++par;
           if (++r == R) {
             r = 0;
             ph ^= 1;
+            ad = adesc0;
+            bd = bdesc0;
+          } else {
+            ad += a_step;
+            bd += b_step;
           }
         }
         umma_commit(acc_full(acc));
@@ -539,6 +562,18 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         tmem_ld16(taddr, r);
         tmem_ld16(taddr + 16, r + 16);
         tmem_wait_ld();
+        if (ka.ni == 2) {
+          // second issuer's accumulator, columns + 128 (tn <= 128 so cb + 31 < 128 + 128)
+          uint32_t r2[16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld16(taddr + 128 + 16 * h, r2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              r[16 * h + i] = __float_as_uint(__uint_as_float(r[16 * h + i]) + __uint_as_float(r2[i]));
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (cb + i >= ntok) break;
@@ -670,8 +705,12 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const int r = std::min(R_MAX, (POOL_BYTES - rc_target * CS_BYTES) / per_k);
   const int rc = std::min(RC_MAX, (POOL_BYTES - r * per_k) / CS_BYTES);
   if (r < 3 || rc < 2) return cudaErrorInvalidConfiguration;
+  // two MMA issuers when the token tile fits two accumulators per buffer and every unit
+  // has at least one k-block for each
+  const int last_unit_kb = p.kblocks - (p.splits - 1) * p.kb_per_split;
+  const int ni = (p.tn <= 128 && p.kb_per_split >= 2 && last_unit_kb >= 2) ? 2 : 1;
   const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
-                 p.kblocks, p.kb_per_split, (int)p.units, r, rc};
+                 p.kblocks, p.kb_per_split, (int)p.units, r, ni, rc};
   gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(tmX, tmC, tmS, ka, ea);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;

@@ -172,6 +172,8 @@ def gemm_case(fg, M, K, N, epi, with_bias, seed, alias=False):
     (130, 80, 512, 0, False),       # K ragged inside a 64-block
     (300, 512, 2048, 1, False),     # several m tiles in one raster group
     (1100, 256, 256, 0, True),      # 9 m tiles (two raster groups)
+    (48, 320, 512, 1, True),        # odd k-block count split over two MMA issuers
+    (64, 1344, 256, 2, True),       # split K with an odd number of k-blocks per split
 ])
 def test_gemm_small(fg, M, K, N, epi, bias):
     gemm_case(fg, M, K, N, epi, bias, seed=M * 31 + K + N)
