@@ -38,6 +38,24 @@ __device__ __forceinline__ uint32_t q4_code(float xf, float af, float bma) {
   return (uint32_t)q;
 }
 
+// The same code with the division replaced, where that cannot change the result, by a
+// multiply: y = fl(d * c15) with d = fl(x - a) and c15 = fl(15 * fl(1 / bma)).  Both y and
+// fl(q), q = fl(d * 15) / bma, equal 15 d / bma times at most three (y) or two (fl(q))
+// factors (1 + e), |e| <= 2^-24; since a <= x <= b makes 15 d / bma <= 15 (1 + 2^-24),
+// |y - fl(q)| <= 16 * 5 * 2^-24 < 2^-17.  So rint(y) == rint(fl(q)) unless y lies within
+// 2^-17 of a half-integer; within 2^-16 of one, or outside [0, 32), the exact division
+// decides.  The rounded code is at most 15, so it needs no clamp.  Codes are therefore
+// bit-identical to q4_code.
+__device__ __forceinline__ uint32_t q4_code_rcp(float xf, float af, float bma, float c15) {
+  if (bma == 0.0f) return 0u;
+  const float d = __fsub_rn(xf, af);
+  const float y = __fmul_rn(d, c15);
+  float q = rintf(y);
+  if (!(y >= 0.0f && y < 32.0f) || fabsf(y - q) > 0.5f - 0x1p-16f)
+    q = rintf(__fdiv_rn(__fmul_rn(d, 15.0f), bma));
+  return (uint32_t)q;
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -20,30 +20,41 @@ namespace {
 constexpr int kThreads = 256;                 // 32 groups per CTA
 constexpr int kGroupsPerCta = kThreads / 8;
 
+// Order keys of the two fp16 values of a word, one per 16-bit lane: unsigned order of a
+// key is the numeric order of the value, with -0 below +0 (key = u ^ 0x8000 for a clear
+// sign bit, u ^ 0xFFFF for a set one).
+__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;
+  return w ^ (0x80008000u | (neg * 0x7FFFu));
+}
+
 // Quantise the 8 values held by this thread (part of a 64-group spread over 8 lanes).
-// Returns the packed codes; *ab_out receives the group's statistics word.
+// Returns the packed codes; *ab_out receives the group's statistics word.  The group min
+// and max travel as one word (min key | ~max key << 16) reduced with a 16-bit SIMD min.
 __device__ __forceinline__ uint32_t quantize8(const uint4 v, uint32_t* ab_out) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  uint32_t kmin2 = order_keys2(w[0]), kmax2 = kmin2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = order_key(w[i] & 0xFFFFu), hi = order_key(w[i] >> 16);
-    kmin = min(kmin, min(lo, hi));
-    kmax = max(kmax, max(lo, hi));
+  for (int i = 1; i < 4; ++i) {
+    const uint32_t k2 = order_keys2(w[i]);
+    kmin2 = __vminu2(kmin2, k2);
+    kmax2 = __vmaxu2(kmax2, k2);
   }
+  const uint32_t kmin = min(kmin2 & 0xFFFFu, kmin2 >> 16);
+  const uint32_t kmax = max(kmax2 & 0xFFFFu, kmax2 >> 16);
+  uint32_t mm = kmin | ((~kmax & 0xFFFFu) << 16);
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
-  }
-  const uint32_t abits = key_to_bits(kmin), bbits = key_to_bits(kmax);
+  for (int o = 1; o < 8; o <<= 1) mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
+  const uint32_t abits = key_to_bits(mm & 0xFFFFu), bbits = key_to_bits(~(mm >> 16) & 0xFFFFu);
   const float af = h2f((uint16_t)abits), bf = h2f((uint16_t)bbits);
   const float bma = __fsub_rn(bf, af);
+  const float c15 = __fmul_rn(15.0f, __frcp_rn(bma));
   uint32_t codes = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t c0 = q4_code(h2f((uint16_t)(w[i] & 0xFFFFu)), af, bma);
-    const uint32_t c1 = q4_code(h2f((uint16_t)(w[i] >> 16)), af, bma);
+    const float2 x2 = unpack_h2(w[i]);
+    const uint32_t c0 = q4_code_rcp(x2.x, af, bma, c15);
+    const uint32_t c1 = q4_code_rcp(x2.y, af, bma, c15);
     codes |= (c0 | (c1 << 4)) << (8 * i);
   }
   *ab_out = abits | (bbits << 16);
@@ -67,13 +78,56 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t ngroups, uint8_t* __rest
   }
 }
 
-// One CTA slice covers groups of the rows (b, t) of K and V: blockIdx.y selects K (0)
-// or V (1).  Row r = b*T + t of the source lives at r*row_stride elements.
+// One CTA covers a block of positions of one (sequence b, head) of K or V (blockIdx.z):
+// thread = (position, group of the head, 8-value slice), kPosPerThread positions apart,
+// whose loads are all issued before any is used so that enough bytes are in flight per SM.
+// The codes of the block's positions are then contiguous runs of the head-major cache
+// (d/2 bytes per position) and so are their (a, b) words, so the writes coalesce; the
+// reads are the head's d values of each source row.  Row r = b*T + t lives at r*row_stride.
+constexpr int kPosPerThread = 4;
 __global__ void __launch_bounds__(kThreads)
 kv_append_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
-                 int64_t row_stride, int T, int pos, int H, int d, int cap, int gpr,
-                 int64_t ngroups, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                 int64_t row_stride, int T, int pos, int H, int d, int cap, int ppc,
+                 uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
                  uint32_t* __restrict__ k_ab, uint32_t* __restrict__ v_ab) {
+  const int gph = d >> 6;                            // groups per head (1 or 2)
+  const int b = blockIdx.x / H, head = blockIdx.x - b * H;
+  const int p0 = threadIdx.x / (8 * gph);            // first position within the block
+  const int pstep = kThreads / (8 * gph);            // ppc / kPosPerThread
+  const int gs = (threadIdx.x >> 3) % gph, sub = threadIdx.x & 7;
+  const uint16_t* src = blockIdx.z ? v_new : k_new;
+  uint8_t* cdst = blockIdx.z ? v_codes : k_codes;
+  uint32_t* adst = blockIdx.z ? v_ab : k_ab;
+  uint4 v[kPosPerThread];
+#pragma unroll
+  for (int i = 0; i < kPosPerThread; ++i) {
+    const int t = blockIdx.y * ppc + p0 + i * pstep;
+    v[i] = make_uint4(0, 0, 0, 0);
+    if (t < T)
+      v[i] = ldg_nc_v4(src + ((int64_t)b * T + t) * row_stride + head * d + gs * 64 + sub * 8);
+  }
+#pragma unroll
+  for (int i = 0; i < kPosPerThread; ++i) {
+    const int t = blockIdx.y * ppc + p0 + i * pstep;
+    // every lane of a warp takes part in the shuffles; positions past the end use a dummy
+    uint32_t abw;
+    const uint32_t c = quantize8(v[i], &abw);
+    if (t < T) {
+      const int64_t slot = ((int64_t)b * H + head) * cap + pos + t;
+      reinterpret_cast<uint32_t*>(cdst + slot * (d >> 1) + gs * 32)[sub] = c;
+      if (sub == 0) adst[slot * gph + gs] = abw;
+    }
+  }
+}
+
+// Short appends (decode: a few positions per sequence): 8 threads per group over the
+// groups of the new rows (b, t) in row order, so every thread has work.
+__global__ void __launch_bounds__(kThreads)
+kv_append_rows_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                      int64_t row_stride, int T, int pos, int H, int d, int cap, int gpr,
+                      int64_t ngroups, uint8_t* __restrict__ k_codes,
+                      uint8_t* __restrict__ v_codes, uint32_t* __restrict__ k_ab,
+                      uint32_t* __restrict__ v_ab) {
   const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   const bool live = grp < ngroups;
@@ -89,7 +143,7 @@ kv_append_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict_
   uint32_t abw;
   const uint32_t c = quantize8(v, &abw);
   if (live) {
-    const int gph = d >> 6;                       // groups per head
+    const int gph = d >> 6;
     const int64_t b = row / T;
     const int t = (int)(row - b * T);
     const int head = gi / gph, gs = gi - head * gph;
@@ -147,13 +201,23 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t row
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
                              int32_t T, int32_t pos, const fg_kvcache& kv, cudaStream_t st) {
-  const int gpr = kv.h / 64;
-  const int64_t ng = (int64_t)kv.B * T * gpr;
-  if (ng == 0) return cudaSuccess;
+  if ((int64_t)kv.B * T == 0) return cudaSuccess;
   const int d = kv.h / kv.H;
-  dim3 grid(grid_for(ng), 2);
+  if (T < 8) {
+    const int gpr = kv.h / 64;
+    const int64_t ng = (int64_t)kv.B * T * gpr;
+    dim3 grid(grid_for(ng), 2);
+    kv_append_rows_kernel<<<grid, kThreads, 0, st>>>(k_new, v_new, row_stride, T, pos, kv.H, d,
+                                                     kv.cap, gpr, ng, kv.k_codes, kv.v_codes,
+                                                     kv.k_ab, kv.v_ab);
+    return cudaGetLastError();
+  }
+  const int ppc = kPosPerThread * kThreads / (8 * (d / 64));   // 64 (d = 128) or 128
+  const int64_t tblocks = (T + ppc - 1) / ppc;
+  if (tblocks > 65535 || (int64_t)kv.B * kv.H > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)(kv.B * kv.H), (unsigned)tblocks, 2);
   kv_append_kernel<<<grid, kThreads, 0, st>>>(k_new, v_new, row_stride, T, pos, kv.H, d, kv.cap,
-                                              gpr, ng, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
+                                              ppc, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
   return cudaGetLastError();
 }
 
