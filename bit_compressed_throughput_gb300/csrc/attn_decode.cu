@@ -11,12 +11,11 @@
 //   q . k^  = sum_g ( s_g * sum_{j in g} c_j q_j  +  a_g * Q_g ),  Q_g = sum_{j in g} q_j
 //   sum_t p_t v^_tj = sum_t (p_t s_tg) c_tj + sum_t p_t a_tg
 // so the per-element work is a dot product of integer codes with fp16 weights.  A nibble
-// OR-ed into the mantissa of 1024.0h gives the exact half 1024 + c (nibble at bit 0) or
-// 1024 + 16c (nibble at bit 4), so one shift per 32-bit word of codes suffices; the 16 is
-// folded into q (K side) or into the epilogue (V side), and the 1024 offsets are removed
-// algebraically: 1024 * sum(q) per group on the K side and 1024 * sum_t w_t on the V side.
-// The dot products run on mma.sync m16n8k16 with fp32 accumulation (the products are
-// exact in fp32).
+// masked in place is an exact fp16 subnormal: c * 2^-24 (nibble at bit 0) or 16c * 2^-24
+// (nibble at bit 4), so one shift and one AND per pair of codes suffice, with no offset to
+// remove; the 16 is folded into q (K side) or into the epilogue (V side), and 2^24 into the
+// group scale.  The dot products run on mma.sync m16n8k16 with fp32 accumulation (the
+// products are exact in fp32).
 //
 // Memory pipeline: a warp owns a flattened stream of 16-position tiles over its work
 // items (b, hd, split).  Lane 0 keeps kRing tiles in flight with 1-D bulk async copies
@@ -69,14 +68,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// The four pairs (c_i, c_{i+4}) of a code word as halves: pairs 0 and 2 hold 1024 + c,
-// pairs 1 and 3 hold 1024 + 16c (factor kPairScale[i]).
+// The four pairs (c_i, c_{i+4}) of a code word as fp16 subnormals: pairs 0 and 2 hold
+// c * 2^-24, pairs 1 and 3 hold 16c * 2^-24.
 __device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {
   const uint32_t w8 = w >> 8;
-  p[0] = (w & 0x000F000Fu) | 0x64006400u;
-  p[1] = (w & 0x00F000F0u) | 0x64006400u;
-  p[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  p[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+  p[0] = w & 0x000F000Fu;
+  p[1] = w & 0x00F000F0u;
+  p[2] = w8 & 0x000F000Fu;
+  p[3] = w8 & 0x00F000F0u;
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -94,6 +93,14 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   return r;
 }
 
+// 2^x on the special-function unit; inputs are <= 8 (lazy rescaling) or -inf, results that
+// would be subnormal flush to zero, which only drops terms below 2^-126 of the largest.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void bar_init(uint32_t bar) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
 }
@@ -108,8 +115,16 @@ __device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait; false (and the device error word set) if it ran out.
+// Bounded wait; false (and the device error word set) if it ran out.  The non-blocking
+// test_wait goes first: a slot's copies have usually landed by the time it is consumed.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+  }
   const long long t0 = clock64();
   while (!bar_try(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) {
@@ -220,8 +235,8 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
     };
     const int my_group = (NG == 2) ? (tig >> 1) : 0;
     // B fragments: q for pairs with factor 1, q/16 (exact) for pairs with factor 16;
-    // qsum = sum of q, qoff = 1024 * sum of the B values (the codes' 1024 offset)
-    float qsum = 0.0f, qoff = 0.0f;
+    // qsum = sum of q
+    float qsum = 0.0f;
     uint32_t bq[2 * NW][2];
 #pragma unroll
     for (int s = 0; s < 2 * NW; ++s) {
@@ -236,22 +251,19 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), *reinterpret_cast<const __half2*>(&k16));
           v = *reinterpret_cast<uint32_t*>(&h);
         }
-        const float2 fb = unpack_h2(v);
-        qoff += 1024.0f * (fb.x + fb.y);
         bq[s][r] = (gid == my_group) ? v : 0u;
       }
     }
     // sum over the lanes sharing this group: tig pairs (NG == 2) or all four (NG == 1)
     qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
-    qoff += __shfl_xor_sync(0xFFFFFFFFu, qoff, 1);
+
     if (NG == 1) {
       qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
-      qoff += __shfl_xor_sync(0xFFFFFFFFu, qoff, 2);
+
     }
     const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3);
     const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) : 0.0f;
-    const float O0 = __shfl_sync(0xFFFFFFFFu, qoff, lane & ~3);
-    const float O1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qoff, (lane & ~3) | 2) : 0.0f;
+
 
     float m_run = -INFINITY, l_run = 0.0f;
     float acc[2 * NW][4];
@@ -259,9 +271,9 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
     for (int u = 0; u < 2 * NW; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-    float asum[NG], wsum[NG];           // sum_t p_t a_tg and sum_t w_tg (1024 offset)
+    float asum[NG];                     // sum_t p_t a_tg
 #pragma unroll
-    for (int g = 0; g < NG; ++g) asum[g] = wsum[g] = 0.0f;
+    for (int g = 0; g < NG; ++g) asum[g] = 0.0f;
 
     for (int j = 0; j < it.ntiles; ++j, ++gc) {
       const int s = (int)(gc % kRing);
@@ -313,10 +325,11 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float2 ab0 = unpack_h2(ka[r][0]);
-        float v = (ab0.y - ab0.x) * (1.0f / 15.0f) * (dk[2 * r] - O0) + ab0.x * Q0;
+        // dk holds 2^-24 * sum_j c_j q_j: fold 2^24 into the group scale
+        float v = (ab0.y - ab0.x) * (16777216.0f / 15.0f) * dk[2 * r] + ab0.x * Q0;
         if (NG == 2) {
           const float2 ab1 = unpack_h2(ka[r][NG - 1]);
-          v += (ab1.y - ab1.x) * (1.0f / 15.0f) * (dk[2 * r + 1] - O1) + ab1.x * Q1;
+          v += (ab1.y - ab1.x) * (16777216.0f / 15.0f) * dk[2 * r + 1] + ab1.x * Q1;
         }
         v = __shfl_sync(0xFFFFFFFFu, v, lane & ~3);
         valid[r] = t0 + gid + 8 * r < it.t_end;
@@ -329,21 +342,19 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       // lazy rescaling: the reference maximum moves only when a score exceeds it by more
       // than 2^8, so p stays <= 256 and the accumulators rarely need scaling
       if (mx > m_run + 8.0f) {
-        const float corr = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
+        const float corr = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mx);
         l_run *= corr;
 #pragma unroll
         for (int u = 0; u < 2 * NW; ++u)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          asum[g] *= corr;
-          wsum[g] *= corr;
-        }
+        for (int g = 0; g < NG; ++g) asum[g] *= corr;
         m_run = mx;
       }
-      const float p0 = valid[0] ? exp2f(sc[0] - m_run) : 0.0f;
-      const float p1 = valid[1] ? exp2f(sc[1] - m_run) : 0.0f;
+      // invalid rows hold -inf scores, and ex2(-inf) = 0
+      const float p0 = ex2(sc[0] - m_run);
+      const float p1 = ex2(sc[1] - m_run);
       float ps = p0 + p1;
       ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
       ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 8);
@@ -366,9 +377,6 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           asum[NG - 1] += valid[r] ? p * ab1.x : 0.0f;
         }
         wrow[r] = pack_h2(w0, w1);
-        const float2 wr = unpack_h2(wrow[r]);       // the fp16 values the MMA uses
-        wsum[0] += wr.x;
-        if (NG == 2) wsum[NG - 1] += wr.y;
       }
       // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid (group n)
       const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
@@ -405,18 +413,17 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 4);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
-      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 4);
-      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 8);
-      wsum[g] += __shfl_xor_sync(0xFFFFFFFFu, wsum[g], 16);
+
     }
     if (tig == 0) {
       const int g_lo = (NG == 2) ? (gid >> 2) : 0;      // group of channel row gid
       const float A = (NG == 2 && g_lo) ? asum[NG - 1] : asum[0];
-      const float W1024 = 1024.0f * ((NG == 2 && g_lo) ? wsum[NG - 1] : wsum[0]);
+
       // channel rows of mma u: pair 2u has factor 1, pair 2u+1 factor 16
-      auto vx_of = [&](int u) { return (g_lo ? acc[u][1] : acc[u][0]) - W1024 + A; };
+      // acc holds 2^-24 * sum_t w_t c_tj (pair 2u) or 2^-20 * ... (pair 2u+1, factor 16)
+      auto vx_of = [&](int u) { return (g_lo ? acc[u][1] : acc[u][0]) * 16777216.0f + A; };
       auto vy_of = [&](int u) {
-        return ((g_lo ? acc[u][3] : acc[u][2]) - W1024) * (1.0f / 16.0f) + A;
+        return (g_lo ? acc[u][3] : acc[u][2]) * 1048576.0f + A;
       };
       const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
       const int jbase = (gid >> 1) * 8 * NW + 4 * (gid & 1);
