@@ -22,7 +22,7 @@ namespace {
 thread_local std::string t_last_error;
 
 // Upper bound on SMs used when sizing workspaces, so workspace sizes need no device query.
-constexpr int kWsSms = 192;
+
 
 int set_cuda_error(cudaError_t e) {
   t_last_error = cudaGetErrorString(e);
@@ -54,7 +54,7 @@ int check_device(int* sms_out) {
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return set_cuda_error(e);
     di.ok = (major == 10 && minor == 3);
-    di.sms = std::min(sms, kWsSms);
+    di.sms = std::min(sms, kMaxSms);
     di.init = true;
   }
   if (!di.ok) {
@@ -266,14 +266,14 @@ LayerWs layer_ws(const fg_dims& dm, int64_t M, const fg_kvcache* kv_for_decode, 
   w.att = round_up((size_t)M * h * 2);
   w.h1 = round_up((size_t)M * h * 2);
   w.mid = round_up((size_t)M * f * 2);
-  size_t g = gemm_plan(M, h, 3 * h, kWsSms).ws_bytes;
-  g = std::max(g, gemm_plan(M, h, h, kWsSms).ws_bytes);
+  size_t g = gemm_plan(M, h, 3 * h, kMaxSms).ws_bytes;
+  g = std::max(g, gemm_plan(M, h, h, kMaxSms).ws_bytes);
   if (f > 0) {
-    g = std::max(g, gemm_plan(M, h, f, kWsSms).ws_bytes);
-    g = std::max(g, gemm_plan(M, f, h, kWsSms).ws_bytes);
+    g = std::max(g, gemm_plan(M, h, f, kMaxSms).ws_bytes);
+    g = std::max(g, gemm_plan(M, f, h, kMaxSms).ws_bytes);
   }
   w.gemm = round_up(g);
-  w.attn = kv_for_decode ? round_up(decode_attn_ws_bytes(*kv_for_decode, len, kWsSms)) : 0;
+  w.attn = kv_for_decode ? round_up(decode_attn_ws_bytes(*kv_for_decode, len, kMaxSms)) : 0;
   w.total = w.ln + w.qkv + w.att + w.h1 + w.mid + w.gemm + w.attn;
   return w;
 }
@@ -354,7 +354,7 @@ int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64
 
 size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   if (M <= 0 || K <= 0 || N <= 0) return 0;
-  return gemm_plan(M, K, N, kWsSms).ws_bytes;
+  return gemm_plan(M, K, N, kMaxSms).ws_bytes;
 }
 
 int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
@@ -394,7 +394,7 @@ int fg_kv_append_q4(const uint16_t* k_new, const uint16_t* v_new, int64_t row_st
 
 size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len) {
   if (!kv || check_kv(kv) != FG_OK || len <= 0) return 0;
-  return decode_attn_ws_bytes(*kv, len, kWsSms);
+  return decode_attn_ws_bytes(*kv, len, kMaxSms);
 }
 
 int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,

@@ -513,16 +513,35 @@ int resident_ctas() {
 
 // Sequence splits: enough work items (b, hd, split) for about two per resident warp, each
 // split at least 4 tiles long, no empty split.
-int decode_attn_splits(const fg_kvcache& kv, int32_t len, int nsm) {
+// Sequence splits: the fewest that minimise the busiest warp's work, with the resident
+// warps (nsm * kPlanWarpsPerSm) taking items round-robin.  Work is counted in tiles: an
+// item costs about one tile more than its tiles (q preparation and its epilogue), and
+// splitting about four (the partials and the combine kernel).
+static int plan_splits(const fg_kvcache& kv, int32_t len, int nsm) {
   const int64_t bh = (int64_t)kv.B * kv.H;
   if (bh == 0) return 1;
   const int ntiles = (len + kTile - 1) / kTile;
-  const int64_t target = 2ll * nsm * kPlanWarpsPerSm;
-  int64_t splits = (target + bh - 1) / bh;
-  splits = std::min<int64_t>(splits, std::max(1, ntiles / 4));
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, ntiles));
-  const int tps = (int)((ntiles + splits - 1) / splits);
+  const int64_t warps = (int64_t)std::max(nsm, 1) * kPlanWarpsPerSm;
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int s = 1; s <= std::min(ntiles, 16); ++s) {
+    const int tps = (ntiles + s - 1) / s;
+    if (s > 1 && (s - 1) * tps >= ntiles) break;           // an empty split
+    const int64_t rounds = (bh * s + warps - 1) / warps;
+    const int64_t cost = rounds * (tps + 1) + (s > 1 ? 4 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  const int tps = (ntiles + best - 1) / best;
   return (ntiles + tps - 1) / tps;
+}
+
+// The device's plan, capped by the plan for kMaxSms SMs: the workspace query sizes for the
+// latter, and partial bytes grow with the split count.
+int decode_attn_splits(const fg_kvcache& kv, int32_t len, int nsm) {
+  return std::min(plan_splits(kv, len, nsm), plan_splits(kv, len, kMaxSms));
 }
 
 size_t decode_attn_ws_bytes(const fg_kvcache& kv, int32_t len, int nsm) {

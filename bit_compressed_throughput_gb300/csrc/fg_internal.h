@@ -10,6 +10,9 @@
 
 namespace fg {
 
+// Largest SM count the workspace queries plan for (GB300 has 152).
+constexpr int kMaxSms = 192;
+
 // Launchers: enqueue one kernel on `st`; return cudaGetLastError().
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* codes,
                             uint32_t* ab, cudaStream_t st);

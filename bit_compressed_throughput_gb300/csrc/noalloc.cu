@@ -67,7 +67,7 @@ int setup_current_device(DeviceScratch** out) {
       return FG_ERR_CUDA;
     }
     d.ptr = p;
-    d.sms = sms < 192 ? sms : 192;   // the same SM bound the workspace entry point plans with
+    d.sms = sms < kMaxSms ? sms : kMaxSms;   // the SM bound the workspace queries plan with
     d.ready = true;
   }
   *out = &d;

@@ -133,3 +133,13 @@ def test_workspace_sizes_monotone(fg):
     assert 0 < a <= b
     # prefill buffers of one GPU batch: LN, QKV, attention, h1 and the FFN activation
     assert a >= 16 * 512 * (4096 * 6 + 16384) * 2
+
+
+
+
+def test_decode_attention_workspace_for_long_few_sequences(fg):
+    """A long sequence over few heads is split (partials in the workspace); the query sizes
+    for the largest planned SM count, so it covers any GB300 launch."""
+    L = fg.lib
+    kv = fg.fg_kvcache(FAKE, FAKE, FAKE, FAKE, 1, 8192, 256, 2)
+    assert L.fg_decode_attn_workspace_bytes(C.byref(kv), 8192) > 0

@@ -65,16 +65,18 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 
 def test_static_scratch_rejects_oversize_calls():
     fg = lib()
-    # 72 sequences x 64 heads: 2 sequence splits for any SM count in [129, 288), so
-    # 4608 x 2 x (128 + 2) floats = 4.79 MB of partials > 4 MiB
-    B, H, d, cap = 72, 64, 128, 256
-    cache = fg.KVCacheQ4(B, cap, H * d, H)
-    need = fg.fg_decode_attn_workspace_bytes(cache, cap)
+    # 25 sequences x 100 heads x 4096 positions: the split planner chooses 6 splits on 152
+    # SMs, so the partials (2500 x 6 x (128 + 2) floats = 7.8 MB) exceed the 4 MiB static
+    # array; the call is rejected on the host before any launch (the cache is allocated, so
+    # a device whose plan did not split would run the call instead of faulting)
+    B, H, d, length = 25, 100, 128, 4096
+    cache = fg.KVCacheQ4(B, length, H * d, H)
+    need = fg.fg_decode_attn_workspace_bytes(cache, length)
     assert need > fg.DECODE_ATTN_STATIC_SCRATCH_BYTES
     q = torch.zeros((B, H * d), dtype=torch.float16, device="cuda")
     out = torch.full((B, H * d), 7.0, dtype=torch.float16, device="cuda")
     with pytest.raises(fg.FgError) as ei:
-        fg.fg_decode_attn_q4kv_static(q, H * d, cache, cap, 0.1, out)
+        fg.fg_decode_attn_q4kv_static(q, H * d, cache, length, 0.1, out)
     assert ei.value.status == fg.FG_ERR_WORKSPACE
     assert "static" in str(ei.value)
     torch.cuda.synchronize()
