@@ -185,6 +185,8 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
+  pdl_launch_dependents();
+  pdl_wait();
 
   // ---- issue cursor (used by lane 0 only): kRing tiles ahead of the compute cursor
   int ii = first;
@@ -472,6 +474,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const float* __restrict__ partial, int64_t nbh, int H, int splits,
                       uint16_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t bh = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (bh >= nbh) return;
@@ -565,14 +569,18 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
   const int64_t want = (items + kWarps - 1) / kWarps;
   if (d == 128) {
     const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<128>());
-    decode_attn_kernel<128><<<grid, kWarps * 32, Ring<128>::CTA_BYTES, st>>>(
-        q, q_stride, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits,
-        tps, sl2, out, partial);
+    cudaError_t e0 = launch_pdl(decode_attn_kernel<128>, dim3(grid), dim3(kWarps * 32),
+                                Ring<128>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes,
+                                kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2, out,
+                                partial);
+    if (e0 != cudaSuccess) return e0;
   } else {
     const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<64>());
-    decode_attn_kernel<64><<<grid, kWarps * 32, Ring<64>::CTA_BYTES, st>>>(
-        q, q_stride, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits,
-        tps, sl2, out, partial);
+    cudaError_t e0 = launch_pdl(decode_attn_kernel<64>, dim3(grid), dim3(kWarps * 32),
+                                Ring<64>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes,
+                                kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2, out,
+                                partial);
+    if (e0 != cudaSuccess) return e0;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -582,10 +590,11 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
     const int64_t nbh = (int64_t)kv.B * kv.H;
     const unsigned g2 = (unsigned)((nbh + 3) / 4);
     if (d == 128)
-      decode_combine_kernel<128><<<g2, 128, 0, st>>>(partial, nbh, kv.H, splits, out);
+      e = launch_pdl(decode_combine_kernel<128>, dim3(g2), dim3(128), 0, st, partial, nbh, kv.H,
+                     splits, out);
     else
-      decode_combine_kernel<64><<<g2, 128, 0, st>>>(partial, nbh, kv.H, splits, out);
-    e = cudaGetLastError();
+      e = launch_pdl(decode_combine_kernel<64>, dim3(g2), dim3(128), 0, st, partial, nbh, kv.H,
+                     splits, out);
     *kernels_out = 2;
   }
   return e;

@@ -63,6 +63,8 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
   constexpr int LD = Smem<D>::LD;
   constexpr int TILE = Smem<D>::TILE;
   extern __shared__ __align__(16) uint16_t sm[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint16_t* sQ = sm;
   uint16_t* sK = sm + TILE;            // 2 tiles
   uint16_t* sV = sm + 3 * TILE;        // 2 tiles
@@ -235,14 +237,15 @@ cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, in
     static cudaError_t attr = cudaFuncSetAttribute(
         prefill_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
     if (attr != cudaSuccess) return attr;
-    prefill_attn_kernel<128><<<grid, 128, Smem<128>::BYTES, st>>>(qkv, s, H, sl2, out);
+    return launch_pdl(prefill_attn_kernel<128>, grid, dim3(128), Smem<128>::BYTES, st, qkv, s, H,
+                      sl2, out);
   } else {
     static cudaError_t attr = cudaFuncSetAttribute(
         prefill_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
     if (attr != cudaSuccess) return attr;
-    prefill_attn_kernel<64><<<grid, 128, Smem<64>::BYTES, st>>>(qkv, s, H, sl2, out);
+    return launch_pdl(prefill_attn_kernel<64>, grid, dim3(128), Smem<64>::BYTES, st, qkv, s, H, sl2,
+                      out);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace fg

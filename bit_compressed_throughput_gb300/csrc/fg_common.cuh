@@ -56,6 +56,15 @@ __device__ __forceinline__ uint32_t q4_code_rcp(float xf, float af, float bma, f
   return (uint32_t)q;
 }
 
+// Programmatic dependent launch: every library kernel lets the next kernel of the stream
+// launch at once and waits for its predecessor's results (and for its predecessor to have
+// finished reading what this kernel overwrites) before touching global data, so launch and
+// setup overlap the previous kernel's tail.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

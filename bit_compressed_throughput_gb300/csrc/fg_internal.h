@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/fg.h"
 
@@ -24,6 +25,23 @@ cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const u
                              const uint16_t* b, float eps, uint16_t* y, cudaStream_t st);
 cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
                                 int32_t d, float scale, uint16_t* out, cudaStream_t st);
+
+// Launch with programmatic stream serialisation (see pdl_wait in fg_common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Message returned by fg_last_error() on this thread.
 void set_last_error(const std::string& msg);

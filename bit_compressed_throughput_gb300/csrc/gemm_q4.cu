@@ -340,6 +340,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers
@@ -606,6 +608,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 // Sum the split-K partials and apply bias / ReLU / residual: 8 outputs per thread.
 __global__ void __launch_bounds__(256)
 gemm_reduce_kernel(const float* __restrict__ partial, int splits, int64_t M, int N, EpiArgs ea) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const int64_t chunks = M * (N / 8);
   if (idx >= chunks) return;
@@ -711,14 +715,13 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const int ni = (p.tn <= 128 && p.kb_per_split >= 2 && last_unit_kb >= 2) ? 2 : 1;
   const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
                  p.kblocks, p.kb_per_split, (int)p.units, r, ni, rc};
-  gemm_q4_tc_kernel<<<(unsigned)p.grid, THREADS, SMEM_BYTES, st>>>(tmX, tmC, tmS, ka, ea);
-  e = cudaGetLastError();
+  e = launch_pdl(gemm_q4_tc_kernel, dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st, tmX, tmC,
+                 tmS, ka, ea);
   if (e != cudaSuccess || p.splits == 1) return e;
   if (mid_event) cudaEventRecord(mid_event, st);
   const int64_t chunks = p.M * (p.N / 8);
-  gemm_reduce_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, st>>>(
-      static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
-  return cudaGetLastError();
+  return launch_pdl(gemm_reduce_kernel, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, st,
+                    static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
 }
 
 cudaError_t gemm_read_error(unsigned int* out) {

@@ -23,6 +23,8 @@ layernorm_kernel(const uint16_t* __restrict__ x, int64_t rows, int h,
                  const uint16_t* __restrict__ gamma, const uint16_t* __restrict__ beta,
                  float eps, uint16_t* __restrict__ y) {
   __shared__ float red[2][kWarps];
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (kWarps / WPR) + warp / WPR;
   const bool live = row < rows;
@@ -110,14 +112,13 @@ cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const u
   const int64_t rows_per_cta = kWarps / wpr;
   const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
   if (wpr == 1)
-    layernorm_kernel<1><<<grid, kThreads, 0, st>>>(x, rows, h, g, b, eps, y);
+    return launch_pdl(layernorm_kernel<1>, dim3(grid), dim3(kThreads), 0, st, x, rows, h, g, b, eps, y);
   else if (wpr == 2)
-    layernorm_kernel<2><<<grid, kThreads, 0, st>>>(x, rows, h, g, b, eps, y);
+    return launch_pdl(layernorm_kernel<2>, dim3(grid), dim3(kThreads), 0, st, x, rows, h, g, b, eps, y);
   else if (wpr == 4)
-    layernorm_kernel<4><<<grid, kThreads, 0, st>>>(x, rows, h, g, b, eps, y);
+    return launch_pdl(layernorm_kernel<4>, dim3(grid), dim3(kThreads), 0, st, x, rows, h, g, b, eps, y);
   else
-    layernorm_kernel<8><<<grid, kThreads, 0, st>>>(x, rows, h, g, b, eps, y);
-  return cudaGetLastError();
+    return launch_pdl(layernorm_kernel<8>, dim3(grid), dim3(kThreads), 0, st, x, rows, h, g, b, eps, y);
 }
 
 }  // namespace fg

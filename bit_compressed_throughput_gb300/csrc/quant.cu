@@ -64,6 +64,8 @@ __device__ __forceinline__ uint32_t quantize8(const uint4 v, uint32_t* ab_out) {
 __global__ void __launch_bounds__(kThreads)
 quantize_kernel(const uint16_t* __restrict__ x, int64_t ngroups, uint8_t* __restrict__ codes,
                 uint32_t* __restrict__ ab) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   // Every lane of a warp takes part in the shuffles; lanes past the end use a dummy.
@@ -90,6 +92,8 @@ kv_append_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict_
                  int64_t row_stride, int T, int pos, int H, int d, int cap, int ppc,
                  uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
                  uint32_t* __restrict__ k_ab, uint32_t* __restrict__ v_ab) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int gph = d >> 6;                            // groups per head (1 or 2)
   const int b = blockIdx.x / H, head = blockIdx.x - b * H;
   const int p0 = threadIdx.x / (8 * gph);            // first position within the block
@@ -128,6 +132,8 @@ kv_append_rows_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __rest
                       int64_t ngroups, uint8_t* __restrict__ k_codes,
                       uint8_t* __restrict__ v_codes, uint32_t* __restrict__ k_ab,
                       uint32_t* __restrict__ v_ab) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   const bool live = grp < ngroups;
@@ -159,6 +165,8 @@ kv_append_rows_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __rest
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ ab,
                int64_t ngroups, uint16_t* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t grp = (int64_t)blockIdx.x * kGroupsPerCta + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   if (grp >= ngroups) return;
@@ -187,16 +195,14 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, uint8
                             uint32_t* ab, cudaStream_t st) {
   const int64_t ng = rows * (cols / 64);
   if (ng == 0) return cudaSuccess;
-  quantize_kernel<<<grid_for(ng), kThreads, 0, st>>>(x, ng, codes, ab);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel, dim3(grid_for(ng)), dim3(kThreads), 0, st, x, ng, codes, ab);
 }
 
 cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64_t cols,
                            uint16_t* y, cudaStream_t st) {
   const int64_t ng = rows * (cols / 64);
   if (ng == 0) return cudaSuccess;
-  dequant_kernel<<<grid_for(ng), kThreads, 0, st>>>(codes, ab, ng, y);
-  return cudaGetLastError();
+  return launch_pdl(dequant_kernel, dim3(grid_for(ng)), dim3(kThreads), 0, st, codes, ab, ng, y);
 }
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
@@ -207,18 +213,15 @@ cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64
     const int gpr = kv.h / 64;
     const int64_t ng = (int64_t)kv.B * T * gpr;
     dim3 grid(grid_for(ng), 2);
-    kv_append_rows_kernel<<<grid, kThreads, 0, st>>>(k_new, v_new, row_stride, T, pos, kv.H, d,
-                                                     kv.cap, gpr, ng, kv.k_codes, kv.v_codes,
-                                                     kv.k_ab, kv.v_ab);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_rows_kernel, grid, dim3(kThreads), 0, st, k_new, v_new, row_stride,
+                      T, pos, kv.H, d, kv.cap, gpr, ng, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
   }
   const int ppc = kPosPerThread * kThreads / (8 * (d / 64));   // 64 (d = 128) or 128
   const int64_t tblocks = (T + ppc - 1) / ppc;
   if (tblocks > 65535 || (int64_t)kv.B * kv.H > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)(kv.B * kv.H), (unsigned)tblocks, 2);
-  kv_append_kernel<<<grid, kThreads, 0, st>>>(k_new, v_new, row_stride, T, pos, kv.H, d, kv.cap,
-                                              ppc, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, grid, dim3(kThreads), 0, st, k_new, v_new, row_stride, T, pos,
+                    kv.H, d, kv.cap, ppc, kv.k_codes, kv.v_codes, kv.k_ab, kv.v_ab);
 }
 
 }  // namespace fg
