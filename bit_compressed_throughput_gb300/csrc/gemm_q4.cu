@@ -65,7 +65,7 @@ namespace {
 constexpr int TCH = 128;                    // output channels per tile (MMA M)
 constexpr int TN_MAX = 256;                 // tokens per tile (MMA N), runtime tn <= 256
 constexpr int BK = 64;
-constexpr int R_MAX = 8;                    // k-block ring: X tile + restored A slot
+constexpr int RA_MAX = 10;                  // restored-A ring (k-block barriers)
 constexpr int RC_MAX = 16;                  // code ring: codes + group statistics
 constexpr int RW = 8;                       // restore warps
 constexpr int RT = RW * 32;                 // restore threads
@@ -84,7 +84,7 @@ constexpr int SMEM_BYTES = 232448;          // the whole per-CTA budget
 constexpr int BAR_BYTES = 512;
 constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * TN_MAX;  // two accumulator buffers
-static_assert((2 * R_MAX + 2 * RC_MAX + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
+static_assert((2 * RA_MAX + 2 * RC_MAX + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
 static_assert(TMEM_COLS == 512, "TMEM budget");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
 static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
@@ -280,7 +280,8 @@ struct KArgs {
   int M, N, K, tn;
   uint32_t idesc;
   int tiles_t, tiles_c, kblocks, kb_per_split, units;
-  int r;               // k-block ring depth (X stage + A slot, freed by one MMA commit)
+  int ra;              // restored-A ring depth (the k-block barriers)
+  int rx;              // X ring depth, <= ra
   int ni;              // MMA issuers: 2 for tn <= 128 (k-blocks alternate, 2 accumulators)
   int rc;              // code ring depth
 };
@@ -291,27 +292,30 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const int tn = ka.tn, R = ka.r, RC = ka.rc, XB = tn * 128;
+  const int tn = ka.tn, R = ka.ra, RX = ka.rx, RC = ka.rc, XB = tn * 128;
   uint8_t* sW = smem;                                  // R x W_BYTES (restored weights)
-  uint8_t* sX = sW + R * W_BYTES;                      // R x XB (activations)
-  uint8_t* sC = sX + R * XB;                           // RC x CS_BYTES (codes | statistics)
+  uint8_t* sX = sW + R * W_BYTES;                      // RX x XB (activations)
+  uint8_t* sC = sX + RX * XB;                          // RC x CS_BYTES (codes | statistics)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + POOL_BYTES);
-  // bars: full[R_MAX], mma_done[R_MAX], full_c[RC_MAX], free_c[RC_MAX], acc_full[2],
-  // acc_empty[2].  full(r) completes when the restore group has written A slot r AND the X
-  // tile of slot r has landed (the X producer's expect_tx arrival plus the TMA bytes), so
-  // the MMA issuer waits once per k-block.  mma_done(r) completes when the MMAs of slot r
-  // are done: its X stage may be refilled and its A slot rewritten.
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * R_MAX + 2 * RC_MAX + 4);
+  // bars: full[RA_MAX], mma_done[RA_MAX], full_c[RC_MAX], free_c[RC_MAX], acc_full[2],
+  // acc_empty[2].  K-block it uses A slot it % R and X slot it % RX (RX <= R).  full(it % R)
+  // completes when the restore group has written the A slot AND the X tile has landed (the
+  // X producer's expect_tx arrival plus the TMA bytes), so the MMA issuer waits once per
+  // k-block.  mma_done(it % R) completes when the MMAs of k-block it are done: its A slot may
+  // be rewritten and its X slot refilled.  The X producer issues k-block it after the MMAs
+  // of k-block it - RX, hence after those of it - R, so its arrival always lands in k-block
+  // it's phase of full(it % R).
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RA_MAX + 2 * RC_MAX + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int r) { return bar0 + 8u * r; };
-  auto mma_done = [&](int r) { return bar0 + 8u * (R_MAX + r); };
-  auto full_c = [&](int c) { return bar0 + 8u * (2 * R_MAX + c); };
-  auto free_c = [&](int c) { return bar0 + 8u * (2 * R_MAX + RC_MAX + c); };
-  auto acc_full = [&](int a) { return bar0 + 8u * (2 * R_MAX + 2 * RC_MAX + a); };
-  auto acc_empty = [&](int a) { return bar0 + 8u * (2 * R_MAX + 2 * RC_MAX + 2 + a); };
+  auto mma_done = [&](int r) { return bar0 + 8u * (RA_MAX + r); };
+  auto full_c = [&](int c) { return bar0 + 8u * (2 * RA_MAX + c); };
+  auto free_c = [&](int c) { return bar0 + 8u * (2 * RA_MAX + RC_MAX + c); };
+  auto acc_full = [&](int a) { return bar0 + 8u * (2 * RA_MAX + 2 * RC_MAX + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (2 * RA_MAX + 2 * RC_MAX + 2 + a); };
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < R; ++r) {
@@ -345,25 +349,37 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers
-    // warp 0: X tiles into the k-block ring; warp 2: codes + statistics into the code ring
+    // warp 0: X tiles into the X ring; warp 2: codes + statistics into the code ring
     if (lane == 0) {
       const bool is_x = (warp == 0);
-      const int depth = is_x ? R : RC;
-      int it = 0, s = 0;
-      uint32_t ph = 0;                                // lap parity of slot s
+      const int depth = is_x ? RX : RC;
+      int it = 0, s = 0;                              // k-block, slot in this ring
+      uint32_t ph = 0;                                // lap parity of slot s (code ring)
+      int kr = 0;                                     // X: A-ring position of k-block it
+      int fa = R - RX;                                // X: A-ring position of it - RX
+      uint32_t fph = 1;                               //    and its lap parity
       bool ok = true;
       for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x) {
         const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
-          if (it >= depth &&
-              !mbar_wait(is_x ? mma_done(s) : free_c(s), ph ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
           if (is_x) {
-            mbar_expect_tx(full(s), (uint32_t)XB);
-            tma_load_2d(smem_u32(sX + s * XB), &tmX, kb * BK, w.t0, full(s));
+            // the X slot is free once the MMAs of k-block it - RX are done
+            if (it >= RX && !mbar_wait(mma_done(fa), fph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full(kr), (uint32_t)XB);
+            tma_load_2d(smem_u32(sX + s * XB), &tmX, kb * BK, w.t0, full(kr));
+            if (++kr == R) kr = 0;
+            if (++fa == R) {
+              fa = 0;
+              fph ^= 1;
+            }
           } else {
+            if (it >= RC && !mbar_wait(free_c(s), ph ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
             uint8_t* cs = sC + s * CS_BYTES;
             mbar_expect_tx(full_c(s), (uint32_t)CS_BYTES);
             tma_load_2d(smem_u32(cs), &tmC, w.c0 / 2, kb * BK, full_c(s));
@@ -380,10 +396,11 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // abort their phases may also lack restore arrivals, so those waits are short.
       if (!is_x || !ok) {
         const long long limit = is_x ? (1ll << 26) : kWaitCycles;
+        const int dep = is_x ? R : RC;
         for (int i = max(0, it - depth); i < it; ++i) {
-          const uint32_t bar = is_x ? full(i % depth) : full_c(i % depth);
+          const uint32_t bar = is_x ? full(i % dep) : full_c(i % dep);
           const long long t0 = clock64();
-          while (!mbar_try(bar, (i / depth) & 1)) {
+          while (!mbar_try(bar, (i / dep) & 1)) {
             if (clock64() - t0 > limit) {
               atomicOr(&g_gemm_error, 2u);
               break;
@@ -408,8 +425,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // 1 or 2): this thread's bookkeeping sits on the MMA stream's critical path
       const uint64_t a_step = W_BYTES >> 4, b_step = (uint64_t)(XB >> 4);
       uint64_t ad = adesc0, bd = bdesc0;
-      int tl = 0, r = 0;
-      uint32_t ph = 0, par = 0;                       // lap parity of slot r; k-block parity
+      int tl = 0, r = 0, rx = 0;                      // A slot, X slot
+      uint32_t ph = 0, par = 0;                       // lap parity of A slot r; k-block parity
       const uint32_t mask = (ka.ni == 2) ? 1u : 0u;
       bool ok = true;
       for (int u = blockIdx.x; u < ka.units && ok; u += gridDim.x, ++tl) {
@@ -438,9 +455,13 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             r = 0;
             ph ^= 1;
             ad = adesc0;
-            bd = bdesc0;
           } else {
             ad += a_step;
+          }
+          if (++rx == RX) {
+            rx = 0;
+            bd = bdesc0;
+          } else {
             bd += b_step;
           }
         }
@@ -702,19 +723,34 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
-  // ring depths: small token tiles (decode) keep 16 code stages (80 KB of codes from HBM
-  // in flight per SM); large ones trade code stages for k-block slots
-  const int per_k = W_BYTES + p.tn * 128;
-  const int rc_target = (p.tn <= 128) ? RC_MAX : 6;
-  const int r = std::min(R_MAX, (POOL_BYTES - rc_target * CS_BYTES) / per_k);
-  const int rc = std::min(RC_MAX, (POOL_BYTES - r * per_k) / CS_BYTES);
-  if (r < 3 || rc < 2) return cudaErrorInvalidConfiguration;
+  // ring depths: large token tiles (prefill) pair each restored slot with an X slot (4 + 4,
+  // 6 code stages); small ones (decode) keep a short X ring (3) and spend the memory on
+  // restored slots (so a restore waits for the MMAs of a k-block many k-blocks back) and on
+  // code stages (14: 70 KB of codes from HBM in flight per SM)
+  const int xb = p.tn * 128;
+  int rx, rc_target;
+  if (p.tn > 128) {
+    rx = 0;
+    rc_target = 6;
+  } else {
+    rx = 3;
+    rc_target = 14;
+  }
+  int ra;
+  if (rx == 0) {
+    ra = std::min(RA_MAX, (POOL_BYTES - rc_target * CS_BYTES) / (W_BYTES + xb));
+    rx = ra;
+  } else {
+    ra = std::min(RA_MAX, (POOL_BYTES - rc_target * CS_BYTES - rx * xb) / W_BYTES);
+  }
+  const int rc = std::min(RC_MAX, (POOL_BYTES - ra * W_BYTES - rx * xb) / CS_BYTES);
+  if (ra < 3 || rx < 2 || rx > ra || rc < 2) return cudaErrorInvalidConfiguration;
   // two MMA issuers when the token tile fits two accumulators per buffer and every unit
   // has at least one k-block for each
   const int last_unit_kb = p.kblocks - (p.splits - 1) * p.kb_per_split;
   const int ni = (p.tn <= 128 && p.kb_per_split >= 2 && last_unit_kb >= 2) ? 2 : 1;
   const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
-                 p.kblocks, p.kb_per_split, (int)p.units, r, ni, rc};
+                 p.kblocks, p.kb_per_split, (int)p.units, ra, rx, ni, rc};
   e = launch_pdl(gemm_q4_tc_kernel, dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st, tmX, tmC,
                  tmS, ka, ea);
   if (e != cudaSuccess || p.splits == 1) return e;
