@@ -724,17 +724,17 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
   // ring depths: large token tiles (prefill) pair each restored slot with an X slot (4 + 4,
-  // 6 code stages); small ones (decode) keep a short X ring (3) and spend the memory on
-  // restored slots (so a restore waits for the MMAs of a k-block many k-blocks back) and on
-  // code stages (14: 70 KB of codes from HBM in flight per SM)
+  // 6 code stages); small ones (decode) keep 6 X slots (L2 latency of the X tile) and spend
+  // the rest on restored slots (so a restore waits for the MMAs of a k-block many k-blocks
+  // back) and code stages (about 12: 60 KB of codes from HBM in flight per SM)
   const int xb = p.tn * 128;
   int rx, rc_target;
   if (p.tn > 128) {
     rx = 0;
     rc_target = 6;
   } else {
-    rx = 3;
-    rc_target = 14;
+    rx = 6;
+    rc_target = 10;
   }
   int ra;
   if (rx == 0) {
