@@ -210,6 +210,36 @@ __device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s16, uint32_t c) 
   return o;
 }
 
+// 8 x 8 fp16 transpose inside each 8-lane group of a warp.  On entry lane p of the group
+// holds w[q] = (D[p][2q], D[p][2q+1]) for columns (tokens) 0..7 of its row p; on return it
+// holds w[q] = (D[2q][p], D[2q+1][p]), column p of every row.  Three exchanges, each swapping
+// one lane-index bit with one element-index bit (half of a word, then word bit 0, then word
+// bit 1).
+__device__ __forceinline__ void transpose8x8_h(uint32_t (&w)[4], int lane) {
+  const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+  const uint32_t sel = b0 ? 0x3276u : 0x5410u;        // (x.hi, w.hi) or (w.lo, x.lo)
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t x = __shfl_xor_sync(0xFFFFFFFFu, w[q], 1);
+    w[q] = __byte_perm(w[q], x, sel);
+  }
+  {
+    const uint32_t y0 = __shfl_xor_sync(0xFFFFFFFFu, b1 ? w[0] : w[1], 2);
+    const uint32_t y1 = __shfl_xor_sync(0xFFFFFFFFu, b1 ? w[2] : w[3], 2);
+    if (b1) { w[0] = y0; w[2] = y1; } else { w[1] = y0; w[3] = y1; }
+  }
+  {
+    const uint32_t z0 = __shfl_xor_sync(0xFFFFFFFFu, b2 ? w[0] : w[2], 4);
+    const uint32_t z1 = __shfl_xor_sync(0xFFFFFFFFu, b2 ? w[1] : w[3], 4);
+    if (b2) { w[0] = z0; w[1] = z1; } else { w[2] = z0; w[3] = z1; }
+  }
+}
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hadd2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 struct EpiArgs {
   const uint16_t* bias;
   const uint16_t* residual;
@@ -571,13 +601,10 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       tc_fence_after();
       const int64_t ch = w.c0 + ch_in_tile;
       const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;
+      // first channel of this lane's 8-lane group (channels in natural order after the
+      // transpose)
+      const int64_t chb = w.c0 + lane_base + (lane & ~7);
       for (int cb = 0; cb < ntok; cb += 32) {
-        // loads that do not depend on the accumulator go first
-        float res[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          res[i] = (add_res && cb + i < ntok)
-                       ? h2f(ea.residual[(int64_t)(w.t0 + cb + i) * N + ch]) : 0.0f;
         // columns past tn (at most cb + 31 <= 255) stay inside this accumulator's 256
         uint32_t r[32];
         __syncwarp();
@@ -597,18 +624,50 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
               r[16 * h + i] = __float_as_uint(__uint_as_float(r[16 * h + i]) + __uint_as_float(r2[i]));
           }
         }
+        if (ea.partial) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (cb + i >= ntok) break;
-          const int64_t t = w.t0 + cb + i;
-          const float a = __uint_as_float(r[i]);
-          if (ea.partial) {
-            ea.partial[((int64_t)w.split * ka.M + t) * N + ch] = a;
-            continue;
+          for (int i = 0; i < 32; ++i) {
+            if (cb + i >= ntok) break;
+            ea.partial[((int64_t)w.split * ka.M + w.t0 + cb + i) * N + ch] = __uint_as_float(r[i]);
           }
-          float v = a + (bias_f + res[i]);
-          if (ea.epi == FG_EPI_RELU) v = fmaxf(v, 0.0f);
-          ea.Y[t * N + ch] = f2h(v);
+          continue;
+        }
+        // bias (and ReLU) in fp32 on this lane's channel, then fp16 pairs along tokens
+        uint32_t hv[16];
+        if (ea.epi == FG_EPI_RELU) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            hv[k] = pack_h2(fmaxf(__uint_as_float(r[2 * k]) + bias_f, 0.0f),
+                            fmaxf(__uint_as_float(r[2 * k + 1]) + bias_f, 0.0f));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            hv[k] = pack_h2(__uint_as_float(r[2 * k]) + bias_f, __uint_as_float(r[2 * k + 1]) + bias_f);
+        }
+        // per 8-token block: transpose so this lane holds token 8j + (lane & 7) for the
+        // group's 8 channels, undo the restore order (positions 0..7 hold channels
+        // 0,4,1,5,2,6,3,7), add the residual row segment and store 16 bytes
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t u[4] = {hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]};
+          transpose8x8_h(u, lane);
+          uint4 o;
+          o.x = __byte_perm(u[0], u[1], 0x5410);          // channels 0, 1
+          o.y = __byte_perm(u[2], u[3], 0x5410);          // 2, 3
+          o.z = __byte_perm(u[0], u[1], 0x7632);          // 4, 5
+          o.w = __byte_perm(u[2], u[3], 0x7632);          // 6, 7
+          const int tt = cb + 8 * j + (lane & 7);
+          if (tt < ntok) {
+            const int64_t t = w.t0 + tt;
+            if (ea.epi == FG_EPI_RESIDUAL) {
+              const uint4 rv = *reinterpret_cast<const uint4*>(ea.residual + t * N + chb);
+              o.x = hadd2_u32(o.x, rv.x);
+              o.y = hadd2_u32(o.y, rv.y);
+              o.z = hadd2_u32(o.z, rv.z);
+              o.w = hadd2_u32(o.w, rv.w);
+            }
+            *reinterpret_cast<uint4*>(ea.Y + t * N + chb) = o;
+          }
         }
       }
       tc_fence_before();
