@@ -504,6 +504,8 @@ template <int D>
 int resident_ctas() {
   static int occ = [] {
     int n = 0;
+    // the rings are small: let the shared-memory carveout admit as many CTAs as registers do
+    cudaFuncSetAttribute(decode_attn_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<D>, kWarps * 32,
                                                       Ring<D>::CTA_BYTES) != cudaSuccess ||
         n < 1)
@@ -515,8 +517,6 @@ int resident_ctas() {
 
 }  // namespace
 
-// Sequence splits: enough work items (b, hd, split) for about two per resident warp, each
-// split at least 4 tiles long, no empty split.
 // Sequence splits: the fewest that minimise the busiest warp's work, with the resident
 // warps (nsm * kPlanWarpsPerSm) taking items round-robin.  Work is counted in tiles: an
 // item costs about one tile more than its tiles (q preparation and its epilogue), and

@@ -64,6 +64,8 @@ CASES = {
     "decode-attn-opt67b": lambda r: attn_case(64, 32, 128, 543, r),
     # KV-dominated workload: 512 sequences x 56 heads x 1056 positions (4.3 GB of cache)
     "decode-attn-kv": lambda r: attn_case(512, 56, 128, 1056, r),
+    # a quarter of it (128 sequences, 1.1 GB of cache): the same per-warp work, capture-sized
+    "decode-attn-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r),
 }
 
 
