@@ -17,20 +17,23 @@
 // group scale.  The dot products run on mma.sync m16n8k16 with fp32 accumulation (the
 // products are exact in fp32).
 //
-// Memory pipeline: a warp owns a flattened stream of 16-position tiles over its work
-// items (b, hd, split).  Lane 0 keeps kRing tiles in flight with 1-D bulk async copies
-// (K codes, V codes, K and V group statistics of one tile: four contiguous runs in the
-// head-major cache) into a per-warp shared-memory ring, completing on one mbarrier per
-// slot; the warp computes on slot i while slots i+1 .. i+kRing-1 land.  The stream runs
-// across item boundaries, so the ring never drains between items.  Tiles are whole 16
-// positions (the cache capacity is a multiple of 16), positions at or past the end are
-// masked with selects, so never-written cache slots cannot leak into the result.
+// Memory pipeline: a warp owns a flattened stream of 32-position slots (two 16-position
+// tiles) over its work items (b, hd, split).  Lane 0 keeps kRing slots in flight with 1-D
+// bulk async copies (K codes, V codes, K and V group statistics: four contiguous runs in
+// the head-major cache) into a per-warp shared-memory ring, completing on one mbarrier
+// per slot; the warp computes on one slot while the others land.  The stream runs across
+// item boundaries, so the ring never drains between items.  Copies cover whole
+// 16-position tiles (the cache capacity is a multiple of 16); positions at or past the
+// end are masked with selects, so never-written cache slots cannot leak into the result.
 //
 // Inside a tile, lane (gid, tig) reads positions gid and gid+8 (16 bytes of codes each
-// for K and V when d = 128).  The dot-product index order is permuted to match what each
-// lane holds; q (K side) is permuted the same way, and the V side is transposed in
-// registers with movmatrix.  Online softmax (base 2) per item; split items write
-// (m, l, unnormalised o) partials that a second kernel combines.
+// for K and V when d = 128).  K side: the dot-product index order is permuted to match
+// what each lane holds and q is permuted the same way; every column of the q operand
+// carries a group's q, so each lane's accumulator fragment holds its own rows' scores.
+// V side: each packed code word is transposed with movmatrix (a lane then holds four
+// channels at two positions) before it is split into code pairs.  Online softmax (base
+// 2) per item; split items write (m, l, unnormalised o) partials that a second kernel
+// combines.
 //
 // Every mbarrier wait is bounded; on timeout the warp sets the device error word read by
 // fg_check_device_error, drains its copies and stops.
@@ -49,17 +52,22 @@ __device__ unsigned int g_attn_error = 0;
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kTile = 16;
-constexpr int kRing = 4;                  // tiles in flight per warp
+constexpr int kTile = 16;                 // positions per mma step
+constexpr int kSub = 2;                   // tiles per ring slot
+constexpr int kSlotPos = kSub * kTile;    // positions per ring slot
+constexpr int kRing = 3;                  // slots per warp
 constexpr int kPlanWarpsPerSm = 16;       // resident warps per SM assumed by the split plan
 constexpr long long kWaitCycles = 1ll << 32;
 
 template <int D>
 struct Ring {
   static constexpr int NG = D / 64;                     // groups per head
-  static constexpr int CODE_BYTES = kTile * (D / 2);    // one tile of K (or V) codes
-  static constexpr int AB_BYTES = kTile * NG * 4;       // one tile of K (or V) statistics
-  static constexpr int SLOT = 2 * CODE_BYTES + 2 * AB_BYTES;
+  static constexpr int ROW_CODE = D / 2;                // code bytes of one position
+  static constexpr int ROW_AB = NG * 4;                 // statistics bytes of one position
+  static constexpr int ROW_BYTES = 2 * ROW_CODE + 2 * ROW_AB;   // K and V
+  static constexpr int CODE_BYTES = kSlotPos * ROW_CODE;
+  static constexpr int AB_BYTES = kSlotPos * ROW_AB;
+  static constexpr int SLOT = kSlotPos * ROW_BYTES;
   static constexpr int WARP_BYTES = kRing * SLOT;
   static constexpr int CTA_BYTES = kWarps * WARP_BYTES + kWarps * kRing * 8;
 };
@@ -146,7 +154,7 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
 
 // Work item -> (b, hd, position range).
 struct Item {
-  int b, hd, split, t_begin, t_end, ntiles;
+  int b, hd, split, t_begin, t_end, nslots;
 };
 __device__ __forceinline__ Item item_of(int item, int H, int len, int splits, int tps) {
   Item it;
@@ -156,7 +164,7 @@ __device__ __forceinline__ Item item_of(int item, int H, int len, int splits, in
   it.hd = bh - it.b * H;
   it.t_begin = it.split * tps * kTile;
   it.t_end = min(len, it.t_begin + tps * kTile);
-  it.ntiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
+  it.nslots = (it.t_end - it.t_begin + kSlotPos - 1) / kSlotPos;
   return it;
 }
 
@@ -188,37 +196,39 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
   pdl_launch_dependents();
   pdl_wait();
 
-  // ---- issue cursor (used by lane 0 only): kRing tiles ahead of the compute cursor
-  int ii = first;
-  int itile = 0;
+  // ---- issue cursor (used by lane 0 only): kRing slots ahead of the compute cursor
+  int ii = first, islot = 0, is = 0, issued = 0;
   Item iitem = item_of(ii < items ? ii : 0, H, len, splits, tps);
-  int64_t gi = 0;
   auto issue = [&]() {
     if (ii >= items) return;
-    const int s = (int)(gi % kRing);
-    const uint32_t bar = bar0 + 8 * s;
-    uint8_t* slot = ring + s * R::SLOT;
-    const int t0 = iitem.t_begin + itile * kTile;
+    const uint32_t bar = bar0 + 8 * is;
+    uint8_t* slot = ring + is * R::SLOT;
+    const int t0 = iitem.t_begin + islot * kSlotPos;
+    // whole 16-position tiles up to the one holding t_end - 1: never past cap, since
+    // t_end <= cap and cap is a multiple of 16
+    const int rows = min(kSlotPos, (iitem.t_end - t0 + kTile - 1) / kTile * kTile);
     const int64_t row0 = ((int64_t)iitem.b * H + iitem.hd) * cap + t0;
     // the slot was last read through the generic proxy; order that before the copy
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    bar_expect_tx(bar, R::SLOT);
-    bulk_copy(smem_u32(slot), kc + row0 * (D / 2), R::CODE_BYTES, bar);
-    bulk_copy(smem_u32(slot + R::CODE_BYTES), vc + row0 * (D / 2), R::CODE_BYTES, bar);
-    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES), kab + row0 * NG, R::AB_BYTES, bar);
-    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES + R::AB_BYTES), vab + row0 * NG, R::AB_BYTES,
-              bar);
-    ++gi;
-    if (++itile == iitem.ntiles) {
+    bar_expect_tx(bar, (uint32_t)(rows * R::ROW_BYTES));
+    bulk_copy(smem_u32(slot), kc + row0 * R::ROW_CODE, rows * R::ROW_CODE, bar);
+    bulk_copy(smem_u32(slot + R::CODE_BYTES), vc + row0 * R::ROW_CODE, rows * R::ROW_CODE, bar);
+    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES), kab + row0 * NG, rows * R::ROW_AB, bar);
+    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES + R::AB_BYTES), vab + row0 * NG,
+              rows * R::ROW_AB, bar);
+    ++issued;
+    if (++is == kRing) is = 0;
+    if (++islot == iitem.nslots) {
       ii += nwarps;
-      itile = 0;
+      islot = 0;
       if (ii < items) iitem = item_of(ii, H, len, splits, tps);
     }
   };
   if (lane == 0)
     for (int r = 0; r < kRing; ++r) issue();
 
-  int64_t gc = 0;
+  int cs = 0, consumed = 0;             // compute cursor: ring slot, slots consumed
+  uint32_t cph = 0;                     // parity of the slot's current phase
   bool ok = true;
   for (int ci = first; ci < items && ok; ci += nwarps) {
     const Item it = item_of(ci, H, len, splits, tps);
@@ -236,8 +246,9 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
     };
     const int my_group = (NG == 2) ? (tig >> 1) : 0;
-    // B fragments: q for pairs with factor 1, q/16 (exact) for pairs with factor 16;
-    // qsum = sum of q
+    // B fragments: q for pairs with factor 1, q/16 (exact) for pairs with factor 16.  Column
+    // n of B carries group n & 1 (NG == 2) or group 0 (NG == 1), so every lane's D fragment
+    // holds its rows' dot products for every group and no lane needs another's.
     float qsum = 0.0f;
     uint32_t bq[2 * NW][2];
 #pragma unroll
@@ -253,210 +264,213 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), *reinterpret_cast<const __half2*>(&k16));
           v = *reinterpret_cast<uint32_t*>(&h);
         }
-        bq[s][r] = (gid == my_group) ? v : 0u;
+        bq[s][r] = (NG == 1 || (gid & 1) == my_group) ? v : 0u;
       }
     }
     // sum over the lanes sharing this group: tig pairs (NG == 2) or all four (NG == 1)
     qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
+    if (NG == 1) qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
+    // scores in base 2: the softmax scale rides on the group sums and the code scale
+    const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3) * scale_log2;
+    const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) * scale_log2
+                               : 0.0f;
+    // dk holds 2^-24 * sum_j c_j q_j: the code scale (b - a)/15 takes the 2^24 back
+    const float ck = (16777216.0f / 15.0f) * scale_log2;
 
-    if (NG == 1) {
-      qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
-
-    }
-    const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3);
-    const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) : 0.0f;
-
-
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_run = -INFINITY;
+    float l_run = 0.0f;                 // this lane's rows only; summed over gid at the end
     float acc[2 * NW][4];
 #pragma unroll
     for (int u = 0; u < 2 * NW; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
-    float asum[NG];                     // sum_t p_t a_tg
+    float asum[NG];                     // sum_t p_t a_tg over this lane's rows
 #pragma unroll
     for (int g = 0; g < NG; ++g) asum[g] = 0.0f;
 
-    for (int j = 0; j < it.ntiles; ++j, ++gc) {
-      const int s = (int)(gc % kRing);
-      ok = __all_sync(0xFFFFFFFFu, bar_wait(bar0 + 8 * s, (uint32_t)((gc / kRing) & 1)));
+    for (int j = 0; j < it.nslots; ++j) {
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(bar0 + 8 * cs, cph));
       if (!ok) break;
-      const uint8_t* slot = ring + s * R::SLOT;
-      // ---- this lane's rows gid and gid+8 of the tile, from shared memory
-      uint32_t kw[2][NW], vw[2][NW], ka[2][NG], va[2][NG];
+      const uint8_t* slot = ring + cs * R::SLOT;
+      const int ts = it.t_begin + j * kSlotPos;
+      const int nsub = min(kSub, (it.t_end - ts + kTile - 1) / kTile);
+      for (int sub = 0; sub < nsub; ++sub) {
+        const int t0 = ts + sub * kTile;
+        // ---- this lane's rows gid and gid+8 of the tile, from shared memory
+        uint32_t kw[2][NW], vw[2][NW], ka[2][NG], va[2][NG];
+        bool valid[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = gid + 8 * r;
-        const uint8_t* kp = slot + row * (D / 2) + tig * 4 * NW;
-        const uint8_t* vp = slot + R::CODE_BYTES + row * (D / 2) + tig * 4 * NW;
-        if (NW == 4) {
-          const uint4 uk = *reinterpret_cast<const uint4*>(kp);
-          const uint4 uv = *reinterpret_cast<const uint4*>(vp);
-          kw[r][0] = uk.x; kw[r][1] = uk.y; kw[r][2 % NW] = uk.z; kw[r][3 % NW] = uk.w;
-          vw[r][0] = uv.x; vw[r][1] = uv.y; vw[r][2 % NW] = uv.z; vw[r][3 % NW] = uv.w;
-        } else {
-          const uint2 uk = *reinterpret_cast<const uint2*>(kp);
-          const uint2 uv = *reinterpret_cast<const uint2*>(vp);
-          kw[r][0] = uk.x; kw[r][1 % NW] = uk.y;
-          vw[r][0] = uv.x; vw[r][1 % NW] = uv.y;
+        for (int r = 0; r < 2; ++r) {
+          const int row = sub * kTile + gid + 8 * r;
+          const uint8_t* kp = slot + row * R::ROW_CODE + tig * 4 * NW;
+          const uint8_t* vp = kp + R::CODE_BYTES;
+          if (NW == 4) {
+            const uint4 uk = *reinterpret_cast<const uint4*>(kp);
+            const uint4 uv = *reinterpret_cast<const uint4*>(vp);
+            kw[r][0] = uk.x; kw[r][1] = uk.y; kw[r][2 % NW] = uk.z; kw[r][3 % NW] = uk.w;
+            vw[r][0] = uv.x; vw[r][1] = uv.y; vw[r][2 % NW] = uv.z; vw[r][3 % NW] = uv.w;
+          } else {
+            const uint2 uk = *reinterpret_cast<const uint2*>(kp);
+            const uint2 uv = *reinterpret_cast<const uint2*>(vp);
+            kw[r][0] = uk.x; kw[r][1 % NW] = uk.y;
+            vw[r][0] = uv.x; vw[r][1 % NW] = uv.y;
+          }
+          const uint8_t* kap = slot + 2 * R::CODE_BYTES + row * R::ROW_AB;
+          if (NG == 2) {
+            const uint2 a2 = *reinterpret_cast<const uint2*>(kap);
+            const uint2 v2 = *reinterpret_cast<const uint2*>(kap + R::AB_BYTES);
+            ka[r][0] = a2.x; ka[r][NG - 1] = a2.y;
+            va[r][0] = v2.x; va[r][NG - 1] = v2.y;
+          } else {
+            ka[r][0] = *reinterpret_cast<const uint32_t*>(kap);
+            va[r][0] = *reinterpret_cast<const uint32_t*>(kap + R::AB_BYTES);
+          }
+          valid[r] = t0 + gid + 8 * r < it.t_end;
         }
-        const uint32_t* kap = reinterpret_cast<const uint32_t*>(slot + 2 * R::CODE_BYTES);
-        const uint32_t* vap = reinterpret_cast<const uint32_t*>(slot + 2 * R::CODE_BYTES +
-                                                                R::AB_BYTES);
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          ka[r][g] = kap[row * NG + g];
-          va[r][g] = vap[row * NG + g];
-        }
-      }
-      const int t0 = it.t_begin + j * kTile;
 
-      // ---- scores: K codes (rows t) x permuted q, one column per group
-      float dk[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- scores: K codes (rows t) x permuted q
+        float dk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        uint32_t c0[4], c1[4];                       // rows gid and gid+8
-        code_pairs(kw[0][w], c0);
-        code_pairs(kw[1][w], c1);
-        mma16816(dk, c0[0], c1[0], c0[1], c1[1], bq[2 * w][0], bq[2 * w][1]);
-        mma16816(dk, c0[2], c1[2], c0[3], c1[3], bq[2 * w + 1][0], bq[2 * w + 1][1]);
-      }
-      // lanes with tig == 0 hold D[t][0..1] for t = gid (dk[0], dk[1]) and gid+8 (dk[2], dk[3])
-      bool valid[2];
-      float sc[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float2 ab0 = unpack_h2(ka[r][0]);
-        // dk holds 2^-24 * sum_j c_j q_j: fold 2^24 into the group scale
-        float v = (ab0.y - ab0.x) * (16777216.0f / 15.0f) * dk[2 * r] + ab0.x * Q0;
-        if (NG == 2) {
-          const float2 ab1 = unpack_h2(ka[r][NG - 1]);
-          v += (ab1.y - ab1.x) * (16777216.0f / 15.0f) * dk[2 * r + 1] + ab1.x * Q1;
+        for (int w = 0; w < NW; ++w) {
+          uint32_t c0[4], c1[4];                     // rows gid and gid+8
+          code_pairs(kw[0][w], c0);
+          code_pairs(kw[1][w], c1);
+          mma16816(dk, c0[0], c1[0], c0[1], c1[1], bq[2 * w][0], bq[2 * w][1]);
+          mma16816(dk, c0[2], c1[2], c0[3], c1[3], bq[2 * w + 1][0], bq[2 * w + 1][1]);
         }
-        v = __shfl_sync(0xFFFFFFFFu, v, lane & ~3);
-        valid[r] = t0 + gid + 8 * r < it.t_end;
-        sc[r] = valid[r] ? v * scale_log2 : -INFINITY;
-      }
-      float mx = fmaxf(sc[0], sc[1]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-      // lazy rescaling: the reference maximum moves only when a score exceeds it by more
-      // than 2^8, so p stays <= 256 and the accumulators rarely need scaling
-      if (mx > m_run + 8.0f) {
-        const float corr = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mx);
-        l_run *= corr;
+        // dk[2r] (group 0) and dk[2r+1] (group 1, or group 0 again) belong to row gid + 8r
+        float sc[2];
 #pragma unroll
-        for (int u = 0; u < 2 * NW; ++u)
+        for (int r = 0; r < 2; ++r) {
+          const float2 ab0 = unpack_h2(ka[r][0]);
+          float dot = (ab0.y - ab0.x) * dk[2 * r];
+          float off = ab0.x * Q0;
+          if (NG == 2) {
+            const float2 ab1 = unpack_h2(ka[r][NG - 1]);
+            dot = fmaf(ab1.y - ab1.x, dk[2 * r + 1], dot);
+            off = fmaf(ab1.x, Q1, off);
+          }
+          sc[r] = valid[r] ? fmaf(dot, ck, off) : -INFINITY;
+        }
+        // lazy rescaling: the reference maximum moves only when a score exceeds it by more
+        // than 2^8, so p stays <= 256 and the accumulators rarely need scaling; the warp
+        // maximum is taken only then
+        const float mloc = fmaxf(sc[0], sc[1]);
+        if (__any_sync(0xFFFFFFFFu, mloc > m_run + 8.0f)) {
+          float mx = mloc;
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+          const float corr = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mx);
+          l_run *= corr;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
+          for (int u = 0; u < 2 * NW; ++u)
 #pragma unroll
-        for (int g = 0; g < NG; ++g) asum[g] *= corr;
-        m_run = mx;
-      }
-      // invalid rows hold -inf scores, and ex2(-inf) = 0
-      const float p0 = ex2(sc[0] - m_run);
-      const float p1 = ex2(sc[1] - m_run);
-      float ps = p0 + p1;
-      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
-      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 8);
-      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
-      l_run += ps;
+            for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) asum[g] *= corr;
+          m_run = mx;
+        }
+        // invalid rows hold -inf scores, and ex2(-inf) = 0
+        const float p0 = ex2(sc[0] - m_run);
+        const float p1 = ex2(sc[1] - m_run);
+        l_run += p0 + p1;
 
-      // ---- V weights w_tg = p_t * s_tg (fp16) and the offset term sum_t p_t a_tg; rows
-      // past the end contribute exact zeros whatever their (never written) bytes hold
-      uint32_t wrow[2];
+        // ---- V weights w_tg = p_t (b - a)_tg / 15 (fp16) and the offset term
+        // sum_t p_t a_tg; rows past the end take (a, b) = (0, 0), so their never-written
+        // bytes contribute exact zeros
+        uint32_t wrow[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float p = r ? p1 : p0;
-        const float2 ab0 = unpack_h2(va[r][0]);
-        const float w0 = valid[r] ? p * (ab0.y - ab0.x) * (1.0f / 15.0f) : 0.0f;
-        asum[0] += valid[r] ? p * ab0.x : 0.0f;
-        float w1 = 0.0f;
-        if (NG == 2) {
-          const float2 ab1 = unpack_h2(va[r][NG - 1]);
-          w1 = valid[r] ? p * (ab1.y - ab1.x) * (1.0f / 15.0f) : 0.0f;
-          asum[NG - 1] += valid[r] ? p * ab1.x : 0.0f;
+        for (int r = 0; r < 2; ++r) {
+          const float p = r ? p1 : p0;
+          const float p15 = p * (1.0f / 15.0f);
+          const float2 ab0 = unpack_h2(valid[r] ? va[r][0] : 0u);
+          const float w0 = p15 * (ab0.y - ab0.x);
+          asum[0] = fmaf(p, ab0.x, asum[0]);
+          float w1 = w0;
+          if (NG == 2) {
+            const float2 ab1 = unpack_h2(valid[r] ? va[r][NG - 1] : 0u);
+            w1 = p15 * (ab1.y - ab1.x);
+            asum[NG - 1] = fmaf(p, ab1.x, asum[NG - 1]);
+          }
+          wrow[r] = pack_h2(w0, w1);
         }
-        wrow[r] = pack_h2(w0, w1);
-      }
-      // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid (group n)
-      const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
-      const uint32_t wb = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig + 4);
-      const uint32_t wc = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig);
-      const uint32_t wd = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig + 4);
-      uint32_t bv0 = 0u, bv1 = 0u;
-      if (gid < NG) {
-        const uint32_t sel = gid ? 0x7632u : 0x5410u;   // pick the high or low halves
-        bv0 = __byte_perm(wa, wb, sel);
-        bv1 = __byte_perm(wc, wd, sel);
-      }
-      // ---- V codes transposed to (channel rows, position columns)
+        // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid carrying group n & 1
+        const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
+        const uint32_t wb = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig + 4);
+        const uint32_t wc = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig);
+        const uint32_t wd = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig + 4);
+        const uint32_t sel = (NG == 2 && (gid & 1)) ? 0x7632u : 0x5410u;
+        const uint32_t bv0 = __byte_perm(wa, wb, sel);
+        const uint32_t bv1 = __byte_perm(wc, wd, sel);
+        // ---- V codes: transpose each packed word first (lane gets 4 channels at two
+        // positions), then split it into code pairs (channel rows, position columns)
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        uint32_t c0[4], c1[4];
-        code_pairs(vw[0][w], c0);
-        code_pairs(vw[1][w], c1);
-        mma16816(acc[2 * w], movtrans(c0[0]), movtrans(c0[1]), movtrans(c1[0]), movtrans(c1[1]),
-                 bv0, bv1);
-        mma16816(acc[2 * w + 1], movtrans(c0[2]), movtrans(c0[3]), movtrans(c1[2]),
-                 movtrans(c1[3]), bv0, bv1);
+        for (int w = 0; w < NW; ++w) {
+          uint32_t c0[4], c1[4];
+          code_pairs(movtrans(vw[0][w]), c0);
+          code_pairs(movtrans(vw[1][w]), c1);
+          mma16816(acc[2 * w], c0[0], c0[1], c1[0], c1[1], bv0, bv1);
+          mma16816(acc[2 * w + 1], c0[2], c0[3], c1[2], c1[3], bv0, bv1);
+        }
       }
-      // every lane has consumed the words it loaded from this slot: refill it kRing tiles
+      // every lane has consumed the words it loaded from this slot: refill it kRing slots
       // ahead (releasing it any earlier would let the copy race the slot's last readers)
       __syncwarp();
       if (lane == 0) issue();
+      ++consumed;
+      if (++cs == kRing) {
+        cs = 0;
+        cph ^= 1u;
+      }
     }
     if (!ok) break;
 
     // ---- epilogue of the item: o_j = (acc + sum_t p_t a_tg) / l
+    float l = l_run;
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 4);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
-
     }
-    if (tig == 0) {
-      const int g_lo = (NG == 2) ? (gid >> 2) : 0;      // group of channel row gid
-      const float A = (NG == 2 && g_lo) ? asum[NG - 1] : asum[0];
-
-      // channel rows of mma u: pair 2u has factor 1, pair 2u+1 factor 16
-      // acc holds 2^-24 * sum_t w_t c_tj (pair 2u) or 2^-20 * ... (pair 2u+1, factor 16)
-      auto vx_of = [&](int u) { return (g_lo ? acc[u][1] : acc[u][0]) * 16777216.0f + A; };
-      auto vy_of = [&](int u) {
-        return (g_lo ? acc[u][3] : acc[u][2]) * 1048576.0f + A;
-      };
-      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-      const int jbase = (gid >> 1) * 8 * NW + 4 * (gid & 1);
+    // acc[2w+h] row gid holds channel cb + 2h (factor 1, times 2^-24), row gid+8 channel
+    // cb + 2h + 1 (factor 16, times 2^-20), cb = 8*NW*(gid>>1) + 8w + 4*(gid&1); its
+    // columns 2tig / 2tig+1 hold groups 0 / 1 (the same in every tig), so lane tig writes
+    // the accumulators u with u % 4 == tig
+    const int g_lane = (NG == 2) ? (gid >> 2) : 0;      // group of every channel of row gid
+    const float A = (NG == 2 && g_lane) ? asum[NG - 1] : asum[0];
+    const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+    const int cbase = 8 * NW * (gid >> 1) + 4 * (gid & 1);
+    uint16_t* o = out + (int64_t)it.b * H * D + (int64_t)it.hd * D;
+    float* pp = partial + (int64_t)ci * (D + 2);
+#pragma unroll
+    for (int u = 0; u < 2 * NW; ++u) {
+      if ((u & 3) != tig) continue;
+      const int ch = cbase + 8 * (u >> 1) + 2 * (u & 1);
+      const float vx = (g_lane ? acc[u][1] : acc[u][0]) * 16777216.0f + A;
+      const float vy = (g_lane ? acc[u][3] : acc[u][2]) * 1048576.0f + A;
       if (splits == 1) {
-        uint16_t* o = out + (int64_t)it.b * H * D + (int64_t)it.hd * D;
-#pragma unroll
-        for (int u = 0; u < 2 * NW; ++u) {
-          const int px = 2 * u, py = 2 * u + 1;
-          o[jbase + 8 * (px >> 2) + (px & 3)] = f2h(vx_of(u) * inv_l);
-          o[jbase + 8 * (py >> 2) + (py & 3)] = f2h(vy_of(u) * inv_l);
-        }
+        o[ch] = f2h(vx * inv_l);
+        o[ch + 1] = f2h(vy * inv_l);
       } else {
-        float* pp = partial + (int64_t)ci * (D + 2);
-#pragma unroll
-        for (int u = 0; u < 2 * NW; ++u) {
-          const int px = 2 * u, py = 2 * u + 1;
-          pp[jbase + 8 * (px >> 2) + (px & 3)] = vx_of(u);
-          pp[jbase + 8 * (py >> 2) + (py & 3)] = vy_of(u);
-        }
-        if (gid == 0) {
-          pp[D] = m_run;
-          pp[D + 1] = l_run;
-        }
+        pp[ch] = vx;
+        pp[ch + 1] = vy;
       }
+    }
+    if (splits > 1 && lane == 0) {
+      pp[D] = m_run;
+      pp[D + 1] = l;
     }
     __syncwarp();
   }
 
   // ---- drain: every issued copy must land before the warp's shared memory is released
   if (lane == 0) {
-    for (int64_t g = gc; g < gi; ++g) {
+    for (int g = consumed; g < issued; ++g) {
       const uint32_t bar = bar0 + 8 * (uint32_t)(g % kRing);
       const long long t0 = clock64();
       while (!bar_try(bar, (uint32_t)((g / kRing) & 1))) {
@@ -504,7 +518,9 @@ template <int D>
 int resident_ctas() {
   static int occ = [] {
     int n = 0;
-    // the rings are small: let the shared-memory carveout admit as many CTAs as registers do
+    // the rings exceed the 48 KB default; prefer the carveout that admits the most CTAs
+    cudaFuncSetAttribute(decode_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Ring<D>::CTA_BYTES);
     cudaFuncSetAttribute(decode_attn_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<D>, kWarps * 32,
                                                       Ring<D>::CTA_BYTES) != cudaSuccess ||
