@@ -41,6 +41,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "fg_common.cuh"
 #include "fg_internal.h"
@@ -53,9 +54,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kTile = 16;                 // positions per mma step
-constexpr int kSub = 2;                   // tiles per ring slot
+constexpr int kSub = 3;                   // tiles per ring slot
 constexpr int kSlotPos = kSub * kTile;    // positions per ring slot
-constexpr int kRing = 3;                  // slots per warp
+constexpr int kRing = 2;                  // slots per warp
 constexpr int kPlanWarpsPerSm = 16;       // resident warps per SM assumed by the split plan
 constexpr long long kWaitCycles = 1ll << 32;
 
@@ -150,6 +151,20 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Loads N consecutive 32-bit words from shared memory (N = 1, 2 or 4).
+template <int N>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[N]) {
+  if constexpr (N == 4) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  } else if constexpr (N == 2) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    w[0] = u.x; w[1] = u.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
 }
 
 // Work item -> (b, hd, position range).
@@ -288,47 +303,27 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
 #pragma unroll
     for (int g = 0; g < NG; ++g) asum[g] = 0.0f;
 
-    for (int j = 0; j < it.nslots; ++j) {
-      ok = __all_sync(0xFFFFFFFFu, bar_wait(bar0 + 8 * cs, cph));
-      if (!ok) break;
-      const uint8_t* slot = ring + cs * R::SLOT;
-      const int ts = it.t_begin + j * kSlotPos;
-      const int nsub = min(kSub, (it.t_end - ts + kTile - 1) / kTile);
-      for (int sub = 0; sub < nsub; ++sub) {
-        const int t0 = ts + sub * kTile;
-        // ---- this lane's rows gid and gid+8 of the tile, from shared memory
-        uint32_t kw[2][NW], vw[2][NW], ka[2][NG], va[2][NG];
-        bool valid[2];
+    // One ring slot in three phases: scores of every tile, one softmax step, then the V
+    // accumulation of every tile.  The tiles of a phase are independent, so their
+    // latencies overlap.  MASK (the item's last slot, which reaches past t_end): rows at
+    // or past t_end are masked, including whole tiles the copy skipped, whose stale bytes
+    // are still finite codes and whose statistics are replaced by zeros.
+    auto process = [&](const uint8_t* slot, int ts, auto mask_tag) {
+      constexpr bool MASK = decltype(mask_tag)::value;
+      auto valid = [&](int sub, int r) {
+        return !MASK || ts + sub * kTile + gid + 8 * r < it.t_end;
+      };
+      // ---- phase 1: scores, K codes (rows t) x permuted q
+      float sc[kSub][2];
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        uint32_t kw[2][NW], ka[2][NG];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int row = sub * kTile + gid + 8 * r;
-          const uint8_t* kp = slot + row * R::ROW_CODE + tig * 4 * NW;
-          const uint8_t* vp = kp + R::CODE_BYTES;
-          if (NW == 4) {
-            const uint4 uk = *reinterpret_cast<const uint4*>(kp);
-            const uint4 uv = *reinterpret_cast<const uint4*>(vp);
-            kw[r][0] = uk.x; kw[r][1] = uk.y; kw[r][2 % NW] = uk.z; kw[r][3 % NW] = uk.w;
-            vw[r][0] = uv.x; vw[r][1] = uv.y; vw[r][2 % NW] = uv.z; vw[r][3 % NW] = uv.w;
-          } else {
-            const uint2 uk = *reinterpret_cast<const uint2*>(kp);
-            const uint2 uv = *reinterpret_cast<const uint2*>(vp);
-            kw[r][0] = uk.x; kw[r][1 % NW] = uk.y;
-            vw[r][0] = uv.x; vw[r][1 % NW] = uv.y;
-          }
-          const uint8_t* kap = slot + 2 * R::CODE_BYTES + row * R::ROW_AB;
-          if (NG == 2) {
-            const uint2 a2 = *reinterpret_cast<const uint2*>(kap);
-            const uint2 v2 = *reinterpret_cast<const uint2*>(kap + R::AB_BYTES);
-            ka[r][0] = a2.x; ka[r][NG - 1] = a2.y;
-            va[r][0] = v2.x; va[r][NG - 1] = v2.y;
-          } else {
-            ka[r][0] = *reinterpret_cast<const uint32_t*>(kap);
-            va[r][0] = *reinterpret_cast<const uint32_t*>(kap + R::AB_BYTES);
-          }
-          valid[r] = t0 + gid + 8 * r < it.t_end;
+          load_words<NW>(slot + row * R::ROW_CODE + tig * 4 * NW, kw[r]);
+          load_words<NG>(slot + 2 * R::CODE_BYTES + row * R::ROW_AB, ka[r]);
         }
-
-        // ---- scores: K codes (rows t) x permuted q
         float dk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
@@ -339,7 +334,6 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           mma16816(dk, c0[2], c1[2], c0[3], c1[3], bq[2 * w + 1][0], bq[2 * w + 1][1]);
         }
         // dk[2r] (group 0) and dk[2r+1] (group 1, or group 0 again) belong to row gid + 8r
-        float sc[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float2 ab0 = unpack_h2(ka[r][0]);
@@ -350,48 +344,63 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
             dot = fmaf(ab1.y - ab1.x, dk[2 * r + 1], dot);
             off = fmaf(ab1.x, Q1, off);
           }
-          sc[r] = valid[r] ? fmaf(dot, ck, off) : -INFINITY;
+          sc[sub][r] = valid(sub, r) ? fmaf(dot, ck, off) : -INFINITY;
         }
-        // lazy rescaling: the reference maximum moves only when a score exceeds it by more
-        // than 2^8, so p stays <= 256 and the accumulators rarely need scaling; the warp
-        // maximum is taken only then
-        const float mloc = fmaxf(sc[0], sc[1]);
-        if (__any_sync(0xFFFFFFFFu, mloc > m_run + 8.0f)) {
-          float mx = mloc;
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-          const float corr = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mx);
-          l_run *= corr;
+      }
+      // ---- phase 2: lazy rescaling: the reference maximum moves only when a score
+      // exceeds it by more than 2^8, so p stays <= 256 and the accumulators rarely need
+      // scaling; the warp maximum is taken only then
+      float mloc = fmaxf(sc[0][0], sc[0][1]);
 #pragma unroll
-          for (int u = 0; u < 2 * NW; ++u)
+      for (int sub = 1; sub < kSub; ++sub) mloc = fmaxf(mloc, fmaxf(sc[sub][0], sc[sub][1]));
+      if (__any_sync(0xFFFFFFFFu, mloc > m_run + 8.0f)) {
+        float mx = mloc;
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const float corr = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mx);
+        l_run *= corr;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
+        for (int u = 0; u < 2 * NW; ++u)
 #pragma unroll
-          for (int g = 0; g < NG; ++g) asum[g] *= corr;
-          m_run = mx;
+          for (int c = 0; c < 4; ++c) acc[u][c] *= corr;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) asum[g] *= corr;
+        m_run = mx;
+      }
+      // invalid rows hold -inf scores, and ex2(-inf) = 0
+      float p[kSub][2];
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        p[sub][0] = ex2(sc[sub][0] - m_run);
+        p[sub][1] = ex2(sc[sub][1] - m_run);
+        l_run += p[sub][0] + p[sub][1];
+      }
+      // ---- phase 3: V weights w_tg = p_t (b - a)_tg / 15 (fp16), the offset term
+      // sum_t p_t a_tg, and the V codes (channel rows, position columns)
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        uint32_t vw[2][NW], va[2][NG];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int row = sub * kTile + gid + 8 * r;
+          load_words<NW>(slot + R::CODE_BYTES + row * R::ROW_CODE + tig * 4 * NW, vw[r]);
+          load_words<NG>(slot + 2 * R::CODE_BYTES + R::AB_BYTES + row * R::ROW_AB, va[r]);
         }
-        // invalid rows hold -inf scores, and ex2(-inf) = 0
-        const float p0 = ex2(sc[0] - m_run);
-        const float p1 = ex2(sc[1] - m_run);
-        l_run += p0 + p1;
-
-        // ---- V weights w_tg = p_t (b - a)_tg / 15 (fp16) and the offset term
-        // sum_t p_t a_tg; rows past the end take (a, b) = (0, 0), so their never-written
-        // bytes contribute exact zeros
         uint32_t wrow[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float p = r ? p1 : p0;
-          const float p15 = p * (1.0f / 15.0f);
-          const float2 ab0 = unpack_h2(valid[r] ? va[r][0] : 0u);
+          const float pr = p[sub][r];
+          const float p15 = pr * (1.0f / 15.0f);
+          // rows past the end take (a, b) = (0, 0): their bytes contribute exact zeros
+          const float2 ab0 = unpack_h2(valid(sub, r) ? va[r][0] : 0u);
           const float w0 = p15 * (ab0.y - ab0.x);
-          asum[0] = fmaf(p, ab0.x, asum[0]);
+          asum[0] = fmaf(pr, ab0.x, asum[0]);
           float w1 = w0;
           if (NG == 2) {
-            const float2 ab1 = unpack_h2(valid[r] ? va[r][NG - 1] : 0u);
+            const float2 ab1 = unpack_h2(valid(sub, r) ? va[r][NG - 1] : 0u);
             w1 = p15 * (ab1.y - ab1.x);
-            asum[NG - 1] = fmaf(p, ab1.x, asum[NG - 1]);
+            asum[NG - 1] = fmaf(pr, ab1.x, asum[NG - 1]);
           }
           wrow[r] = pack_h2(w0, w1);
         }
@@ -403,8 +412,8 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
         const uint32_t sel = (NG == 2 && (gid & 1)) ? 0x7632u : 0x5410u;
         const uint32_t bv0 = __byte_perm(wa, wb, sel);
         const uint32_t bv1 = __byte_perm(wc, wd, sel);
-        // ---- V codes: transpose each packed word first (lane gets 4 channels at two
-        // positions), then split it into code pairs (channel rows, position columns)
+        // each packed code word is transposed first (the lane gets 4 channels at two
+        // positions), then split into code pairs
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           uint32_t c0[4], c1[4];
@@ -414,6 +423,17 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           mma16816(acc[2 * w + 1], c0[2], c0[3], c1[2], c1[3], bv0, bv1);
         }
       }
+    };
+
+    for (int j = 0; j < it.nslots; ++j) {
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(bar0 + 8 * cs, cph));
+      if (!ok) break;
+      const uint8_t* slot = ring + cs * R::SLOT;
+      const int ts = it.t_begin + j * kSlotPos;
+      if (ts + kSlotPos <= it.t_end)
+        process(slot, ts, std::false_type{});
+      else
+        process(slot, ts, std::true_type{});
       // every lane has consumed the words it loaded from this slot: refill it kRing slots
       // ahead (releasing it any earlier would let the copy race the slot's last readers)
       __syncwarp();
