@@ -44,7 +44,7 @@ UNIT = "tokens/s"
 # DRAM bytes (read + write) per GEMM launch: the mean over the 560 GEMM launches of one
 # generation pass of this workload, from an ncu capture of dram__bytes_read.sum and
 # dram__bytes_write.sum; reset to None whenever the GEMM kernel changes
-GEMM_TRAFFIC_PER_LAUNCH = 83.23e6
+GEMM_TRAFFIC_PER_LAUNCH = None
 
 
 def peaks():
@@ -264,6 +264,8 @@ def run_gpu(args, wl):
     pk = peaks()
     g_ = prof["q4_dequant_gemm_tc"]
     gemm_tflops = g_["work"] / (g_["ms"] * 1e-3) / 1e12 if g_["ms"] else None
+    d_ = prof["q4_dequant_gemm_stream"]
+    dgemm_gbs = d_["work"] / (d_["ms"] * 1e-3) / 1e9 if d_["ms"] else None
     a_ = prof["q4kv_decode_attn"]
     attn_gbs = a_["work"] / (a_["ms"] * 1e-3) / 1e9 if a_["ms"] else None
     total_kernel_ms = sum(p["ms"] for p in prof.values())
@@ -288,6 +290,11 @@ def run_gpu(args, wl):
                      "traffic": GEMM_TRAFFIC_PER_LAUNCH,
                      "share_of_kernel_time": round(g_["ms"] / total_kernel_ms, 4)
                      if total_kernel_ms else None},
+        "decode_gemm_roofline": {"kernel": "q4_dequant_gemm_stream", "bound": "hbm",
+                                 "achieved": round(dgemm_gbs, 1) if dgemm_gbs else None,
+                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                 "frac": round(dgemm_gbs / pk["hbm_gbs"], 4) if dgemm_gbs else None,
+                                 "launches": d_["launches"]},
         "decode_attn_roofline": {"kernel": "q4kv_decode_attn", "bound": "hbm",
                                  "achieved": round(attn_gbs, 1) if attn_gbs else None,
                                  "peak": pk["hbm_gbs"], "unit": "GB/s",

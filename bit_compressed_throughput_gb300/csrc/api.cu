@@ -198,11 +198,14 @@ int run_gemm(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bi
   cudaEvent_t mid = (p.splits > 1) ? sp.mid_event() : nullptr;
   cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid);
   if (e != cudaSuccess) return set_cuda_error(e);
+  const bool stream = (p.kind == kGemmStream);
+  const int kind = stream ? FG_K_GEMM_STREAM : FG_K_GEMM;
+  const double w = stream ? work_gemm_stream(M, W.N, W.K) : work_gemm(M, W.N, W.K);
   if (p.splits > 1 && mid) {
-    sp.close(FG_K_GEMM, work_gemm(M, W.N, W.K), mid);
+    sp.close(kind, w, mid);
     sp.stop(FG_K_GEMM_REDUCE, work_gemm_reduce(M, W.N, p.splits));
   } else {
-    sp.stop(FG_K_GEMM, work_gemm(M, W.N, W.K));
+    sp.stop(kind, w);
   }
   return FG_OK;
 }
@@ -307,9 +310,12 @@ const char* fg_last_error(void) { return t_last_error.c_str(); }
 int fg_check_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return set_cuda_error(e);
-  unsigned int flag = 0, aflag = 0;
+  unsigned int flag = 0, sflag = 0, aflag = 0;
   e = gemm_read_error(&flag);
   if (e != cudaSuccess) return set_cuda_error(e);
+  e = gemm_stream_read_error(&sflag);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  flag |= sflag;
   e = attn_read_error(&aflag);
   if (e != cudaSuccess) return set_cuda_error(e);
   if (flag || aflag) {
@@ -587,7 +593,7 @@ const char* fg_kernel_name(int kind) {
   static const char* names[FG_K_COUNT] = {
       "q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
       "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn",
-      "layernorm"};
+      "layernorm", "q4_dequant_gemm_stream"};
   return (kind >= 0 && kind < FG_K_COUNT) ? names[kind] : "unknown";
 }
 

@@ -57,8 +57,13 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
                                cudaEvent_t mid_event);
 
 // Dequant-fused GEMM plan: tn tokens x 128 channels per tile, split-K factor and
-// workspace.
+// workspace.  kind 0: the tiled kernel (restored weights in shared memory); kind 1: the
+// weight-streaming kernel for M <= 128 (restored weights in tensor memory).
+constexpr int kGemmTiled = 0;
+constexpr int kGemmStream = 1;
+constexpr int kStreamStage = 4;          // k-blocks of 64 per code stage of the streaming kernel
 struct GemmPlan {
+  int kind;
   int64_t M, N, K;
   int tn;                  // tokens per tile: a multiple of 16 in [16, 256]
   int tiles_t, tiles_c, kblocks, splits, kb_per_split;
@@ -72,12 +77,18 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         void* ws, cudaStream_t st, cudaEvent_t mid_event);
 // Device error words of the bounded waits (GEMM, decode attention): read-and-clear.
 cudaError_t gemm_read_error(unsigned int* out);
+cudaError_t gemm_stream_read_error(unsigned int* out);
 cudaError_t attn_read_error(unsigned int* out);
 
 // Algorithmic work of one launch (bytes for memory-bound kernels, flops for the GEMM and
 // prefill attention): 4-bit storage costs 0.5 byte per element plus one (a, b) fp16 pair
 // per group of 64, i.e. 0.5625 byte.
 inline double work_gemm(int64_t M, int64_t N, int64_t K) { return 2.0 * M * N * K; }
+// Weight-streaming GEMM (few tokens): bound by the 4-bit weight stream, so its work is
+// bytes: the weights at 0.5625 byte per element plus the fp16 activations in and out.
+inline double work_gemm_stream(int64_t M, int64_t N, int64_t K) {
+  return 0.5625 * K * N + 2.0 * M * K + 2.0 * M * N;
+}
 inline double work_gemm_reduce(int64_t M, int64_t N, int splits) {
   return (double)splits * M * N * 4.0 + 2.0 * M * N;
 }

@@ -55,6 +55,7 @@
 
 #include "fg_common.cuh"
 #include "fg_internal.h"
+#include "gemm_tc.cuh"
 
 namespace fg {
 
@@ -96,36 +97,6 @@ __host__ __device__ constexpr uint32_t make_idesc(int tn) {
   return (1u << 4) | (1u << 15) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(TCH >> 4) << 24);
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-// Non-blocking probe of a phase: far cheaper than try_wait when the phase is already
-// complete, which is the common case on the MMA issuer's path.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
 // Bounded wait.  Returns false (and raises the CTA abort flag) on timeout or when another
 // warp already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -140,74 +111,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
   return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x),
-      "r"(y), "r"(bar)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: start, leading / stride byte offsets (>> 4), the
-// descriptor version bit of this architecture, 128-byte swizzle layout.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t x, uint32_t s, uint32_t c) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&s),
-                      *reinterpret_cast<__half2*>(&c));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// Restore 8 codes (one word) of one group to 4 half2 in (n0,n4),(n1,n5),(n2,n6),(n3,n7).
-__device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s16, uint32_t c) {
-  uint4 o;
-  o.x = hfma2_u32(((w << 6) & 0x03C003C0u) | 0x3C003C00u, s16, c);
-  o.y = hfma2_u32(((w << 2) & 0x03C003C0u) | 0x3C003C00u, s16, c);
-  o.z = hfma2_u32(((w >> 2) & 0x03C003C0u) | 0x3C003C00u, s16, c);
-  o.w = hfma2_u32(((w >> 6) & 0x03C003C0u) | 0x3C003C00u, s16, c);
-  return o;
 }
 
 // 8 x 8 fp16 transpose inside each 8-lane group of a warp.  On entry lane p of the group
@@ -239,14 +142,6 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hadd2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
-
-struct EpiArgs {
-  const uint16_t* bias;
-  const uint16_t* residual;
-  uint16_t* Y;
-  float* partial;     // split-K: [splits][M][N] fp32, else null
-  int epi;
-};
 
 // Bias / ReLU / residual on 8 consecutive outputs and the fp16 store (reduce kernel).
 __device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int64_t row, int n,
@@ -705,8 +600,10 @@ gemm_reduce_kernel(const float* __restrict__ partial, int splits, int64_t M, int
   epilogue8(ea, v, row, n, N);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
 
 cudaError_t get_encode() {
   std::call_once(g_encode_once, [] {
@@ -733,11 +630,49 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
+
+// Weight-streaming plan (M <= 128): one token tile, 128-channel tiles, K split so that the
+// busiest persistent CTA (units taken round-robin) has the fewest k-blocks, counting about
+// two k-blocks of pipeline ramp per unit and four for a split's partials and reduce.  Splits
+// are whole code stages of kStreamStage k-blocks.  The split count is capped independently
+// of the SM count, and the workspace is sized for the cap, so a workspace sized by the query
+// for kMaxSms covers every device.
+static void stream_plan(GemmPlan& p, int nsm) {
+  p.kind = kGemmStream;
+  p.tiles_t = 1;
+  p.tn = (int)std::max<int64_t>(16, (p.M + 15) / 16 * 16);
+  p.tiles_c = (int)(p.N / TCH);
+  p.kblocks = (int)((p.K + BK - 1) / BK);
+  const int cap = std::max(1, std::min({16, p.kblocks / 4,
+                                        (2 * kMaxSms + p.tiles_c - 1) / p.tiles_c}));
+  const int64_t cta = std::max(1, nsm);
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int s = 1; s <= cap; ++s) {
+    const int kbs = ((p.kblocks + s - 1) / s + kStreamStage - 1) / kStreamStage * kStreamStage;
+    if (s > 1 && (s - 1) * kbs >= p.kblocks) break;    // an empty split
+    const int64_t rounds = ((int64_t)p.tiles_c * s + cta - 1) / cta;
+    const int64_t cost = rounds * (kbs + 2) + (s > 1 ? 4 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  p.kb_per_split = ((p.kblocks + best - 1) / best + kStreamStage - 1) / kStreamStage * kStreamStage;
+  p.splits = (p.kblocks + p.kb_per_split - 1) / p.kb_per_split;
+  p.ws_bytes = (cap > 1) ? (size_t)cap * p.M * p.N * sizeof(float) : 0;
+  p.units = (int64_t)p.tiles_c * p.splits;
+  p.grid = (int)std::min<int64_t>(p.units, nsm);
+}
 
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
   GemmPlan p{};
   p.M = M; p.N = N; p.K = K;
+  if (M > 0 && M <= 128) {
+    stream_plan(p, nsm);
+    return p;
+  }
+  p.kind = kGemmTiled;
   p.tiles_t = (int)std::max<int64_t>(1, (M + TN_MAX - 1) / TN_MAX);
   // tokens per tile: the smallest multiple of 16 that covers M in tiles_t tiles
   const int64_t per = (M + p.tiles_t - 1) / p.tiles_t;
@@ -782,6 +717,14 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
+  if (p.kind == kGemmStream) {
+    e = launch_gemm_stream(p, W, tmX, ea, st);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    if (mid_event) cudaEventRecord(mid_event, st);
+    const int64_t chunks = p.M * (p.N / 8);
+    return launch_pdl(gemm_reduce_kernel, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0,
+                      st, static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
+  }
   // ring depths: large token tiles (prefill) pair each restored slot with an X slot (4 + 4,
   // 6 code stages); small ones (decode) keep 6 X slots (L2 latency of the X tile) and spend
   // the rest on restored slots (so a restore waits for the MMAs of a k-block many k-blocks

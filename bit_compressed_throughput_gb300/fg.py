@@ -23,9 +23,10 @@ FG_OK, FG_ERR_ARG, FG_ERR_SHAPE, FG_ERR_WORKSPACE = 0, -1, -2, -3
 FG_ERR_CUDA, FG_ERR_ARCH, FG_ERR_CAPACITY, FG_ERR_TIMEOUT = -4, -5, -6, -7
 FG_EPI_NONE, FG_EPI_RELU, FG_EPI_RESIDUAL = 0, 1, 2
 KINDS = ["q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
-         "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn", "layernorm"]
+         "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn", "layernorm",
+         "q4_dequant_gemm_stream"]
 K_QUANT, K_DEQUANT, K_GEMM, K_GEMM_REDUCE, K_KV_APPEND, K_DECODE_ATTN, K_DECODE_COMBINE, \
-    K_PREFILL_ATTN, K_LAYERNORM = range(9)
+    K_PREFILL_ATTN, K_LAYERNORM, K_GEMM_STREAM = range(10)
 
 
 class fg_q4mat(C.Structure):

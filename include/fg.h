@@ -234,7 +234,9 @@ int fg_check_device_error(void* stream);
 enum {
   FG_K_QUANT = 0, FG_K_DEQUANT = 1, FG_K_GEMM = 2, FG_K_GEMM_REDUCE = 3,
   FG_K_KV_APPEND = 4, FG_K_DECODE_ATTN = 5, FG_K_DECODE_COMBINE = 6,
-  FG_K_PREFILL_ATTN = 7, FG_K_LAYERNORM = 8, FG_K_COUNT = 9
+  FG_K_PREFILL_ATTN = 7, FG_K_LAYERNORM = 8,
+  FG_K_GEMM_STREAM = 9,   /* the weight-streaming GEMM (M <= 128): work counted in bytes */
+  FG_K_COUNT = 10
 };
 int fg_prof_enable(int on);
 int fg_prof_reset(void);

@@ -179,6 +179,25 @@ def test_gemm_small(fg, M, K, N, epi, bias):
     gemm_case(fg, M, K, N, epi, bias, seed=M * 31 + K + N)
 
 
+@pytest.mark.parametrize("M,K,N,epi,bias", [
+    (128, 4096, 4096, 2, True),     # largest token tile of the streaming kernel, split K
+    (127, 208, 512, 1, True),       # ragged M and K (three k-blocks and 16 rows)
+    (16, 16, 256, 0, False),        # a single partial k-block
+    (64, 2048, 12288, 0, True),     # decode QKV width: 96 channel tiles, K split in three
+    (8, 16384, 1024, 2, False),     # long K over few tiles: sixteen splits
+])
+def test_gemm_stream(fg, M, K, N, epi, bias):
+    """M <= 128 runs the weight-streaming kernel (restored weights in tensor memory)."""
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    try:
+        gemm_case(fg, M, K, N, epi, bias, seed=M * 7 + K + N)
+    finally:
+        fg.fg_prof_enable(False)
+    assert fg.fg_prof_query(fg.K_GEMM_STREAM)["launches"] == 1
+    assert fg.fg_prof_query(fg.K_GEMM)["launches"] == 0
+
+
 def test_gemm_split_k(fg):
     wsb = gemm_case(fg, 64, 4096, 512, 2, True, seed=77)
     assert wsb > 0                                        # the split-K path ran
