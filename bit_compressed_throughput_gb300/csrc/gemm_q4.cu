@@ -633,7 +633,8 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 
 // Weight-streaming plan (M <= 128): one token tile, 128-channel tiles, K split so that the
 // busiest persistent CTA (units taken round-robin) has the fewest k-blocks, counting about
-// two k-blocks of pipeline ramp per unit and four for a split's partials and reduce.  Splits
+// two k-blocks of pipeline ramp per unit and 24 (~6 us) for a split's partials and reduce
+// launch.  Splits
 // are whole code stages of kStreamStage k-blocks.  The split count is capped independently
 // of the SM count, and the workspace is sized for the cap, so a workspace sized by the query
 // for kMaxSms covers every device.
@@ -652,7 +653,7 @@ static void stream_plan(GemmPlan& p, int nsm) {
     const int kbs = ((p.kblocks + s - 1) / s + kStreamStage - 1) / kStreamStage * kStreamStage;
     if (s > 1 && (s - 1) * kbs >= p.kblocks) break;    // an empty split
     const int64_t rounds = ((int64_t)p.tiles_c * s + cta - 1) / cta;
-    const int64_t cost = rounds * (kbs + 2) + (s > 1 ? 4 : 0);
+    const int64_t cost = rounds * (kbs + 2) + (s > 1 ? 24 : 0);
     if (best_cost < 0 || cost < best_cost) {
       best = s;
       best_cost = cost;
