@@ -197,6 +197,18 @@ def time_region(fn, steps, dist=None):
     return replicas.max_over_ranks(e0.elapsed_time(e1), dist, device="cuda")
 
 
+def cost_model_line(wl, value):
+    """The pages' analytical cost model re-parameterised with the measured peaks: the
+    roofline-ideal throughput of this workload and the measured fraction of it."""
+    from bit_compressed_throughput_gb300 import cost_model
+    hw = cost_model.measured_peaks(ROOT)
+    p = cost_model.predict(wl, hw, "kernel", include_aux=True)
+    return {"predicted_tokens_per_s": round(p["tokens_per_s"], 1),
+            "measured_over_predicted": round(value / p["tokens_per_s"], 4),
+            "granularity": "per-kernel max(HBM bytes / bandwidth, flops / tensor peak), summed",
+            "peaks": "measured HBM copy and sustained bf16"}
+
+
 def run_gpu(args, wl):
     import torch
     world, rank, local = dist_env()
@@ -302,6 +314,7 @@ def run_gpu(args, wl):
                                  "launches": a_["launches"]},
         "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)}
                     for k, v in prof.items() if v["launches"]},
+        "cost_model": cost_model_line(wl, value),
         "eager_ms_per_step": round(ms_eager / args.steps, 3),
         "gpu_launches": launches,
         "e2e": {"value": round(replicas.total_tokens(world, wl.B, wl.n, args.steps)
