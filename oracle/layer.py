@@ -87,6 +87,43 @@ def decode_attention(q, K, V, H: int, d: int, dt=F64):
     return (p @ vh).reshape(S_, h)
 
 
+def decode_attention_topk(q, K, V, H: int, d: int, k: int, dt=F64, selected=None):
+    """Top-K sparse decode attention: the scores of all T positions come from K, the
+    softmax runs over all of them, and only the k positions with the highest scores
+    contribute their values: o = sum_{t in top-k} p_t v_t, without renormalising
+    [论文阅读：FlexGen, §3.4 "4-bit 压缩权重和 KV cache": optional sparse attention that
+    loads only the top 10% of the value cache; FlexGen paper explainer, §3.3 "Roadmap for
+    the Deep Dive": Top-K sparse attention, an approximate method that cuts I/O volume].  Readings: p is the full softmax (loading fewer values
+    drops terms, it does not change the others); equal scores at the k-th place go to the
+    lower position.  q [S][h], K, V [S][T][h] -> ([S][h], top-k positions [S][H][k] in
+    decreasing score order).
+
+    ``selected`` ([S][H][k] positions), when given, replaces the selection: the output is
+    then the same weighted sum over those positions (used to evaluate another
+    implementation's choice among near-equal scores).  Parity: pinned by k = T reducing to
+    dense decode attention, k = 1 to the single largest term, and a pure-Python loop."""
+    q, K, V = (np.asarray(t, dtype=dt) for t in (q, K, V))
+    S_, T, h = K.shape
+    qh = q.reshape(S_, H, 1, d)
+    kh, vh = _heads(K, H, d), _heads(V, H, d)
+    sc = ((qh @ kh.transpose(0, 1, 3, 2)) / np.sqrt(dt(d)))[:, :, 0, :]      # [S][H][T]
+    e = np.exp(sc - sc.max(axis=-1, keepdims=True))
+    p = e / e.sum(axis=-1, keepdims=True)
+    if selected is None:
+        # stable sort on -score: among equal scores the lower position comes first
+        selected = np.argsort(-sc, axis=-1, kind="stable")[:, :, :k]
+    sel = np.asarray(selected)
+    w = np.take_along_axis(p, sel, axis=-1)                                   # [S][H][k]
+    vs = np.take_along_axis(vh, sel[..., None], axis=2)                       # [S][H][k][d]
+    o = (w[..., None] * vs).sum(axis=2)
+    return o.reshape(S_, h), sel
+
+
+def topk_count(T: int, frac: float = 0.1) -> int:
+    """Positions kept by a top-fraction rule: ceil(frac * T), at least one."""
+    return max(1, int(np.ceil(frac * T - 1e-9)))
+
+
 class QuantLayer:
     """A layer's weights quantised once (R1-R3) and restored to fp16 (R4).
 

@@ -107,6 +107,57 @@ def test_decode_attention_loop():
             assert np.allclose(o[s, sl], ref, rtol=0, atol=1e-12)
 
 
+def test_topk_attention_pins():
+    r = np.random.Generator(np.random.PCG64(15))
+    S, T, H, d = 2, 9, 2, 4
+    q = r.standard_normal((S, H * d))
+    K, V = r.standard_normal((S, T, H * d)), r.standard_normal((S, T, H * d))
+    # k = T: every value is loaded, the dense result
+    o, _ = OL.decode_attention_topk(q, K, V, H, d, T)
+    assert np.allclose(o, OL.decode_attention(q, K, V, H, d), rtol=0, atol=1e-13)
+    # k = 1: the largest-score position's probability times its value
+    o1, sel = OL.decode_attention_topk(q, K, V, H, d, 1)
+    for s in range(S):
+        for hh in range(H):
+            sl = slice(hh * d, hh * d + d)
+            scores = [sum(a * b for a, b in zip(q[s, sl], K[s, t, sl])) / math.sqrt(d)
+                      for t in range(T)]
+            t_max = max(range(T), key=lambda t: (scores[t], -t))
+            z = sum(math.exp(x - scores[t_max]) for x in scores)
+            assert sel[s, hh, 0] == t_max
+            assert np.allclose(o1[s, sl], V[s, t_max, sl] / z, rtol=0, atol=1e-13)
+    # a middle k against a pure-Python loop (sort by score, ties to the lower position)
+    k = 4
+    ok, selk = OL.decode_attention_topk(q, K, V, H, d, k)
+    for s in range(S):
+        for hh in range(H):
+            sl = slice(hh * d, hh * d + d)
+            scores = [sum(a * b for a, b in zip(q[s, sl], K[s, t, sl])) / math.sqrt(d)
+                      for t in range(T)]
+            order = sorted(range(T), key=lambda t: (-scores[t], t))[:k]
+            m = max(scores)
+            z = sum(math.exp(x - m) for x in scores)
+            ref = [sum(math.exp(scores[t] - m) / z * V[s, t, sl][j] for t in order)
+                   for j in range(d)]
+            assert list(selk[s, hh]) == order
+            assert np.allclose(ok[s, sl], ref, rtol=0, atol=1e-13)
+    # the kept probability mass grows with k and reaches 1 at k = T
+    q2 = r.standard_normal((1, H * d))
+    K2, V1 = r.standard_normal((1, T, H * d)), np.ones((1, T, H * d))
+    mass = [OL.decode_attention_topk(q2, K2, V1, H, d, kk)[0][0, 0] for kk in range(1, T + 1)]
+    assert all(b >= a for a, b in zip(mass, mass[1:])) and abs(mass[-1] - 1) < 1e-13
+
+
+def test_topk_ties_go_to_the_lower_position():
+    H, d, T = 1, 4, 6
+    K = np.zeros((1, T, d))          # every score equal
+    V = np.arange(T * d, dtype=np.float64).reshape(1, T, d)
+    o, sel = OL.decode_attention_topk(np.ones((1, d)), K, V, H, d, 2)
+    assert sel[0, 0].tolist() == [0, 1]
+    assert np.allclose(o[0], (V[0, 0] + V[0, 1]) / T)
+    assert OL.topk_count(543) == 55 and OL.topk_count(1056) == 106 and OL.topk_count(5) == 1
+
+
 def test_relu():
     assert OL.relu(np.array([-1.0, 0.0, 2.0])).tolist() == [0.0, 0.0, 2.0]
 
