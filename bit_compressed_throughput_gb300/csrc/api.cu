@@ -422,6 +422,36 @@ int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* k
                          static_cast<cudaStream_t>(stream));
 }
 
+size_t fg_decode_attn_topk_workspace_bytes(const fg_kvcache* kv, int32_t len) {
+  if (!kv || check_kv(kv) != FG_OK || len <= 0) return 0;
+  return decode_attn_topk_ws_bytes(*kv, len);
+}
+
+int fg_decode_attn_q4kv_topk(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv,
+                             int32_t len, int32_t k, float scale, uint16_t* out, int32_t* sel,
+                             void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  if (len <= 0 || k <= 0 || k > len) return FG_ERR_SHAPE;
+  if (len > kv->cap) return FG_ERR_CAPACITY;
+  if ((int64_t)(len + k) * 4 > 227 * 1024) return FG_ERR_SHAPE;
+  if (q_stride < kv->h || q_stride % 8 != 0) return FG_ERR_SHAPE;
+  if (!(scale > 0.0f) || !isfinite(scale)) return FG_ERR_ARG;
+  if (kv->B == 0) return FG_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return FG_ERR_ARG;
+  const size_t need = fg_decode_attn_topk_workspace_bytes(kv, len);
+  if (ws_bytes < need || !ws || !aligned16(ws)) return FG_ERR_WORKSPACE;
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp(st);
+  cudaError_t e = launch_decode_attn_topk(q, q_stride, *kv, len, k, scale, out, sel, ws, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  sp.stop(FG_K_DECODE_ATTN_TOPK,
+          work_decode_attn_topk(kv->B, kv->H, len, k, kv->h));
+  return FG_OK;
+}
+
 int fg_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, int32_t d,
                     float scale, uint16_t* out, void* stream) {
   if (nseq < 0 || s < 0 || H <= 0 || (d != 64 && d != 128) || nseq > 65535) return FG_ERR_SHAPE;
@@ -593,7 +623,7 @@ const char* fg_kernel_name(int kind) {
   static const char* names[FG_K_COUNT] = {
       "q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
       "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn",
-      "layernorm", "q4_dequant_gemm_stream"};
+      "layernorm", "q4_dequant_gemm_stream", "q4kv_decode_attn_topk"};
   return (kind >= 0 && kind < FG_K_COUNT) ? names[kind] : "unknown";
 }
 

@@ -56,6 +56,13 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
                                int num_sms, cudaStream_t st, int* kernels_out,
                                cudaEvent_t mid_event);
 
+// Top-K sparse decode attention: score workspace bytes; launches the score and the
+// select-and-attend kernels.
+size_t decode_attn_topk_ws_bytes(const fg_kvcache& kv, int32_t len);
+cudaError_t launch_decode_attn_topk(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
+                                    int32_t len, int32_t k, float scale, uint16_t* out,
+                                    int32_t* sel, void* ws, cudaStream_t st);
+
 // Dequant-fused GEMM plan: tn tokens x 128 channels per tile, split-K factor and
 // workspace.  kind 0: the tiled kernel (restored weights in shared memory); kind 1: the
 // weight-streaming kernel for M <= 128 (restored weights in tensor memory).
@@ -95,6 +102,11 @@ inline double work_gemm_reduce(int64_t M, int64_t N, int splits) {
 inline double work_quantize(double elems) { return elems * (2.0 + 0.5625); }
 inline double work_decode_attn(int64_t B, int64_t len, int64_t h) {
   return 2.0 * B * len * h * 0.5625 + 4.0 * B * h;
+}
+// Top-K attention: the whole 4-bit K, the 4-bit V of k positions, the fp32 scores written
+// and read back, q in and out.
+inline double work_decode_attn_topk(int64_t B, int64_t H, int64_t len, int64_t k, int64_t h) {
+  return B * len * h * 0.5625 + B * k * h * 0.5625 + 8.0 * B * H * len + 4.0 * B * h;
 }
 inline double work_prefill_attn(int64_t nseq, int64_t s, int64_t h) {
   return 2.0 * nseq * h * s * (s + 1);

@@ -24,9 +24,9 @@ FG_ERR_CUDA, FG_ERR_ARCH, FG_ERR_CAPACITY, FG_ERR_TIMEOUT = -4, -5, -6, -7
 FG_EPI_NONE, FG_EPI_RELU, FG_EPI_RESIDUAL = 0, 1, 2
 KINDS = ["q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
          "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn", "layernorm",
-         "q4_dequant_gemm_stream"]
+         "q4_dequant_gemm_stream", "q4kv_decode_attn_topk"]
 K_QUANT, K_DEQUANT, K_GEMM, K_GEMM_REDUCE, K_KV_APPEND, K_DECODE_ATTN, K_DECODE_COMBINE, \
-    K_PREFILL_ATTN, K_LAYERNORM, K_GEMM_STREAM = range(10)
+    K_PREFILL_ATTN, K_LAYERNORM, K_GEMM_STREAM, K_DECODE_ATTN_TOPK = range(11)
 
 
 class fg_q4mat(C.Structure):
@@ -63,6 +63,9 @@ _SIGS = {
                             C.c_int),
     "fg_decode_attn_workspace_bytes": ([C.POINTER(fg_kvcache), _I32], _SZ),
     "fg_decode_attn_q4kv_static": ([_P, _I64, C.POINTER(fg_kvcache), _I32, _F, _P, _P], C.c_int),
+    "fg_decode_attn_q4kv_topk": ([_P, _I64, C.POINTER(fg_kvcache), _I32, _I32, _F, _P, _P, _P,
+                                  _SZ, _P], C.c_int),
+    "fg_decode_attn_topk_workspace_bytes": ([C.POINTER(fg_kvcache), _I32], _SZ),
     "fg_prefill_attn": ([_P, _I32, _I32, _I32, _I32, _F, _P, _P], C.c_int),
     "fg_layernorm": ([_P, _I64, _I32, _P, _P, _F, _P, _P], C.c_int),
     "fg_layer_prefill": ([C.POINTER(fg_dims), C.POINTER(fg_layer), C.POINTER(fg_kvcache), _P, _P,
@@ -235,6 +238,22 @@ def fg_decode_attn_q4kv(q, q_stride: int, cache: KVCacheQ4, length: int, scale: 
     _check("fg_decode_attn_q4kv",
            lib.fg_decode_attn_q4kv(_ptr(q), q_stride, C.byref(st), length, scale, _ptr(out),
                                    _ptr(ws), wsb, _stream(stream)))
+
+
+def fg_decode_attn_topk_workspace_bytes(cache: KVCacheQ4, length: int) -> int:
+    st = cache.struct()
+    return int(lib.fg_decode_attn_topk_workspace_bytes(C.byref(st), length))
+
+
+def fg_decode_attn_q4kv_topk(q, q_stride: int, cache: KVCacheQ4, length: int, k: int,
+                             scale: float, out, ws, sel=None, stream=None):
+    """Top-K sparse decode attention: softmax over all positions' scores, values of the k
+    highest-scoring positions only; ``sel`` (optional int32 [B][H][k]) receives them."""
+    st = cache.struct()
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("fg_decode_attn_q4kv_topk",
+           lib.fg_decode_attn_q4kv_topk(_ptr(q), q_stride, C.byref(st), length, k, scale,
+                                        _ptr(out), _ptr(sel), _ptr(ws), wsb, _stream(stream)))
 
 
 DECODE_ATTN_STATIC_SCRATCH_BYTES = 4 << 20

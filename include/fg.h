@@ -180,6 +180,22 @@ size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len);
 int fg_decode_attn_q4kv_static(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv,
                                int32_t len, float scale, uint16_t* out, void* stream);
 
+/* Top-K sparse decode attention over the same cache: the scores of all positions
+ * 0 .. len-1 come from the 4-bit K and the softmax runs over all of them, but only the k
+ * positions with the highest scores contribute their values:
+ *   out[b][hd*d + j] = sum_{t in top-k(b,hd)} p_t V^_b,hd,t,j   (no renormalisation)
+ * with equal scores at the k-th place going to the lower position.  1 <= k <= len <= cap,
+ * d in {64, 128}, (len + k) * 4 bytes <= 227 KB.  q, out as fg_decode_attn_q4kv.  sel
+ * (nullable): device int32 [B][H][k] receiving the selected positions in increasing
+ * position order.  ws: device scratch of at least fg_decode_attn_topk_workspace_bytes(kv,
+ * len) bytes (the scores).
+ * [论文阅读：FlexGen, §3.4: optional sparse attention that loads only the top 10% of the value
+ *  cache; FlexGen paper explainer, §3.3: Top-K sparse attention cuts I/O volume] */
+int fg_decode_attn_q4kv_topk(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv,
+                             int32_t len, int32_t k, float scale, uint16_t* out, int32_t* sel,
+                             void* ws, size_t ws_bytes, void* stream);
+size_t fg_decode_attn_topk_workspace_bytes(const fg_kvcache* kv, int32_t len);
+
 /* Causal prefill attention over fp16 Q/K/V read from a QKV buffer qkv[nseq*s][3h]
  * (columns q | k | v, head hd at hd*d): out[nseq*s][h] fp16, position i attends over
  * positions 0..i of its own sequence, scores scaled by `scale`.  d in {64, 128}.
@@ -236,7 +252,8 @@ enum {
   FG_K_KV_APPEND = 4, FG_K_DECODE_ATTN = 5, FG_K_DECODE_COMBINE = 6,
   FG_K_PREFILL_ATTN = 7, FG_K_LAYERNORM = 8,
   FG_K_GEMM_STREAM = 9,   /* the weight-streaming GEMM (M <= 128): work counted in bytes */
-  FG_K_COUNT = 10
+  FG_K_DECODE_ATTN_TOPK = 10,   /* both kernels of the top-K attention: bytes */
+  FG_K_COUNT = 11
 };
 int fg_prof_enable(int on);
 int fg_prof_reset(void);

@@ -331,6 +331,107 @@ def test_decode_attention_full_kv_workload_sampled(fg):
         assert_close(f16(out[b:b + 1]), ref, f"kv workload seq {b}")
 
 
+# ----------------------------------------------------------------------------- top-K attention
+
+
+def _topk_check(q16, khat, vhat, H, d, k, got, sel_gpu, label):
+    """The GPU's selection is a valid top-k of the oracle's scores (near-equal scores at the
+    k-th place may fall either way) and its output is the oracle's weighted sum over it."""
+    S = q16.shape[0]
+    qh = q16.astype(np.float64).reshape(S, H, 1, d)
+    kh = khat.astype(np.float64).reshape(S, -1, H, d).transpose(0, 2, 1, 3)
+    sc = ((qh @ kh.transpose(0, 1, 3, 2)) / math.sqrt(d))[:, :, 0, :]       # [S][H][T]
+    kth = -np.sort(-sc, axis=-1)[:, :, k - 1:k]
+    eps = 2e-3 * np.abs(sc).max() + 1e-4
+    picked = np.zeros(sc.shape, dtype=bool)
+    np.put_along_axis(picked, sel_gpu.astype(np.int64), True, axis=-1)
+    assert (np.sort(sel_gpu, axis=-1)[:, :, 1:] > np.sort(sel_gpu, axis=-1)[:, :, :-1]).all(), \
+        f"{label}: repeated position"
+    assert (sc[picked] >= np.broadcast_to(kth, sc.shape)[picked] - eps).all(), f"{label}: low pick"
+    assert (sc[~picked] <= np.broadcast_to(kth, sc.shape)[~picked] + eps).all(), f"{label}: missed"
+    ref, oracle_sel = OL.decode_attention_topk(q16, khat, vhat, H, d, k, selected=sel_gpu)
+    assert_close(got, ref, label)
+    same = np.mean([len(set(a) & set(b)) / k for a, b in
+                    zip(sel_gpu.reshape(-1, k).tolist(),
+                        OL.decode_attention_topk(q16, khat, vhat, H, d, k)[1].reshape(-1, k).tolist())])
+    assert same > 0.95, f"{label}: only {same:.3f} of the oracle's selection"
+
+
+@pytest.mark.parametrize("B,H,d,T,length,k,stride3", [
+    (3, 4, 128, 100, 100, 10, False), (2, 4, 64, 40, 37, 4, True), (2, 2, 128, 600, 600, 60, False),
+    (2, 2, 64, 50, 50, 1, False), (64, 32, 128, 543, 543, 55, True)])
+def test_decode_attention_topk(fg, B, H, d, T, length, k, stride3):
+    h = H * d
+    k16 = fg_synth.random_fp16((B, T, h), seed=B * 77 + T, scale=1.5)
+    v16 = fg_synth.random_fp16((B, T, h), seed=B * 77 + T + 1, scale=1.0, offset=0.2)
+    cache, khat, vhat = oracle_cache_from_rows(fg, k16, v16, T + 3, H)
+    cache.k_codes[:, :, T:] = 0x5A                  # never read: garbage past the end
+    cache.v_codes[:, :, T:] = 0xA5
+    cache.k_ab[:, :, T:] = 0x7E007E00
+    cache.v_ab[:, :, T:] = 0x7E007E00
+    qbuf16 = fg_synth.random_fp16((B, 3 * h if stride3 else h), seed=T + 9, scale=1.5)
+    q16 = qbuf16[:, :h]
+    out = torch.empty((B, h), dtype=torch.float16, device="cuda")
+    sel = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, length), dtype=torch.uint8,
+                     device="cuda")
+    fg.fg_decode_attn_q4kv_topk(dev(qbuf16), qbuf16.shape[1], cache, length, k,
+                                1.0 / math.sqrt(d), out, ws, sel)
+    fg.fg_check_device_error()
+    _topk_check(q16, khat[:, :length], vhat[:, :length], H, d, k, f16(out), host(sel),
+                f"topk B={B} H={H} d={d} len={length} k={k}")
+
+
+def test_decode_attention_topk_all_positions_is_dense(fg):
+    """k = len keeps every value: the dense kernel's result."""
+    B, H, d, T = 4, 4, 128, 300
+    h = H * d
+    k16 = fg_synth.random_fp16((B, T, h), seed=31, scale=1.5)
+    v16 = fg_synth.random_fp16((B, T, h), seed=32, scale=1.0)
+    cache, _, _ = oracle_cache_from_rows(fg, k16, v16, T, H)
+    q = dev(fg_synth.random_fp16((B, h), seed=33, scale=1.5))
+    dense = torch.empty((B, h), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_decode_attn_workspace_bytes(cache, T)
+    fg.fg_decode_attn_q4kv(q, h, cache, T, 0.1, dense,
+                           torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None)
+    top = torch.empty_like(dense)
+    ws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, T), dtype=torch.uint8,
+                     device="cuda")
+    fg.fg_decode_attn_q4kv_topk(q, h, cache, T, T, 0.1, top, ws)
+    fg.fg_check_device_error()
+    assert_close(f16(top), f16(dense).astype(np.float64), "topk k=len vs dense")
+
+
+def test_decode_attention_topk_kv_workload_sampled(fg):
+    """The KV-dominated workload's cache with the pages' top 10% (106 of 1056 positions);
+    two sequences checked against the oracle."""
+    wl = fg_synth.WORKLOADS["kv-decode"]
+    B, H, d, cap = wl.B, wl.H, wl.d, wl.cap
+    k = OL.topk_count(cap)
+    kc, vc, ka, va = fg_synth.random_q4_cache_torch(B, H, cap, d, seed=5)
+    cache = fg.KVCacheQ4.__new__(fg.KVCacheQ4)
+    cache.B, cache.cap, cache.h, cache.H, cache.d = B, cap, wl.h, H, d
+    cache.k_codes, cache.v_codes, cache.k_ab, cache.v_ab = kc, vc, ka, va
+    q16 = fg_synth.random_fp16((B, wl.h), seed=45, scale=1.5)
+    out = torch.empty((B, wl.h), dtype=torch.float16, device="cuda")
+    sel = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, cap), dtype=torch.uint8,
+                     device="cuda")
+    fg.fg_decode_attn_q4kv_topk(dev(q16), wl.h, cache, cap, k, 1.0 / math.sqrt(d), out, ws, sel)
+    fg.fg_check_device_error()
+    for b in (0, B - 1):
+        hats = []
+        for codes_t, ab_t in ((kc, ka), (vc, va)):
+            codes = cache_codes_to_rows(host(codes_t[b:b + 1]))[0]
+            abw = cache_codes_to_rows(host(ab_t[b:b + 1]))[0].view(np.uint32)
+            qq = OQ.unpack_nibbles(codes)
+            a = (abw & 0xFFFF).astype(np.uint16).view(np.float16)
+            bb = (abw >> 16).astype(np.uint16).view(np.float16)
+            hats.append(OQ.dequant_g64(qq, a, bb))
+        _topk_check(q16[b:b + 1], hats[0][None], hats[1][None], H, d, k, f16(out[b:b + 1]),
+                    host(sel[b:b + 1]), f"topk kv workload seq {b}")
+
+
 # ----------------------------------------------------------------------------- prefill attention
 
 
