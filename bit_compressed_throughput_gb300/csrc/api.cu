@@ -434,7 +434,7 @@ int fg_decode_attn_q4kv_topk(const uint16_t* q, int64_t q_stride, const fg_kvcac
   if (rc) return rc;
   if (len <= 0 || k <= 0 || k > len) return FG_ERR_SHAPE;
   if (len > kv->cap) return FG_ERR_CAPACITY;
-  if ((int64_t)(len + k) * 4 > 227 * 1024) return FG_ERR_SHAPE;
+  if ((int64_t)(len + k) * 4 + 1024 > 227 * 1024) return FG_ERR_SHAPE;
   if (q_stride < kv->h || q_stride % 8 != 0) return FG_ERR_SHAPE;
   if (!(scale > 0.0f) || !isfinite(scale)) return FG_ERR_ARG;
   if (kv->B == 0) return FG_OK;

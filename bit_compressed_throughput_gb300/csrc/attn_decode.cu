@@ -43,6 +43,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "attn_q4.cuh"
 #include "fg_common.cuh"
 #include "fg_internal.h"
 
@@ -77,30 +78,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// The four pairs (c_i, c_{i+4}) of a code word as fp16 subnormals: pairs 0 and 2 hold
-// c * 2^-24, pairs 1 and 3 hold 16c * 2^-24.
-__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {
-  const uint32_t w8 = w >> 8;
-  p[0] = w & 0x000F000Fu;
-  p[1] = w & 0x00F000F0u;
-  p[2] = w8 & 0x000F000Fu;
-  p[3] = w8 & 0x00F000F0u;
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
 
 // 2^x on the special-function unit; inputs are <= 8 (lazy rescaling) or -inf, results that
 // would be subnormal flush to zero, which only drops terms below 2^-126 of the largest.
@@ -248,49 +225,10 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
   for (int ci = first; ci < items && ok; ci += nwarps) {
     const Item it = item_of(ci, H, len, splits, tps);
 
-    // ---- q: this lane's channels j = tig*8*NW + 8w + i + 4e, permuted into B fragments
-    const uint16_t* qh = q + (int64_t)it.b * q_stride + (int64_t)it.hd * D + tig * 8 * NW;
-    uint32_t qw[NW * 4];
-#pragma unroll
-    for (int c = 0; c < NW; ++c) {
-      const uint4 u = ldg_nc_v4(qh + 8 * c);
-      qw[4 * c] = u.x; qw[4 * c + 1] = u.y; qw[4 * c + 2] = u.z; qw[4 * c + 3] = u.w;
-    }
-    auto qval = [&](int w, int i) -> uint32_t {     // fp16 bits of channel 8w+i of the chunk
-      const uint32_t word = qw[4 * w + (i >> 1)];
-      return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
-    };
-    const int my_group = (NG == 2) ? (tig >> 1) : 0;
-    // B fragments: q for pairs with factor 1, q/16 (exact) for pairs with factor 16.  Column
-    // n of B carries group n & 1 (NG == 2) or group 0 (NG == 1), so every lane's D fragment
-    // holds its rows' dot products for every group and no lane needs another's.
-    float qsum = 0.0f;
-    uint32_t bq[2 * NW][2];
-#pragma unroll
-    for (int s = 0; s < 2 * NW; ++s) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int p = 2 * s + r, w = p >> 2, i = p & 3;
-        uint32_t v = qval(w, i) | (qval(w, i + 4) << 16);
-        const float2 fq = unpack_h2(v);
-        qsum += fq.x + fq.y;
-        if (i & 1) {
-          const uint32_t k16 = 0x2C002C00u;             // half2(1/16, 1/16)
-          __half2 h = __hmul2(*reinterpret_cast<__half2*>(&v), *reinterpret_cast<const __half2*>(&k16));
-          v = *reinterpret_cast<uint32_t*>(&h);
-        }
-        bq[s][r] = (NG == 1 || (gid & 1) == my_group) ? v : 0u;
-      }
-    }
-    // sum over the lanes sharing this group: tig pairs (NG == 2) or all four (NG == 1)
-    qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
-    if (NG == 1) qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
-    // scores in base 2: the softmax scale rides on the group sums and the code scale
-    const float Q0 = __shfl_sync(0xFFFFFFFFu, qsum, lane & ~3) * scale_log2;
-    const float Q1 = (NG == 2) ? __shfl_sync(0xFFFFFFFFu, qsum, (lane & ~3) | 2) * scale_log2
-                               : 0.0f;
-    // dk holds 2^-24 * sum_j c_j q_j: the code scale (b - a)/15 takes the 2^24 back
-    const float ck = (16777216.0f / 15.0f) * scale_log2;
+    // ---- q as B fragments (permuted to the lanes' code words), group sums, code scale
+    q4attn::QFrag<D> qf;
+    q4attn::load_q_frag<D>(q + (int64_t)it.b * q_stride + (int64_t)it.hd * D, lane, scale_log2,
+                           qf);
 
     float m_run = -INFINITY;
     float l_run = 0.0f;                 // this lane's rows only; summed over gid at the end
@@ -324,28 +262,10 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           load_words<NW>(slot + row * R::ROW_CODE + tig * 4 * NW, kw[r]);
           load_words<NG>(slot + 2 * R::CODE_BYTES + row * R::ROW_AB, ka[r]);
         }
-        float dk[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          uint32_t c0[4], c1[4];                     // rows gid and gid+8
-          code_pairs(kw[0][w], c0);
-          code_pairs(kw[1][w], c1);
-          mma16816(dk, c0[0], c1[0], c0[1], c1[1], bq[2 * w][0], bq[2 * w][1]);
-          mma16816(dk, c0[2], c1[2], c0[3], c1[3], bq[2 * w + 1][0], bq[2 * w + 1][1]);
-        }
-        // dk[2r] (group 0) and dk[2r+1] (group 1, or group 0 again) belong to row gid + 8r
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float2 ab0 = unpack_h2(ka[r][0]);
-          float dot = (ab0.y - ab0.x) * dk[2 * r];
-          float off = ab0.x * Q0;
-          if (NG == 2) {
-            const float2 ab1 = unpack_h2(ka[r][NG - 1]);
-            dot = fmaf(ab1.y - ab1.x, dk[2 * r + 1], dot);
-            off = fmaf(ab1.x, Q1, off);
-          }
-          sc[sub][r] = valid(sub, r) ? fmaf(dot, ck, off) : -INFINITY;
-        }
+        float t_sc[2];
+        q4attn::tile_scores<D>(kw, ka, qf, t_sc);
+        sc[sub][0] = valid(sub, 0) ? t_sc[0] : -INFINITY;
+        sc[sub][1] = valid(sub, 1) ? t_sc[1] : -INFINITY;
       }
       // ---- phase 2: lazy rescaling: the reference maximum moves only when a score
       // exceeds it by more than 2^8, so p stays <= 256 and the accumulators rarely need
@@ -387,41 +307,8 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
           load_words<NW>(slot + R::CODE_BYTES + row * R::ROW_CODE + tig * 4 * NW, vw[r]);
           load_words<NG>(slot + 2 * R::CODE_BYTES + R::AB_BYTES + row * R::ROW_AB, va[r]);
         }
-        uint32_t wrow[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float pr = p[sub][r];
-          const float p15 = pr * (1.0f / 15.0f);
-          // rows past the end take (a, b) = (0, 0): their bytes contribute exact zeros
-          const float2 ab0 = unpack_h2(valid(sub, r) ? va[r][0] : 0u);
-          const float w0 = p15 * (ab0.y - ab0.x);
-          asum[0] = fmaf(pr, ab0.x, asum[0]);
-          float w1 = w0;
-          if (NG == 2) {
-            const float2 ab1 = unpack_h2(valid(sub, r) ? va[r][NG - 1] : 0u);
-            w1 = p15 * (ab1.y - ab1.x);
-            asum[NG - 1] = fmaf(pr, ab1.x, asum[NG - 1]);
-          }
-          wrow[r] = pack_h2(w0, w1);
-        }
-        // B fragment: rows t = 2tig, 2tig+1 (and +8), column n = gid carrying group n & 1
-        const uint32_t wa = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig);
-        const uint32_t wb = __shfl_sync(0xFFFFFFFFu, wrow[0], 8 * tig + 4);
-        const uint32_t wc = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig);
-        const uint32_t wd = __shfl_sync(0xFFFFFFFFu, wrow[1], 8 * tig + 4);
-        const uint32_t sel = (NG == 2 && (gid & 1)) ? 0x7632u : 0x5410u;
-        const uint32_t bv0 = __byte_perm(wa, wb, sel);
-        const uint32_t bv1 = __byte_perm(wc, wd, sel);
-        // each packed code word is transposed first (the lane gets 4 channels at two
-        // positions), then split into code pairs
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          uint32_t c0[4], c1[4];
-          code_pairs(movtrans(vw[0][w]), c0);
-          code_pairs(movtrans(vw[1][w]), c1);
-          mma16816(acc[2 * w], c0[0], c0[1], c1[0], c1[1], bv0, bv1);
-          mma16816(acc[2 * w + 1], c0[2], c0[3], c1[2], c1[3], bv0, bv1);
-        }
+        const bool vr[2] = {valid(sub, 0), valid(sub, 1)};
+        q4attn::v_tile<D>(vw, va, p[sub], vr, lane, acc, asum);
       }
     };
 
@@ -457,30 +344,13 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
     }
-    // acc[2w+h] row gid holds channel cb + 2h (factor 1, times 2^-24), row gid+8 channel
-    // cb + 2h + 1 (factor 16, times 2^-20), cb = 8*NW*(gid>>1) + 8w + 4*(gid&1); its
-    // columns 2tig / 2tig+1 hold groups 0 / 1 (the same in every tig), so lane tig writes
-    // the accumulators u with u % 4 == tig
-    const int g_lane = (NG == 2) ? (gid >> 2) : 0;      // group of every channel of row gid
-    const float A = (NG == 2 && g_lane) ? asum[NG - 1] : asum[0];
     const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-    const int cbase = 8 * NW * (gid >> 1) + 4 * (gid & 1);
     uint16_t* o = out + (int64_t)it.b * H * D + (int64_t)it.hd * D;
     float* pp = partial + (int64_t)ci * (D + 2);
-#pragma unroll
-    for (int u = 0; u < 2 * NW; ++u) {
-      if ((u & 3) != tig) continue;
-      const int ch = cbase + 8 * (u >> 1) + 2 * (u & 1);
-      const float vx = (g_lane ? acc[u][1] : acc[u][0]) * 16777216.0f + A;
-      const float vy = (g_lane ? acc[u][3] : acc[u][2]) * 1048576.0f + A;
-      if (splits == 1) {
-        o[ch] = f2h(vx * inv_l);
-        o[ch + 1] = f2h(vy * inv_l);
-      } else {
-        pp[ch] = vx;
-        pp[ch + 1] = vy;
-      }
-    }
+    if (splits == 1)
+      q4attn::v_channels<D>(acc, asum, lane, [&](int ch, float v) { o[ch] = f2h(v * inv_l); });
+    else
+      q4attn::v_channels<D>(acc, asum, lane, [&](int ch, float v) { pp[ch] = v; });
     if (splits > 1 && lane == 0) {
       pp[D] = m_run;
       pp[D + 1] = l;

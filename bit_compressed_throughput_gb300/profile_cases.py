@@ -30,12 +30,14 @@ def gemm_case(M, K, N, epi, reps):
     Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     wsb = fg.fg_gemm_workspace_bytes(M, K, N)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    tws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, length), dtype=torch.uint8,
+                      device="cuda") if topk else None
     for _ in range(1 + reps):
         fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
     fg.fg_check_device_error()
 
 
-def attn_case(B, H, d, length, reps):
+def attn_case(B, H, d, length, reps, topk=0):
     import torch
     import fg_synth
     from bit_compressed_throughput_gb300 import fg
@@ -48,8 +50,14 @@ def attn_case(B, H, d, length, reps):
     out = torch.empty_like(q)
     wsb = fg.fg_decode_attn_workspace_bytes(cache, length)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    tws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, length), dtype=torch.uint8,
+                      device="cuda") if topk else None
     for _ in range(1 + reps):
-        fg.fg_decode_attn_q4kv(q, H * d, cache, length, 1.0 / math.sqrt(d), out, ws)
+        if topk:
+            fg.fg_decode_attn_q4kv_topk(q, H * d, cache, length, topk, 1.0 / math.sqrt(d), out,
+                                        tws)
+        else:
+            fg.fg_decode_attn_q4kv(q, H * d, cache, length, 1.0 / math.sqrt(d), out, ws)
     torch.cuda.synchronize()
 
 
@@ -66,6 +74,8 @@ CASES = {
     "decode-attn-kv": lambda r: attn_case(512, 56, 128, 1056, r),
     # a quarter of it (128 sequences, 1.1 GB of cache): the same per-warp work, capture-sized
     "decode-attn-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r),
+    # top-K sparse attention on the quarter KV workload: the top 10% (106 of 1056 positions)
+    "decode-attn-topk-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r, topk=106),
 }
 
 

@@ -185,7 +185,7 @@ int fg_decode_attn_q4kv_static(const uint16_t* q, int64_t q_stride, const fg_kvc
  * positions with the highest scores contribute their values:
  *   out[b][hd*d + j] = sum_{t in top-k(b,hd)} p_t V^_b,hd,t,j   (no renormalisation)
  * with equal scores at the k-th place going to the lower position.  1 <= k <= len <= cap,
- * d in {64, 128}, (len + k) * 4 bytes <= 227 KB.  q, out as fg_decode_attn_q4kv.  sel
+ * d in {64, 128}, (len + k) * 4 + 1024 bytes <= 227 KB.  q, out as fg_decode_attn_q4kv.  sel
  * (nullable): device int32 [B][H][k] receiving the selected positions in increasing
  * position order.  ws: device scratch of at least fg_decode_attn_topk_workspace_bytes(kv,
  * len) bytes (the scores).
