@@ -190,17 +190,37 @@ fg_kvcache kv_slice(const fg_kvcache& kv, int b0, int nb) {
   return s;
 }
 
+// The K/V append of rows b*T + t (positions pos + t) into `kv`.
+KvOut kv_out(const fg_kvcache& kv, int T, int pos) {
+  KvOut o;
+  o.k_codes = kv.k_codes;
+  o.v_codes = kv.v_codes;
+  o.k_ab = reinterpret_cast<uint32_t*>(kv.k_ab);
+  o.v_ab = reinterpret_cast<uint32_t*>(kv.v_ab);
+  o.h = kv.h;
+  o.H = kv.H;
+  o.d = kv.h / kv.H;
+  o.cap = kv.cap;
+  o.T = T;
+  o.pos = pos;
+  return o;
+}
+
 // ---------------------------------------------------------------- timed launches
+// kv: the QKV projection's K/V append in the GEMM epilogue (null: none).
 int run_gemm(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bias, int epi,
-             const uint16_t* residual, uint16_t* Y, void* ws, int sms, cudaStream_t st) {
+             const uint16_t* residual, uint16_t* Y, void* ws, int sms, cudaStream_t st,
+             const KvOut* kv = nullptr) {
   const GemmPlan p = gemm_plan(M, W.K, W.N, sms);
   Span sp(st);
   cudaEvent_t mid = (p.splits > 1) ? sp.mid_event() : nullptr;
-  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid);
+  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, kv);
   if (e != cudaSuccess) return set_cuda_error(e);
   const bool stream = (p.kind == kGemmStream);
   const int kind = stream ? FG_K_GEMM_STREAM : FG_K_GEMM;
-  const double w = stream ? work_gemm_stream(M, W.N, W.K) : work_gemm(M, W.N, W.K);
+  // the streaming kernel's work is bytes: with the append, also the 4-bit K/V written
+  const double w = stream ? work_gemm_stream(M, W.N, W.K) + (kv ? 2.0 * M * kv->h * 0.5625 : 0.0)
+                          : work_gemm(M, W.N, W.K);
   if (p.splits > 1 && mid) {
     sp.close(kind, w, mid);
     sp.stop(FG_K_GEMM_REDUCE, work_gemm_reduce(M, W.N, p.splits));
@@ -216,6 +236,36 @@ int run_layernorm(const uint16_t* x, int64_t rows, int h, const uint16_t* g, con
   cudaError_t e = launch_layernorm(x, rows, h, g, b, eps, y, st);
   if (e != cudaSuccess) return set_cuda_error(e);
   sp.stop(FG_K_LAYERNORM, work_layernorm(rows, h));
+  return FG_OK;
+}
+
+// GEMM whose output rows also go through LayerNorm (y_ln = LN(Y)): with a split-K plan
+// the reduce kernel does both (one launch after the GEMM); otherwise the GEMM, then the
+// LayerNorm kernel.
+int run_gemm_ln(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bias, int epi,
+                const uint16_t* residual, uint16_t* Y, const uint16_t* g, const uint16_t* b,
+                float eps, uint16_t* y_ln, void* ws, int sms, cudaStream_t st) {
+  const GemmPlan p = gemm_plan(M, W.K, W.N, sms);
+  if (p.splits == 1) {
+    int rc = run_gemm(X, M, W, bias, epi, residual, Y, ws, sms, st);
+    if (rc) return rc;
+    return run_layernorm(Y, M, (int)W.N, g, b, eps, y_ln, st);
+  }
+  Span sp(st);
+  cudaEvent_t mid = sp.mid_event();
+  const LnOut ln{g, b, eps, y_ln};
+  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, nullptr, &ln);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  const bool stream = (p.kind == kGemmStream);
+  const int kind = stream ? FG_K_GEMM_STREAM : FG_K_GEMM;
+  const double w = stream ? work_gemm_stream(M, W.N, W.K) : work_gemm(M, W.N, W.K);
+  if (mid) {
+    sp.close(kind, w, mid);
+    // the reduce reads the partials and writes Y (its work), then writes LN(Y)
+    sp.stop(FG_K_GEMM_REDUCE, work_gemm_reduce(M, W.N, p.splits) + 2.0 * M * W.N);
+  } else {
+    sp.stop(kind, w);
+  }
   return FG_OK;
 }
 
@@ -384,6 +434,50 @@ int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const ui
                   static_cast<cudaStream_t>(stream));
 }
 
+int fg_dequant_gemm_q4_kv(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
+                          uint16_t* Y, const fg_kvcache* kv, int32_t T, int32_t pos, void* ws,
+                          size_t ws_bytes, void* stream) {
+  int rc = check_q4mat(W);
+  if (rc) return rc;
+  if ((rc = check_kv(kv))) return rc;
+  // Y = [Q | K | V]: three h-wide column blocks, each a whole number of 128-channel tiles
+  if (W->N != 3 * (int64_t)kv->h || kv->h % 128 != 0) return FG_ERR_SHAPE;
+  if (T <= 0 || pos < 0 || M != (int64_t)kv->B * T || M > (1ll << 31) - 1) return FG_ERR_SHAPE;
+  if ((int64_t)pos + T > kv->cap) return FG_ERR_CAPACITY;
+  if (M == 0) return FG_OK;
+  if (!X || !Y || !aligned16(X) || !aligned16(Y) || (bias && !aligned16(bias))) return FG_ERR_ARG;
+  const size_t need = fg_gemm_workspace_bytes(M, W->K, W->N);
+  if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return FG_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  const KvOut ko = kv_out(*kv, T, pos);
+  return run_gemm(X, M, *W, bias, FG_EPI_NONE, nullptr, Y, ws, sms,
+                  static_cast<cudaStream_t>(stream), &ko);
+}
+
+int fg_dequant_gemm_q4_ln(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
+                          int epilogue, const uint16_t* residual, uint16_t* Y,
+                          const uint16_t* ln_gamma, const uint16_t* ln_beta, float ln_eps,
+                          uint16_t* Y_ln, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_q4mat(W);
+  if (rc) return rc;
+  if (M < 0 || M > (1ll << 31) - 1 || W->N > 16384) return FG_ERR_SHAPE;
+  if (epilogue < FG_EPI_NONE || epilogue > FG_EPI_RESIDUAL || !(ln_eps > 0.0f)) return FG_ERR_ARG;
+  if (M == 0) return FG_OK;
+  if (!X || !Y || !Y_ln || !ln_gamma || !ln_beta || Y_ln == Y ||
+      (epilogue == FG_EPI_RESIDUAL && !residual))
+    return FG_ERR_ARG;
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(Y_ln) || !aligned16(ln_gamma) ||
+      !aligned16(ln_beta) || (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
+    return FG_ERR_ARG;
+  const size_t need = fg_gemm_workspace_bytes(M, W->K, W->N);
+  if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return FG_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  return run_gemm_ln(X, M, *W, bias, epilogue, residual, Y, ln_gamma, ln_beta, ln_eps, Y_ln, ws,
+                     sms, static_cast<cudaStream_t>(stream));
+}
+
 int fg_kv_append_q4(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride, int32_t T,
                     int32_t pos, const fg_kvcache* kv, void* stream) {
   int rc = check_kv(kv);
@@ -537,16 +631,20 @@ int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const
     uint16_t* yk = y + (int64_t)k * M * h;
     const fg_kvcache kvk = kv_slice(*kv, k * g, g);
     if ((rc = run_layernorm(xk, M, h, L->ln1_g, L->ln1_b, dm->ln_eps, ln, st))) return rc;
-    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st)))
+    // QKV projection; its epilogue appends the 4-bit K/V of positions 0 .. s-1
+    const KvOut ko = kv_out(kvk, s, 0);
+    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st, &ko)))
       return rc;
-    if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, s, 0, kvk, st))) return rc;
     if ((rc = run_prefill_attn(qkv, g, s, dm->H, dm->d, scale, att, st))) return rc;
-    uint16_t* o_dst = (dm->f > 0) ? h1 : yk;
-    if ((rc = run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, o_dst, gws, sms, st))) return rc;
     if (dm->f > 0) {
-      if ((rc = run_layernorm(h1, M, h, L->ln2_g, L->ln2_b, dm->ln_eps, ln, st))) return rc;
+      // O projection + residual into h1, then LN2(h1) (fused into a split-K reduce)
+      if ((rc = run_gemm_ln(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, h1, L->ln2_g, L->ln2_b,
+                            dm->ln_eps, ln, gws, sms, st)))
+        return rc;
       if ((rc = run_gemm(ln, M, L->w1, L->b1, FG_EPI_RELU, nullptr, mid, gws, sms, st))) return rc;
       if ((rc = run_gemm(mid, M, L->w2, L->b2, FG_EPI_RESIDUAL, h1, yk, gws, sms, st))) return rc;
+    } else if ((rc = run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, yk, gws, sms, st))) {
+      return rc;
     }
   }
   return FG_OK;
@@ -578,17 +676,18 @@ int fg_layer_decode(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const 
   const int h = dm->h;
   const float scale = 1.0f / sqrtf((float)dm->d);
   if ((rc = run_layernorm(x, M, h, L->ln1_g, L->ln1_b, dm->ln_eps, ln, st))) return rc;
-  if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st))) return rc;
-  if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, 1, pos, *kv, st))) return rc;
+  // QKV projection; its epilogue appends the new token's 4-bit K/V at position pos
+  const KvOut ko = kv_out(*kv, 1, pos);
+  if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st, &ko)))
+    return rc;
   if ((rc = run_decode_attn(qkv, 3 * h, *kv, pos + 1, scale, att, aws, sms, st))) return rc;
-  uint16_t* o_dst = (dm->f > 0) ? h1 : y;
-  if ((rc = run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, x, o_dst, gws, sms, st))) return rc;
-  if (dm->f > 0) {
-    if ((rc = run_layernorm(h1, M, h, L->ln2_g, L->ln2_b, dm->ln_eps, ln, st))) return rc;
-    if ((rc = run_gemm(ln, M, L->w1, L->b1, FG_EPI_RELU, nullptr, mid, gws, sms, st))) return rc;
-    if ((rc = run_gemm(mid, M, L->w2, L->b2, FG_EPI_RESIDUAL, h1, y, gws, sms, st))) return rc;
-  }
-  return FG_OK;
+  if (dm->f == 0) return run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, x, y, gws, sms, st);
+  // O projection + residual into h1, then LN2(h1) (fused into the split-K reduce)
+  if ((rc = run_gemm_ln(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, x, h1, L->ln2_g, L->ln2_b,
+                        dm->ln_eps, ln, gws, sms, st)))
+    return rc;
+  if ((rc = run_gemm(ln, M, L->w1, L->b1, FG_EPI_RELU, nullptr, mid, gws, sms, st))) return rc;
+  return run_gemm(mid, M, L->w2, L->b2, FG_EPI_RESIDUAL, h1, y, gws, sms, st);
 }
 
 // ---------------------------------------------------------------- profiling ABI

@@ -56,6 +56,61 @@ __device__ __forceinline__ uint32_t q4_code_rcp(float xf, float af, float bma, f
   return (uint32_t)q;
 }
 
+// ---- one quantisation group of 64 fp16 values, held 8 per thread (or 1 per thread)
+// Order keys of the two fp16 values of a word, one per 16-bit lane (order_key on each).
+__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;
+  return w ^ (0x80008000u | (neg * 0x7FFFu));
+}
+// Min/max word of 8 fp16 values (four words): min key | (~max key) << 16.  Words of the
+// parts of a group merge with __vminu2 (a 16-bit SIMD min of both halves).
+__device__ __forceinline__ uint32_t q4_minmax8(const uint32_t (&w)[4]) {
+  uint32_t kmin2 = order_keys2(w[0]), kmax2 = kmin2;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    const uint32_t k2 = order_keys2(w[i]);
+    kmin2 = __vminu2(kmin2, k2);
+    kmax2 = __vmaxu2(kmax2, k2);
+  }
+  const uint32_t kmin = min(kmin2 & 0xFFFFu, kmin2 >> 16);
+  const uint32_t kmax = max(kmax2 & 0xFFFFu, kmax2 >> 16);
+  return kmin | ((~kmax & 0xFFFFu) << 16);
+}
+// Min/max word of one fp16 value.
+__device__ __forceinline__ uint32_t q4_minmax1(uint16_t u) {
+  const uint32_t k = order_key(u);
+  return k | ((~k & 0xFFFFu) << 16);
+}
+// The group's statistics word (a | b << 16, fp16 bits) from its merged min/max word.
+__device__ __forceinline__ uint32_t q4_ab_word(uint32_t mm) {
+  return key_to_bits(mm & 0xFFFFu) | (key_to_bits(~(mm >> 16) & 0xFFFFu) << 16);
+}
+// The per-group constants of the code formula: a, b - a and fl(15 * fl(1 / (b - a))).
+struct Q4Group {
+  float af, bma, c15;
+};
+__device__ __forceinline__ Q4Group q4_group(uint32_t abw) {
+  Q4Group g;
+  g.af = h2f((uint16_t)(abw & 0xFFFFu));
+  g.bma = __fsub_rn(h2f((uint16_t)(abw >> 16)), g.af);
+  g.c15 = __fmul_rn(15.0f, __frcp_rn(g.bma));
+  return g;
+}
+
+// Packed codes of 8 fp16 values against their group: element 2i in the low nibble, 2i+1
+// in the high nibble of byte i.
+__device__ __forceinline__ uint32_t q4_codes8(const uint32_t (&w)[4], const Q4Group& g) {
+  uint32_t codes = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x2 = unpack_h2(w[i]);
+    const uint32_t c0 = q4_code_rcp(x2.x, g.af, g.bma, g.c15);
+    const uint32_t c1 = q4_code_rcp(x2.y, g.af, g.bma, g.c15);
+    codes |= (c0 | (c1 << 4)) << (8 * i);
+  }
+  return codes;
+}
+
 // Programmatic dependent launch: every library kernel lets the next kernel of the stream
 // launch at once and waits for its predecessor's results (and for its predecessor to have
 // finished reading what this kernel overwrites) before touching global data, so launch and

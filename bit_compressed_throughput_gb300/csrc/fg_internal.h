@@ -78,10 +78,35 @@ struct GemmPlan {
   int grid;        // persistent CTAs: min(units, SMs)
   size_t ws_bytes;
 };
+// K/V append of the QKV projection: columns [h, 2h) of Y are K and [2h, 3h) are V; row
+// r = b*T + t of the GEMM is position pos + t of sequence b.  Each 64-channel group of a
+// K or V row is quantised from its fp16 output values (the values Y holds) and written to
+// the head-major cache: codes at ((b*H + head)*cap + pos + t)*(d/2) + c/2, the (a, b) word
+// at that slot times d/64 plus c/64 (c = the channel within the head).  k_codes == null:
+// no append.
+struct KvOut {
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  uint32_t* k_ab;
+  uint32_t* v_ab;
+  int h, H, d, cap, T, pos;
+};
+
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms);
+// LayerNorm of the GEMM's output rows, fused into the split-K reduce: y = LN(Y) with
+// (gamma, beta, eps), N <= 16384.
+struct LnOut {
+  const uint16_t* gamma;
+  const uint16_t* beta;
+  float eps;
+  uint16_t* y;
+};
+// kv: K/V append in the epilogue (null or k_codes == null: none).  ln: LayerNorm in the
+// split-K reduce (only for a split plan; null: none).
 cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
-                        void* ws, cudaStream_t st, cudaEvent_t mid_event);
+                        void* ws, cudaStream_t st, cudaEvent_t mid_event,
+                        const KvOut* kv = nullptr, const LnOut* ln = nullptr);
 // Device error words of the bounded waits (GEMM, decode attention): read-and-clear.
 cudaError_t gemm_read_error(unsigned int* out);
 cudaError_t gemm_stream_read_error(unsigned int* out);

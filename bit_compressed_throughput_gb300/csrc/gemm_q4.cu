@@ -82,10 +82,11 @@ constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
 constexpr int CS_BYTES = C_BYTES + S_BYTES; // one code stage
 constexpr int SMEM_BYTES = 232448;          // the whole per-CTA budget
-constexpr int BAR_BYTES = 512;
+constexpr int BAR_BYTES = 512 + 1024;       // barriers, then the epilogue's exchange words
+constexpr int XCH_OFF = 512;
 constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * TN_MAX;  // two accumulator buffers
-static_assert((2 * RA_MAX + 2 * RC_MAX + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
+static_assert((2 * RA_MAX + 2 * RC_MAX + 5) * 8 + 8 <= XCH_OFF, "barrier space");
 static_assert(TMEM_COLS == 512, "TMEM budget");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
 static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
@@ -143,9 +144,10 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// Bias / ReLU / residual on 8 consecutive outputs and the fp16 store (reduce kernel).
-__device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int64_t row, int n,
-                                          int N) {
+// Bias / ReLU / residual on 8 consecutive outputs and the fp16 store (reduce kernel);
+// returns the stored fp16 words.
+__device__ __forceinline__ uint4 epilogue8(const EpiArgs& ea, float (&v)[8], int64_t row, int n,
+                                           int N) {
   if (ea.bias) {
     const uint4 bu = ldg_nc_v4(ea.bias + n);
     const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
@@ -175,6 +177,7 @@ __device__ __forceinline__ void epilogue8(const EpiArgs& ea, float (&v)[8], int6
   o.z = pack_h2(v[4], v[5]);
   o.w = pack_h2(v[6], v[7]);
   *reinterpret_cast<uint4*>(ea.Y + row * N + n) = o;
+  return o;
 }
 
 struct Unit {
@@ -230,8 +233,10 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   // be rewritten and its X slot refilled.  The X producer issues k-block it after the MMAs
   // of k-block it - RX, hence after those of it - R, so its arrival always lands in k-block
   // it's phase of full(it % R).
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RA_MAX + 2 * RC_MAX + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RA_MAX + 2 * RC_MAX + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // K/V append: per-token min/max words of the four epilogue warps, two buffers
+  uint32_t* xch = reinterpret_cast<uint32_t*>(smem + POOL_BYTES + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -241,6 +246,7 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   auto free_c = [&](int c) { return bar0 + 8u * (2 * RA_MAX + RC_MAX + c); };
   auto acc_full = [&](int a) { return bar0 + 8u * (2 * RA_MAX + 2 * RC_MAX + a); };
   auto acc_empty = [&](int a) { return bar0 + 8u * (2 * RA_MAX + 2 * RC_MAX + 2 + a); };
+  const uint32_t xchg = bar0 + 8u * (2 * RA_MAX + 2 * RC_MAX + 4);
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < R; ++r) {
@@ -255,6 +261,7 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       mbar_init(acc_full(a), ka.ni);               // one commit per MMA issuer
       mbar_init(acc_empty(a), 4);                  // one arrival per epilogue warp
     }
+    mbar_init(xchg, 4);                            // one arrival per epilogue warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -480,7 +487,10 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int ch_in_tile = (L & ~7) + ((L & 7) >> 1) + ((L & 1) << 2);
     const int64_t N = ka.N;
     const bool add_res = !ea.partial && ea.epi == FG_EPI_RESIDUAL;
+    const int q = warp & 3;                           // TMEM lane quarter
     int tl = 0;
+    uint32_t xph = 0;                                 // K/V exchanges so far
+    bool fail = false;
     for (int u = blockIdx.x; u < ka.units; u += gridDim.x, ++tl) {
       const Unit w = unit_coords(u, tn, ka.tiles_t, ka.tiles_c, ka.kblocks, ka.kb_per_split);
       const int acc = tl & 1;
@@ -499,6 +509,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // first channel of this lane's 8-lane group (channels in natural order after the
       // transpose)
       const int64_t chb = w.c0 + lane_base + (lane & ~7);
+      // a K or V tile of the QKV projection (h is a multiple of 128: no tile straddles)
+      const bool kv_tile = ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
       for (int cb = 0; cb < ntok; cb += 32) {
         // columns past tn (at most cb + 31 <= 255) stay inside this accumulator's 256
         uint32_t r[32];
@@ -542,6 +554,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         // per 8-token block: transpose so this lane holds token 8j + (lane & 7) for the
         // group's 8 channels, undo the restore order (positions 0..7 hold channels
         // 0,4,1,5,2,6,3,7), add the residual row segment and store 16 bytes
+        uint4 ov[4];                                  // the stored fp16 outputs
+        uint32_t mmv[4];                              // their min/max over the warp's channels
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t u[4] = {hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]};
@@ -563,8 +577,43 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             }
             *reinterpret_cast<uint4*>(ea.Y + t * N + chb) = o;
           }
+          ov[j] = o;
+          if (kv_tile) {
+            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+            uint32_t mm = q4_minmax8(ow);
+            mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, 8));
+            mmv[j] = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, 16));
+          }
+        }
+        if (!kv_tile) continue;
+        // ---- K/V append.  A 64-channel group is two lane quarters (q, q ^ 1): lanes 0..7
+        // publish the quarter's min/max of tokens 8j + lane, then read the partner's
+        uint32_t* xb = xch + (xph & 1) * 128;
+        if (lane < 8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) xb[32 * q + 8 * j + lane] = mmv[j];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xchg);
+        if (!mbar_wait(xchg, xph & 1, abort_flag)) {
+          fail = true;
+          break;
+        }
+        ++xph;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tt = cb + 8 * j + (lane & 7);
+          const uint32_t abw = q4_ab_word(__vminu2(mmv[j], xb[32 * (q ^ 1) + 8 * j + (lane & 7)]));
+          const uint32_t ow[4] = {ov[j].x, ov[j].y, ov[j].z, ov[j].w};
+          const uint32_t cw = q4_codes8(ow, q4_group(abw));
+          if (tt < ntok) {
+            const KvDst dst = kv_dst(ea.kv, w.t0 + tt, chb);
+            *reinterpret_cast<uint32_t*>(dst.codes) = cw;
+            if ((chb & 63) == 0) *dst.ab = abw;
+          }
         }
       }
+      if (fail) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(acc));
@@ -580,24 +629,124 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   }
 }
 
-// Sum the split-K partials and apply bias / ReLU / residual: 8 outputs per thread.
+// Sum the split-K partials and apply bias / ReLU / residual: 8 outputs per thread.  With
+// a K/V append the 8 threads of a lane segment hold one 64-channel group of a row (N and
+// the chunk count are multiples of 64 and 8), quantised as the standalone quantiser does.
 __global__ void __launch_bounds__(256)
 gemm_reduce_kernel(const float* __restrict__ partial, int splits, int64_t M, int N, EpiArgs ea) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const int64_t chunks = M * (N / 8);
-  if (idx >= chunks) return;
-  const int64_t row = idx / (N / 8);
-  const int n = (int)(idx - row * (N / 8)) * 8;
-  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < splits; ++s) {
-    const float4* pp = reinterpret_cast<const float4*>(partial + ((int64_t)s * M + row) * N + n);
-    const float4 x = pp[0], y = pp[1];
-    v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
-    v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+  const bool live = idx < chunks;               // whole lane segments are live or not
+  const int64_t row = live ? idx / (N / 8) : 0;
+  const int n = live ? (int)(idx - row * (N / 8)) * 8 : 0;
+  uint4 o = make_uint4(0, 0, 0, 0);
+  if (live) {
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+      const float4* pp = reinterpret_cast<const float4*>(partial + ((int64_t)s * M + row) * N + n);
+      const float4 x = pp[0], y = pp[1];
+      v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+    }
+    o = epilogue8(ea, v, row, n, N);
   }
-  epilogue8(ea, v, row, n, N);
+  if (ea.kv.k_codes == nullptr || !__any_sync(0xFFFFFFFFu, live && n >= ea.kv.h)) return;
+  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+  uint32_t mm = q4_minmax8(w);
+#pragma unroll
+  for (int k = 1; k < 8; k <<= 1) mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, k));
+  if (live && n >= ea.kv.h) {
+    const uint32_t abw = q4_ab_word(mm);
+    const KvDst dst = kv_dst(ea.kv, row, n);
+    *reinterpret_cast<uint32_t*>(dst.codes) = q4_codes8(w, q4_group(abw));
+    if ((n & 63) == 0) *dst.ab = abw;
+  }
+}
+
+// One CTA per output row: the split-K sum and the epilogue as gemm_reduce_kernel (the row
+// stored to Y), then the pre-LN LayerNorm of the stored fp16 row into y_ln with the
+// statistics of the standalone LayerNorm: fp32 mean, then the mean squared deviation (a
+// population variance), rsqrt(var + eps), (x - mean) * rstd * gamma + beta.  A thread keeps
+// at most 8 chunks of 8 values in registers (N <= 16384).
+constexpr int kLnChunks = 8;
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();                                  // red is free (a previous sum was read)
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) s += red[w];
+  return s;
+}
+
+__global__ void __launch_bounds__(256)
+gemm_reduce_ln_kernel(const float* __restrict__ partial, int splits, int64_t M, int N, EpiArgs ea,
+                      const uint16_t* __restrict__ gamma, const uint16_t* __restrict__ beta,
+                      float eps, uint16_t* __restrict__ y_ln) {
+  __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  const int nchunk = N / 8;
+  uint4 yv[kLnChunks];
+  float s = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kLnChunks; ++c) {
+    const int ci = threadIdx.x + 256 * c;
+    yv[c] = make_uint4(0, 0, 0, 0);
+    if (ci < nchunk) {
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int sp = 0; sp < splits; ++sp) {
+        const float4* pp =
+            reinterpret_cast<const float4*>(partial + ((int64_t)sp * M + row) * N + ci * 8);
+        const float4 x = pp[0], y = pp[1];
+        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+        v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+      }
+      yv[c] = epilogue8(ea, v, row, ci * 8, N);
+      const uint32_t w[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_h2(w[i]);
+        s += f.x + f.y;
+      }
+    }
+  }
+  const float mean = block_sum256(s, red) / (float)N;
+  float q = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kLnChunks; ++c) {
+    if (threadIdx.x + 256 * c < nchunk) {
+      const uint32_t w[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_h2(w[i]);
+        const float d0 = f.x - mean, d1 = f.y - mean;
+        q += d0 * d0 + d1 * d1;
+      }
+    }
+  }
+  const float rstd = rsqrtf(block_sum256(q, red) / (float)N + eps);
+#pragma unroll
+  for (int c = 0; c < kLnChunks; ++c) {
+    const int ci = threadIdx.x + 256 * c;
+    if (ci < nchunk) {
+      const uint4 gu = ldg_nc_v4(gamma + ci * 8), bu = ldg_nc_v4(beta + ci * 8);
+      const uint32_t w[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
+      const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w}, bw[4] = {bu.x, bu.y, bu.z, bu.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_h2(w[i]), g2 = unpack_h2(gw[i]), b2 = unpack_h2(bw[i]);
+        o[i] = pack_h2((f.x - mean) * rstd * g2.x + b2.x, (f.y - mean) * rstd * g2.y + b2.y);
+      }
+      reinterpret_cast<uint4*>(y_ln + row * N)[ci] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 }  // namespace
@@ -696,10 +845,26 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
   return p;
 }
 
+// The split-K reduce: 8 outputs per thread, or with a LayerNorm one row per CTA.
+static cudaError_t launch_reduce(const GemmPlan& p, void* ws, const EpiArgs& ea, const LnOut* ln,
+                                 cudaStream_t st) {
+  const float* part = static_cast<const float*>(ws);
+  if (ln) {
+    if (p.N > 256 * 8 * kLnChunks || p.M > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    return launch_pdl(gemm_reduce_ln_kernel, dim3((unsigned)p.M), dim3(256), 0, st, part, p.splits,
+                      p.M, (int)p.N, ea, ln->gamma, ln->beta, ln->eps, ln->y);
+  }
+  const int64_t chunks = p.M * (p.N / 8);
+  return launch_pdl(gemm_reduce_kernel, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, st,
+                    part, p.splits, p.M, (int)p.N, ea);
+}
+
 cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
-                        void* ws, cudaStream_t st, cudaEvent_t mid_event) {
+                        void* ws, cudaStream_t st, cudaEvent_t mid_event, const KvOut* kv,
+                        const LnOut* ln) {
   if (p.M == 0) return cudaSuccess;
+  if (ln && p.splits == 1) return cudaErrorInvalidValue;     // the caller runs LayerNorm
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   static cudaError_t attr_err = cudaFuncSetAttribute(
@@ -715,16 +880,14 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   e = make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT32, W.ab, (uint64_t)(p.N / 64),
                   (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  const EpiArgs final_ea{bias, residual, Y, nullptr, epi};
+  const EpiArgs final_ea{bias, residual, Y, nullptr, epi, kv ? *kv : KvOut{}};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
   if (p.kind == kGemmStream) {
     e = launch_gemm_stream(p, W, tmX, ea, st);
     if (e != cudaSuccess || p.splits == 1) return e;
     if (mid_event) cudaEventRecord(mid_event, st);
-    const int64_t chunks = p.M * (p.N / 8);
-    return launch_pdl(gemm_reduce_kernel, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0,
-                      st, static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
+    return launch_reduce(p, ws, final_ea, ln, st);
   }
   // ring depths: large token tiles (prefill) pair each restored slot with an X slot (4 + 4,
   // 6 code stages); small ones (decode) keep 6 X slots (L2 latency of the X tile) and spend
@@ -758,9 +921,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                  tmS, ka, ea);
   if (e != cudaSuccess || p.splits == 1) return e;
   if (mid_event) cudaEventRecord(mid_event, st);
-  const int64_t chunks = p.M * (p.N / 8);
-  return launch_pdl(gemm_reduce_kernel, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, st,
-                    static_cast<const float*>(ws), p.splits, p.M, (int)p.N, final_ea);
+  return launch_reduce(p, ws, final_ea, ln, st);
 }
 
 cudaError_t gemm_read_error(unsigned int* out) {

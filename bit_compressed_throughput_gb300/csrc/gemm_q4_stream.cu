@@ -80,12 +80,13 @@ constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes per k-block (64-byt
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
 constexpr int CS_BYTES = SK * (C_BYTES + S_BYTES);  // one code stage: codes, then statistics
 constexpr int SMEM_BYTES = 232448;
-constexpr int BAR_BYTES = 640;
+constexpr int BAR_BYTES = 640 + 1024;      // barriers, then the epilogue's exchange words
+constexpr int XCH_OFF = 640;
 constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL0 = ACC_COLS;       // A ring after the accumulators
 static_assert(A_COL0 + RA * (BK / 2) == TMEM_COLS, "TMEM budget");
-static_assert((2 * RC_MAX + 2 * RA + 4) * 8 + 8 <= BAR_BYTES, "barrier space");
+static_assert((2 * RC_MAX + 2 * RA + 5) * 8 + 8 <= XCH_OFF, "barrier space");
 static_assert(CS_BYTES % 1024 == 0 && (SK * C_BYTES) % 512 == 0, "stage alignment");
 static_assert(SK % RPAR == 0, "restore warps take every RPAR-th position of a stage");
 constexpr long long kWaitCycles = 1ll << 32;
@@ -173,8 +174,10 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
   uint8_t* sX = smem;                                  // RX x XB
   uint8_t* sC = sX + RX * XB;                          // RC x (codes, statistics)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sC + RC * CS_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RC_MAX + 2 * RA + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RC_MAX + 2 * RA + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // K/V append: per-token min/max words of the four lane quarters, two buffers
+  uint32_t* xch = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -184,6 +187,7 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
   auto mma_done = [&](int s) { return bar0 + 8u * (2 * RC_MAX + RA + s); };
   auto acc_full = [&](int s) { return bar0 + 8u * (2 * RC_MAX + 2 * RA + s); };
   auto acc_empty = [&](int s) { return bar0 + 8u * (2 * RC_MAX + 2 * RA + 2 + s); };
+  const uint32_t xchg = bar0 + 8u * (2 * RC_MAX + 2 * RA + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RC; ++s) {
@@ -198,6 +202,7 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
       mbar_init(acc_full(s), NI);                // one commit per MMA issuer
       mbar_init(acc_empty(s), 4);                // one arrival per epilogue warp
     }
+    mbar_init(xchg, 4);                          // one arrival per epilogue warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -415,6 +420,8 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
     const int64_t N = ka.N;
     const int M = ka.M;
     int tl = 0, it = 0;
+    uint32_t xph = 0;                                 // K/V exchanges so far
+    bool fail = false;
     for (int u = blockIdx.x; u < ka.units; u += gridDim.x, ++tl) {
       const SUnit w = stream_unit(u, ka);
       const int b = tl % ka.nbuf, use = tl / ka.nbuf;
@@ -426,6 +433,8 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
       const int L = w.kb_end - w.kb_begin;
       const int64_t ch = w.c0 + ch_in_tile;
       const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;
+      // a K or V tile of the QKV projection (h is a multiple of 128: no tile straddles)
+      const bool kv_tile = ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
       for (int cb = 0; cb < M; cb += 32) {
         float v[32];
 #pragma unroll
@@ -449,16 +458,60 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
             if (cb + i < M) pp[(int64_t)i * N] = v[i];
           continue;
         }
+        uint32_t yp[16];                              // the stored fp16 outputs, in pairs
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float y = v[i] + bias_f;
+          if (ea.epi == FG_EPI_RELU) y = fmaxf(y, 0.0f);
+          else if (ea.epi == FG_EPI_RESIDUAL && cb + i < M) y += h2f(ea.residual[(cb + i) * N + ch]);
+          const uint32_t yh = f2h(y);
+          yp[i >> 1] = (i & 1) ? (yp[i >> 1] | (yh << 16)) : yh;
+          if (cb + i < M) ea.Y[(int64_t)(cb + i) * N + ch] = (uint16_t)yh;
+        }
+        if (!kv_tile) continue;
+        // ---- K/V append.  A 64-channel group is two lane quarters (q, q ^ 1): the min/max
+        // of token i over this quarter's 32 channels goes to lane i, then to the partner
+        // through shared memory
+        uint32_t my = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t k = order_key((yp[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+          const uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, k);
+          const uint32_t kmaxn = __reduce_min_sync(0xFFFFFFFFu, ~k & 0xFFFFu);
+          if (lane == i) my = kmin | (kmaxn << 16);
+        }
+        uint32_t* xb = xch + (xph & 1) * 128;
+        xb[32 * q + lane] = my;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xchg);
+        if (!swait(xchg, xph & 1, abort_flag)) {
+          fail = true;
+          break;
+        }
+        ++xph;
+        const uint32_t abw = q4_ab_word(__vminu2(my, xb[32 * (q ^ 1) + lane]));
+        const Q4Group gl = q4_group(abw);             // the group of token cb + lane
+        // lanes 0, 2, 4, 6 store the code words of channels 32q + 8j .. + 7 (j = lane / 2);
+        // this lane's channel is nibble 4 (lane & 1) + (lane >> 3) of its word
+        const int sh = 4 * (4 * (lane & 1) + (lane >> 3));
+        const int64_t n0 = w.c0 + 32 * q + 4 * (lane & 6);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (cb + i >= M) break;
-          const int64_t t = cb + i;
-          float y = v[i] + bias_f;
-          if (ea.epi == FG_EPI_RELU) y = fmaxf(y, 0.0f);
-          else if (ea.epi == FG_EPI_RESIDUAL) y += h2f(ea.residual[t * N + ch]);
-          ea.Y[t * N + ch] = f2h(y);
+          const float af = __shfl_sync(0xFFFFFFFFu, gl.af, i);
+          const float bma = __shfl_sync(0xFFFFFFFFu, gl.bma, i);
+          const float c15 = __shfl_sync(0xFFFFFFFFu, gl.c15, i);
+          const float x = h2f((uint16_t)(yp[i >> 1] >> (16 * (i & 1))));
+          uint32_t cw = q4_code_rcp(x, af, bma, c15) << sh;
+          cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 1);
+          cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 8);
+          cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 16);
+          if ((lane & 0x19) == 0)
+            *reinterpret_cast<uint32_t*>(kv_dst(ea.kv, cb + i, n0).codes) = cw;
         }
+        if ((q & 1) == 0 && cb + lane < M) *kv_dst(ea.kv, cb + lane, w.c0 + 32 * q).ab = abw;
       }
+      if (fail) break;
       it += L;
       tc_fence_before();
       __syncwarp();

@@ -109,12 +109,31 @@ __device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s16, uint32_t c) 
 }
 
 // Epilogue of a GEMM launch: Y = epi(acc + bias), or fp32 partials for a split-K reduce.
+// Destination of the group slice that starts at column n (n >= h) of row r.
+struct KvDst {
+  uint8_t* codes;      // the slice's first code byte
+  uint32_t* ab;        // the group's statistics word
+};
+__device__ __forceinline__ KvDst kv_dst(const KvOut& kv, int64_t r, int64_t n) {
+  const bool isv = n >= 2 * (int64_t)kv.h;
+  const int c = (int)(n - (isv ? 2 * (int64_t)kv.h : (int64_t)kv.h));
+  const int head = c / kv.d, cin = c - head * kv.d;
+  const int64_t b = r / kv.T;
+  const int t = (int)(r - b * kv.T);
+  const int64_t slot = (b * kv.H + head) * (int64_t)kv.cap + kv.pos + t;
+  KvDst o;
+  o.codes = (isv ? kv.v_codes : kv.k_codes) + slot * (kv.d / 2) + cin / 2;
+  o.ab = (isv ? kv.v_ab : kv.k_ab) + slot * (kv.d / 64) + cin / 64;
+  return o;
+}
+
 struct EpiArgs {
   const uint16_t* bias;
   const uint16_t* residual;
   uint16_t* Y;
   float* partial;     // split-K: [splits][M][N] fp32, else null
   int epi;
+  KvOut kv;
 };
 
 

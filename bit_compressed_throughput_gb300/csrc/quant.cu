@@ -20,45 +20,16 @@ namespace {
 constexpr int kThreads = 256;                 // 32 groups per CTA
 constexpr int kGroupsPerCta = kThreads / 8;
 
-// Order keys of the two fp16 values of a word, one per 16-bit lane: unsigned order of a
-// key is the numeric order of the value, with -0 below +0 (key = u ^ 0x8000 for a clear
-// sign bit, u ^ 0xFFFF for a set one).
-__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
-  const uint32_t neg = (w >> 15) & 0x00010001u;
-  return w ^ (0x80008000u | (neg * 0x7FFFu));
-}
-
 // Quantise the 8 values held by this thread (part of a 64-group spread over 8 lanes).
 // Returns the packed codes; *ab_out receives the group's statistics word.  The group min
 // and max travel as one word (min key | ~max key << 16) reduced with a 16-bit SIMD min.
 __device__ __forceinline__ uint32_t quantize8(const uint4 v, uint32_t* ab_out) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t kmin2 = order_keys2(w[0]), kmax2 = kmin2;
-#pragma unroll
-  for (int i = 1; i < 4; ++i) {
-    const uint32_t k2 = order_keys2(w[i]);
-    kmin2 = __vminu2(kmin2, k2);
-    kmax2 = __vmaxu2(kmax2, k2);
-  }
-  const uint32_t kmin = min(kmin2 & 0xFFFFu, kmin2 >> 16);
-  const uint32_t kmax = max(kmax2 & 0xFFFFu, kmax2 >> 16);
-  uint32_t mm = kmin | ((~kmax & 0xFFFFu) << 16);
+  uint32_t mm = q4_minmax8(w);
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
-  const uint32_t abits = key_to_bits(mm & 0xFFFFu), bbits = key_to_bits(~(mm >> 16) & 0xFFFFu);
-  const float af = h2f((uint16_t)abits), bf = h2f((uint16_t)bbits);
-  const float bma = __fsub_rn(bf, af);
-  const float c15 = __fmul_rn(15.0f, __frcp_rn(bma));
-  uint32_t codes = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 x2 = unpack_h2(w[i]);
-    const uint32_t c0 = q4_code_rcp(x2.x, af, bma, c15);
-    const uint32_t c1 = q4_code_rcp(x2.y, af, bma, c15);
-    codes |= (c0 | (c1 << 4)) << (8 * i);
-  }
-  *ab_out = abits | (bbits << 16);
-  return codes;
+  *ab_out = q4_ab_word(mm);
+  return q4_codes8(w, q4_group(*ab_out));
 }
 
 __global__ void __launch_bounds__(kThreads)

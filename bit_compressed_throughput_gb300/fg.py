@@ -58,6 +58,10 @@ _SIGS = {
     "fg_dequant_gemm_q4": ([_P, _I64, C.POINTER(fg_q4mat), _P, C.c_int, _P, _P, _P, _SZ, _P],
                            C.c_int),
     "fg_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
+    "fg_dequant_gemm_q4_kv": ([_P, _I64, C.POINTER(fg_q4mat), _P, _P, C.POINTER(fg_kvcache),
+                               _I32, _I32, _P, _SZ, _P], C.c_int),
+    "fg_dequant_gemm_q4_ln": ([_P, _I64, C.POINTER(fg_q4mat), _P, C.c_int, _P, _P, _P, _P, _F,
+                               _P, _P, _SZ, _P], C.c_int),
     "fg_kv_append_q4": ([_P, _P, _I64, _I32, _I32, C.POINTER(fg_kvcache), _P], C.c_int),
     "fg_decode_attn_q4kv": ([_P, _I64, C.POINTER(fg_kvcache), _I32, _F, _P, _P, _SZ, _P],
                             C.c_int),
@@ -217,6 +221,27 @@ def fg_dequant_gemm_q4(X, W: Q4Weight, bias, epilogue: int, residual, Y, ws=None
     _check("fg_dequant_gemm_q4",
            lib.fg_dequant_gemm_q4(_ptr(X), M, C.byref(st), _ptr(bias), epilogue, _ptr(residual),
                                   _ptr(Y), _ptr(ws), wsb, _stream(stream)))
+
+
+def fg_dequant_gemm_q4_kv(X, W: Q4Weight, bias, Y, cache: KVCacheQ4, T: int, pos: int, ws=None,
+                          stream=None):
+    M = X.shape[0]
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    st, kst = W.struct(), cache.struct()
+    _check("fg_dequant_gemm_q4_kv",
+           lib.fg_dequant_gemm_q4_kv(_ptr(X), M, C.byref(st), _ptr(bias), _ptr(Y), C.byref(kst),
+                                     T, pos, _ptr(ws), wsb, _stream(stream)))
+
+
+def fg_dequant_gemm_q4_ln(X, W: Q4Weight, bias, epilogue: int, residual, Y, gamma, beta,
+                          eps: float, Y_ln, ws=None, stream=None):
+    M = X.shape[0]
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    st = W.struct()
+    _check("fg_dequant_gemm_q4_ln",
+           lib.fg_dequant_gemm_q4_ln(_ptr(X), M, C.byref(st), _ptr(bias), epilogue, _ptr(residual),
+                                     _ptr(Y), _ptr(gamma), _ptr(beta), eps, _ptr(Y_ln), _ptr(ws),
+                                     wsb, _stream(stream)))
 
 
 def fg_kv_append_q4(k_new, v_new, row_stride: int, T: int, pos: int, cache: KVCacheQ4,

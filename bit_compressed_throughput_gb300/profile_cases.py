@@ -30,8 +30,6 @@ def gemm_case(M, K, N, epi, reps):
     Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     wsb = fg.fg_gemm_workspace_bytes(M, K, N)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
-    tws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(cache, length), dtype=torch.uint8,
-                      device="cuda") if topk else None
     for _ in range(1 + reps):
         fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
     fg.fg_check_device_error()
@@ -76,6 +74,8 @@ CASES = {
     "decode-attn-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r),
     # top-K sparse attention on the quarter KV workload: the top 10% (106 of 1056 positions)
     "decode-attn-topk-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r, topk=106),
+    # top-K on the full KV workload (launch lists only: 4.3 GB of cache)
+    "decode-attn-topk-kv": lambda r: attn_case(512, 56, 128, 1056, r, topk=106),
 }
 
 

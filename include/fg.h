@@ -137,6 +137,36 @@ int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const ui
                        size_t ws_bytes, void* stream);
 size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
+/* The QKV projection with the KV quantise-and-append in its epilogue:
+ *   Y[M][3h] = X[M][K] * W^[K][3h] + bias   (columns: Q, then K, then V),
+ * and for every row r = b*T + t (sequence b of the cache, t < T) the K and V columns of
+ * row r, rounded to fp16 as Y holds them, are quantised in groups of 64 (the same codes
+ * and (a, b) as fg_kv_append_q4 gives for those rows) and written at position pos + t.
+ * One launch (two when M is small enough for a split-K sum): the fp16 K/V are not read
+ * back from memory.  h = kv->h, a multiple of 128; W->N == 3h; M == kv->B * T; T >= 1;
+ * pos + T <= kv->cap.  Y is still written in full (prefill attention reads the fp16 K/V).
+ * ws as for fg_dequant_gemm_q4.  Errors as fg_dequant_gemm_q4, plus FG_ERR_CAPACITY.
+ * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": K/V grouped 64
+ *  along the hidden dimension] */
+int fg_dequant_gemm_q4_kv(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
+                          uint16_t* Y, const fg_kvcache* kv, int32_t T, int32_t pos, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* A GEMM whose output rows also pass through the pre-LN LayerNorm of the next sub-layer:
+ *   Y = epilogue(X * W^ + bias)   (as fg_dequant_gemm_q4),
+ *   Y_ln[r] = (Y[r] - mean) / sqrt(var + ln_eps) * ln_gamma + ln_beta   over the N values of
+ *   row r of Y as stored (fp16), fp32 mean and population variance (as fg_layernorm).
+ * When the plan splits K (few rows) the split-K reduce sums the partials, applies the
+ * epilogue, stores Y and normalises the row in the same kernel (one CTA per row); otherwise
+ * the GEMM is followed by the LayerNorm kernel.  N <= 16384; Y_ln must not alias Y (it
+ * may alias nothing the GEMM reads).  ws as for fg_dequant_gemm_q4.  Errors as
+ * fg_dequant_gemm_q4.  [OPT decoder layer as a pre-LN block; FlexGen paper explainer,
+ *  "Computation Delegation": the layer's GEMMs and attention on the GPU] */
+int fg_dequant_gemm_q4_ln(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
+                          int epilogue, const uint16_t* residual, uint16_t* Y,
+                          const uint16_t* ln_gamma, const uint16_t* ln_beta, float ln_eps,
+                          uint16_t* Y_ln, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------- KV cache */
 
 /* Quantise new keys and values into the cache at positions pos .. pos+T-1 of every

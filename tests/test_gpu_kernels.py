@@ -198,6 +198,140 @@ def test_gemm_stream(fg, M, K, N, epi, bias):
     assert fg.fg_prof_query(fg.K_GEMM)["launches"] == 0
 
 
+# QKV projection with the KV quantise-and-append in the GEMM epilogue.  The codes and (a, b)
+# are bit-exact against the oracle's quantiser applied to the K/V columns of the kernel's own
+# fp16 output (Y); Y itself matches the plain GEMM bit for bit and the oracle GEMM within
+# the float tolerance.  Cases cover the streaming kernel unsplit and split-K (the reduce
+# kernel appends), and the tiled kernel with ragged token tiles; d = 64 and 128.
+@pytest.mark.parametrize("B,T,pos,h,H,K,cap,path", [
+    (64, 1, 7, 512, 4, 256, 16, "stream"),          # decode: one new token per sequence
+    (16, 1, 0, 256, 4, 4096, 16, "split"),         # long K: split-K, appended by the reduce
+    (5, 1, 31, 768, 6, 1024, 32, "any"),           # six heads of 128, last cache slot
+    (40, 5, 3, 256, 4, 256, 16, "tiled"),          # 200 rows: tiled kernel, ragged tile
+    (3, 100, 0, 512, 8, 512, 112, "tiled"),        # prefill rows, d = 64
+])
+def test_gemm_kv_append(fg, B, T, pos, h, H, K, cap, path):
+    M, N = B * T, 3 * h
+    seed = B * 1000 + T * 10 + h
+    x16 = fg_synth.random_fp16((M, K), seed, 1.0)
+    w16 = fg_synth.random_fp16((K, N), seed + 1, 0.02)
+    bias16 = fg_synth.random_fp16((N,), seed + 2, 0.1)
+    W = fg.Q4Weight.from_fp16(dev(w16))
+    X, bias = dev(x16), dev(bias16)
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+    cache = fg.KVCacheQ4(B, cap, h, H)
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    try:
+        fg.fg_dequant_gemm_q4_kv(X, W, bias, Y, cache, T, pos, ws)
+        fg.fg_check_device_error()
+    finally:
+        fg.fg_prof_enable(False)
+    n_stream = fg.fg_prof_query(fg.K_GEMM_STREAM)["launches"]
+    n_reduce = fg.fg_prof_query(fg.K_GEMM_REDUCE)["launches"]
+    assert fg.fg_prof_query(fg.K_KV_APPEND)["launches"] == 0
+    if path == "stream":
+        assert n_stream == 1 and n_reduce == 0
+    elif path == "split":
+        assert n_reduce == 1
+    elif path == "tiled":
+        assert n_stream == 0 and fg.fg_prof_query(fg.K_GEMM)["launches"] == 1
+    y16 = host(Y).view(np.float16)
+    # Y: bit-identical to the plain GEMM, and within tolerance of the oracle GEMM
+    Y2 = torch.empty_like(Y)
+    fg.fg_dequant_gemm_q4(X, W, bias, 0, None, Y2, ws)
+    assert torch.equal(Y, Y2)
+    q, a, b = OQ.quantize_g64(w16)
+    ref = x16.astype(np.float64) @ OQ.dequant_g64(q, a, b).astype(np.float64) + bias16
+    assert_close(y16.astype(np.float64), ref, f"qkv+append M={M} N={N}")
+    # the cache: codes and (a, b) of the output's K and V columns, nothing else written
+    for src, codes_t, ab_t in ((y16[:, h:2 * h], cache.k_codes, cache.k_ab),
+                               (y16[:, 2 * h:], cache.v_codes, cache.v_ab)):
+        c_ref, ab_ref = oracle_packed(np.ascontiguousarray(src))
+        got_c = cache_codes_to_rows(host(codes_t))
+        got_ab = cache_codes_to_rows(host(ab_t)).view(np.uint32)
+        assert np.array_equal(got_c[:, pos:pos + T].reshape(M, h // 2), c_ref)
+        assert np.array_equal(got_ab[:, pos:pos + T].reshape(M, h // 64), ab_ref)
+        untouched = np.ones(cap, bool)
+        untouched[pos:pos + T] = False
+        assert not got_c[:, untouched].any() and not got_ab[:, untouched].any()
+
+
+def test_gemm_kv_append_rejects_bad_shapes(fg):
+    h, H, B = 256, 2, 4
+    W = fg.Q4Weight.from_fp16(torch.zeros((256, 3 * h), dtype=torch.float16, device="cuda"))
+    X = torch.zeros((B, 256), dtype=torch.float16, device="cuda")
+    Y = torch.empty((B, 3 * h), dtype=torch.float16, device="cuda")
+    cache = fg.KVCacheQ4(B, 16, h, H)
+    with pytest.raises(fg.FgError, match=r"\(-6\)"):                       # FG_ERR_CAPACITY
+        fg.fg_dequant_gemm_q4_kv(X, W, None, Y, cache, 1, 16, None)      # pos + T > cap
+    with pytest.raises(fg.FgError):
+        fg.fg_dequant_gemm_q4_kv(X[:3], W, None, Y, cache, 1, 0, None)   # M != B * T
+    W2 = fg.Q4Weight.from_fp16(torch.zeros((256, 2 * h), dtype=torch.float16, device="cuda"))
+    with pytest.raises(fg.FgError):
+        fg.fg_dequant_gemm_q4_kv(X, W2, None, Y, cache, 1, 0, None)      # N != 3h
+    assert not host(cache.k_codes).any()
+
+
+# GEMM + LayerNorm of its output rows: Y bit-identical to the plain GEMM, Y_ln within the
+# float tolerance of the oracle's LayerNorm of Y as stored, and within one fp16 step of the
+# standalone LayerNorm kernel on the same Y (the statistics are summed in another order).
+# Split plans run the fused reduce (no LayerNorm launch); unsplit ones the GEMM then the
+# LayerNorm kernel.
+@pytest.mark.parametrize("M,K,N,epi,fused", [
+    (64, 4096, 4096, 2, True),       # decode O projection + residual, then LN2
+    (16, 4096, 8192, 1, True),       # FC1-wide rows: four chunks of 8 per thread
+    (7, 16384, 768, 0, True),        # FC2-long K split 16 ways; 96 chunks for 256 threads
+    (300, 512, 1024, 2, False),      # many rows: unsplit GEMM, then the LayerNorm kernel
+])
+def test_gemm_layernorm(fg, M, K, N, epi, fused):
+    seed = M * 13 + K + N
+    x16 = fg_synth.random_fp16((M, K), seed, 1.0)
+    w16 = fg_synth.random_fp16((K, N), seed + 1, 0.02)
+    bias16 = fg_synth.random_fp16((N,), seed + 2, 0.1)
+    res16 = fg_synth.random_fp16((M, N), seed + 3, 1.0, offset=0.5) if epi == 2 else None
+    g16 = fg_synth.random_fp16((N,), seed + 4, 0.1, offset=1.0)
+    b16 = fg_synth.random_fp16((N,), seed + 5, 0.1)
+    W = fg.Q4Weight.from_fp16(dev(w16))
+    X, bias, g, b = dev(x16), dev(bias16), dev(g16), dev(b16)
+    res = dev(res16) if res16 is not None else None
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    Yln = torch.empty_like(Y)
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    try:
+        fg.fg_dequant_gemm_q4_ln(X, W, bias, epi, res, Y, g, b, 1e-5, Yln, ws)
+        fg.fg_check_device_error()
+    finally:
+        fg.fg_prof_enable(False)
+    n_ln = fg.fg_prof_query(fg.K_LAYERNORM)["launches"]
+    n_red = fg.fg_prof_query(fg.K_GEMM_REDUCE)["launches"]
+    assert (n_ln, n_red) == ((0, 1) if fused else (1, 0))
+    Y2 = torch.empty_like(Y)
+    fg.fg_dequant_gemm_q4(X, W, bias, epi, res, Y2, ws)
+    assert torch.equal(Y, Y2)
+    y16 = host(Y).view(np.float16)
+    ref = OL.layernorm(y16, g16, b16, 1e-5)
+    assert_close(f16(Yln), ref, f"gemm+ln M={M} N={N}")
+    Y3 = torch.empty_like(Y)
+    fg.fg_layernorm(Y, g, b, 1e-5, Y3)
+    d = np.abs(f16(Yln) - f16(Y3))
+    assert d.max() <= np.abs(f16(Y3)).max() * 2.0 ** -10
+
+
+def test_gemm_layernorm_rejects_aliasing(fg):
+    W = fg.Q4Weight.from_fp16(torch.zeros((64, 256), dtype=torch.float16, device="cuda"))
+    X = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
+    Y = torch.empty((4, 256), dtype=torch.float16, device="cuda")
+    g = torch.ones(256, dtype=torch.float16, device="cuda")
+    with pytest.raises(fg.FgError):
+        fg.fg_dequant_gemm_q4_ln(X, W, None, 0, None, Y, g, g, 1e-5, Y, None)
+
+
 def test_gemm_split_k(fg):
     wsb = gemm_case(fg, 64, 4096, 512, 2, True, seed=77)
     assert wsb > 0                                        # the split-K path ran
