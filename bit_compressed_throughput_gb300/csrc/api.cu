@@ -631,10 +631,12 @@ int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const
     uint16_t* yk = y + (int64_t)k * M * h;
     const fg_kvcache kvk = kv_slice(*kv, k * g, g);
     if ((rc = run_layernorm(xk, M, h, L->ln1_g, L->ln1_b, dm->ln_eps, ln, st))) return rc;
-    // QKV projection; its epilogue appends the 4-bit K/V of positions 0 .. s-1
-    const KvOut ko = kv_out(kvk, s, 0);
-    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st, &ko)))
+    // QKV projection, then the 4-bit K/V of positions 0 .. s-1.  The append stays a kernel
+    // of its own: quantising in the GEMM epilogue (fg_dequant_gemm_q4_kv) measured slower,
+    // the epilogue warps becoming the bottleneck of the K/V tiles
+    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st)))
       return rc;
+    if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, s, 0, kvk, st))) return rc;
     if ((rc = run_prefill_attn(qkv, g, s, dm->H, dm->d, scale, att, st))) return rc;
     if (dm->f > 0) {
       // O projection + residual into h1, then LN2(h1) (fused into a split-K reduce)
@@ -676,10 +678,10 @@ int fg_layer_decode(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const 
   const int h = dm->h;
   const float scale = 1.0f / sqrtf((float)dm->d);
   if ((rc = run_layernorm(x, M, h, L->ln1_g, L->ln1_b, dm->ln_eps, ln, st))) return rc;
-  // QKV projection; its epilogue appends the new token's 4-bit K/V at position pos
-  const KvOut ko = kv_out(*kv, 1, pos);
-  if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st, &ko)))
-    return rc;
+  // QKV projection, then the new token's 4-bit K/V at position pos (a kernel of its own:
+  // measured faster than the append in the streaming GEMM's epilogue)
+  if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st))) return rc;
+  if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, 1, pos, *kv, st))) return rc;
   if ((rc = run_decode_attn(qkv, 3 * h, *kv, pos + 1, scale, att, aws, sms, st))) return rc;
   if (dm->f == 0) return run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, x, y, gws, sms, st);
   // O projection + residual into h1, then LN2(h1) (fused into the split-K reduce)

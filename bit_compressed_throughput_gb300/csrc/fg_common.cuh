@@ -41,19 +41,19 @@ __device__ __forceinline__ uint32_t q4_code(float xf, float af, float bma) {
 // The same code with the division replaced, where that cannot change the result, by a
 // multiply: y = fl(d * c15) with d = fl(x - a) and c15 = fl(15 * fl(1 / bma)).  Both y and
 // fl(q), q = fl(d * 15) / bma, equal 15 d / bma times at most three (y) or two (fl(q))
-// factors (1 + e), |e| <= 2^-24; since a <= x <= b makes 15 d / bma <= 15 (1 + 2^-24),
+// factors (1 + e), |e| <= 2^-24; since a <= x <= b makes 0 <= 15 d / bma <= 15 (1 + 2^-24),
 // |y - fl(q)| <= 16 * 5 * 2^-24 < 2^-17.  So rint(y) == rint(fl(q)) unless y lies within
-// 2^-17 of a half-integer; within 2^-16 of one, or outside [0, 32), the exact division
-// decides.  The rounded code is at most 15, so it needs no clamp.  Codes are therefore
-// bit-identical to q4_code.
-__device__ __forceinline__ uint32_t q4_code_rcp(float xf, float af, float bma, float c15) {
-  if (bma == 0.0f) return 0u;
-  const float d = __fsub_rn(xf, af);
-  const float y = __fmul_rn(d, c15);
-  float q = rintf(y);
-  if (!(y >= 0.0f && y < 32.0f) || fabsf(y - q) > 0.5f - 0x1p-16f)
-    q = rintf(__fdiv_rn(__fmul_rn(d, 15.0f), bma));
-  return (uint32_t)q;
+// 2^-17 of a half-integer; within 2^-16 of one (or y not a number) `near` is set and the
+// caller must take the exact division (q4_code) instead.  rint(y) comes from adding
+// 1.5 * 2^23: for 0 <= y < 2^22 the sum's unit in the last place is 1, so round-to-nearest-
+// even leaves rint(y) in the low mantissa bits.  Valid for values of the group (a <= x <= b).
+// No branch: the callers quantise many values in unrolled code and fix the rare near ties
+// afterwards.
+__device__ __forceinline__ uint32_t q4_code_fast(float xf, float af, float c15, bool& near) {
+  const float y = __fmul_rn(__fsub_rn(xf, af), c15);
+  const float t = __fadd_rn(y, 12582912.0f);
+  near |= !(fabsf(__fsub_rn(y, __fsub_rn(t, 12582912.0f))) <= 0.5f - 0x1p-16f);
+  return __float_as_uint(t) & 0xFu;
 }
 
 // ---- one quantisation group of 64 fp16 values, held 8 per thread (or 1 per thread)
@@ -98,17 +98,35 @@ __device__ __forceinline__ Q4Group q4_group(uint32_t abw) {
 }
 
 // Packed codes of 8 fp16 values against their group: element 2i in the low nibble, 2i+1
-// in the high nibble of byte i.
-__device__ __forceinline__ uint32_t q4_codes8(const uint32_t (&w)[4], const Q4Group& g) {
+// in the high nibble of byte i.  q4_codes8 takes the fast path and sets `near` when a code
+// needs the exact division; q4_codes8_exact is that division for all 8 (a called function,
+// kept out of the unrolled code that calls it rarely).
+__device__ __forceinline__ uint32_t q4_codes8(const uint32_t (&w)[4], const Q4Group& g, bool& near) {
+  if (g.bma == 0.0f) return 0u;                   // constant group
   uint32_t codes = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 x2 = unpack_h2(w[i]);
-    const uint32_t c0 = q4_code_rcp(x2.x, g.af, g.bma, g.c15);
-    const uint32_t c1 = q4_code_rcp(x2.y, g.af, g.bma, g.c15);
+    const uint32_t c0 = q4_code_fast(x2.x, g.af, g.c15, near);
+    const uint32_t c1 = q4_code_fast(x2.y, g.af, g.c15, near);
     codes |= (c0 | (c1 << 4)) << (8 * i);
   }
   return codes;
+}
+static __device__ __noinline__ uint32_t q4_codes8_exact(uint4 v, float af, float bma) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t codes = 0;
+  for (int i = 0; i < 4; ++i) {
+    const float2 x2 = unpack_h2(w[i]);
+    codes |= (q4_code(x2.x, af, bma) | (q4_code(x2.y, af, bma) << 4)) << (8 * i);
+  }
+  return codes;
+}
+// Fast path, then the exact one when any of the 8 codes is near a tie.
+__device__ __forceinline__ uint32_t q4_codes8_checked(const uint32_t (&w)[4], const Q4Group& g) {
+  bool near = false;
+  const uint32_t c = q4_codes8(w, g, near);
+  return near ? q4_codes8_exact(make_uint4(w[0], w[1], w[2], w[3]), g.af, g.bma) : c;
 }
 
 // Programmatic dependent launch: every library kernel lets the next kernel of the stream

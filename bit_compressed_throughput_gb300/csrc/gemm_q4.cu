@@ -214,6 +214,10 @@ struct KArgs {
   int rc;              // code ring depth
 };
 
+// KV: the K/V append in the epilogue (a separate instance, so that the plain GEMM carries
+// none of its code: the larger kernel measured a few percent slower even when the append
+// never ran).
+template <bool KV>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                   const __grid_constant__ CUtensorMap tmS, const KArgs ka, const EpiArgs ea) {
@@ -510,7 +514,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // transpose)
       const int64_t chb = w.c0 + lane_base + (lane & ~7);
       // a K or V tile of the QKV projection (h is a multiple of 128: no tile straddles)
-      const bool kv_tile = ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
+      const bool kv_tile = KV && ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
+      const KvCol kcol = kv_tile ? kv_col(ea.kv, (int)chb) : KvCol{};
       for (int cb = 0; cb < ntok; cb += 32) {
         // columns past tn (at most cb + 31 <= 255) stay inside this accumulator's 256
         uint32_t r[32];
@@ -600,16 +605,33 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
           break;
         }
         ++xph;
+        // codes of the four tokens' words on the fast path; words with a code near a tie
+        // are redone with the exact division after the unrolled loop
+        uint32_t abv[4], cwv[4], nmask = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          abv[j] = q4_ab_word(__vminu2(mmv[j], xb[32 * (q ^ 1) + 8 * j + (lane & 7)]));
+          const uint32_t ow[4] = {ov[j].x, ov[j].y, ov[j].z, ov[j].w};
+          bool nr = false;
+          cwv[j] = q4_codes8(ow, q4_group(abv[j]), nr);
+          nmask |= (uint32_t)nr << j;
+        }
+        if (nmask) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if ((nmask >> j) & 1u) {
+              const Q4Group g = q4_group(abv[j]);
+              cwv[j] = q4_codes8_exact(ov[j], g.af, g.bma);
+            }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int tt = cb + 8 * j + (lane & 7);
-          const uint32_t abw = q4_ab_word(__vminu2(mmv[j], xb[32 * (q ^ 1) + 8 * j + (lane & 7)]));
-          const uint32_t ow[4] = {ov[j].x, ov[j].y, ov[j].z, ov[j].w};
-          const uint32_t cw = q4_codes8(ow, q4_group(abw));
           if (tt < ntok) {
-            const KvDst dst = kv_dst(ea.kv, w.t0 + tt, chb);
-            *reinterpret_cast<uint32_t*>(dst.codes) = cw;
-            if ((chb & 63) == 0) *dst.ab = abw;
+            const int kr = kv_row(ea.kv, w.t0 + tt);
+            *kv_codes_at(ea.kv, kcol, kr) = cwv[j];
+            if ((chb & 63) == 0) *kv_ab_at(ea.kv, kcol, kr) = abv[j];
           }
         }
       }
@@ -659,9 +681,10 @@ gemm_reduce_kernel(const float* __restrict__ partial, int splits, int64_t M, int
   for (int k = 1; k < 8; k <<= 1) mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, k));
   if (live && n >= ea.kv.h) {
     const uint32_t abw = q4_ab_word(mm);
-    const KvDst dst = kv_dst(ea.kv, row, n);
-    *reinterpret_cast<uint32_t*>(dst.codes) = q4_codes8(w, q4_group(abw));
-    if ((n & 63) == 0) *dst.ab = abw;
+    const KvCol col = kv_col(ea.kv, n);
+    const int kr = kv_row(ea.kv, (int)row);
+    *kv_codes_at(ea.kv, col, kr) = q4_codes8_checked(w, q4_group(abw));
+    if ((n & 63) == 0) *kv_ab_at(ea.kv, col, kr) = abw;
   }
 }
 
@@ -867,8 +890,13 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   if (ln && p.splits == 1) return cudaErrorInvalidValue;     // the caller runs LayerNorm
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
-  static cudaError_t attr_err = cudaFuncSetAttribute(
-      gemm_q4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static cudaError_t attr_err = [] {
+    cudaError_t e0 = cudaFuncSetAttribute(gemm_q4_tc_kernel<false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e1 = cudaFuncSetAttribute(gemm_q4_tc_kernel<true>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    return e0 != cudaSuccess ? e0 : e1;
+  }();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tmX, tmC, tmS;
   e = make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K, (uint64_t)p.M,
@@ -917,7 +945,9 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const int ni = (p.tn <= 128 && p.kb_per_split >= 2 && last_unit_kb >= 2) ? 2 : 1;
   const KArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, make_idesc(p.tn), p.tiles_t, p.tiles_c,
                  p.kblocks, p.kb_per_split, (int)p.units, ra, rx, ni, rc};
-  e = launch_pdl(gemm_q4_tc_kernel, dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st, tmX, tmC,
+  const bool with_kv = ea.kv.k_codes != nullptr && p.splits == 1;
+  e = launch_pdl(with_kv ? gemm_q4_tc_kernel<true> : gemm_q4_tc_kernel<false>,
+                 dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st, tmX, tmC,
                  tmS, ka, ea);
   if (e != cudaSuccess || p.splits == 1) return e;
   if (mid_event) cudaEventRecord(mid_event, st);

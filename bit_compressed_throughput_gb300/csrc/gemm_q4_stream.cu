@@ -162,6 +162,9 @@ __device__ __forceinline__ float2 restore_consts(uint32_t ab) {
   return make_float2(s16, f.x - s16);
 }
 
+// KV: the K/V append in the epilogue (a separate instance, so that the plain GEMM carries
+// none of its code: the larger kernel measured slower even when the append never ran).
+template <bool KV>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmC,
@@ -434,7 +437,10 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
       const int64_t ch = w.c0 + ch_in_tile;
       const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;
       // a K or V tile of the QKV projection (h is a multiple of 128: no tile straddles)
-      const bool kv_tile = ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
+      const bool kv_tile = KV && ea.kv.k_codes != nullptr && !ea.partial && w.c0 >= ea.kv.h;
+      // column part of this lane's destination: its code word (lanes 0, 2, 4, 6: channels
+      // 32q + 4 lane ..) and the group's statistics word (quarters 0 and 2)
+      const KvCol kcol = kv_tile ? kv_col(ea.kv, w.c0 + 32 * q + 4 * (lane & 6)) : KvCol{};
       for (int cb = 0; cb < M; cb += 32) {
         float v[32];
 #pragma unroll
@@ -491,25 +497,47 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
         ++xph;
         const uint32_t abw = q4_ab_word(__vminu2(my, xb[32 * (q ^ 1) + lane]));
         const Q4Group gl = q4_group(abw);             // the group of token cb + lane
+        const int krow = (cb + lane < M) ? kv_row(ea.kv, cb + lane) : 0;
+        if ((q & 1) == 0 && cb + lane < M) *kv_ab_at(ea.kv, kcol, krow) = abw;
         // lanes 0, 2, 4, 6 store the code words of channels 32q + 8j .. + 7 (j = lane / 2);
         // this lane's channel is nibble 4 (lane & 1) + (lane >> 3) of its word
         const int sh = 4 * (4 * (lane & 1) + (lane >> 3));
-        const int64_t n0 = w.c0 + 32 * q + 4 * (lane & 6);
+        // c15 of a constant group is not finite (b - a = 0): its codes are 0, never near
+        const float c15l = (gl.bma == 0.0f) ? 0.0f : gl.c15;
+        uint32_t nearbits = 0;                        // tokens with a code near a tie
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (cb + i >= M) break;
           const float af = __shfl_sync(0xFFFFFFFFu, gl.af, i);
-          const float bma = __shfl_sync(0xFFFFFFFFu, gl.bma, i);
-          const float c15 = __shfl_sync(0xFFFFFFFFu, gl.c15, i);
+          const float c15 = __shfl_sync(0xFFFFFFFFu, c15l, i);
+          const int kr = __shfl_sync(0xFFFFFFFFu, krow, i);
           const float x = h2f((uint16_t)(yp[i >> 1] >> (16 * (i & 1))));
-          uint32_t cw = q4_code_rcp(x, af, bma, c15) << sh;
+          bool nr = false;
+          uint32_t cw = q4_code_fast(x, af, c15, nr) << sh;
+          nearbits |= (uint32_t)nr << i;
           cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 1);
           cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 8);
           cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 16);
-          if ((lane & 0x19) == 0)
-            *reinterpret_cast<uint32_t*>(kv_dst(ea.kv, cb + i, n0).codes) = cw;
+          if ((lane & 0x19) == 0) *kv_codes_at(ea.kv, kcol, kr) = cw;
         }
-        if ((q & 1) == 0 && cb + lane < M) *kv_dst(ea.kv, cb + lane, w.c0 + 32 * q).ab = abw;
+        // rare: tokens with a code near a tie; their words again with the exact division,
+        // from the outputs this thread stored to Y
+        nearbits = __reduce_or_sync(0xFFFFFFFFu, nearbits);
+        while (nearbits) {
+          const int i = __ffs(nearbits) - 1;
+          nearbits &= nearbits - 1;
+          {
+            const float af = __shfl_sync(0xFFFFFFFFu, gl.af, i);
+            const float bma = __shfl_sync(0xFFFFFFFFu, gl.bma, i);
+            const int kr = __shfl_sync(0xFFFFFFFFu, krow, i);
+            const float x = h2f(ea.Y[(int64_t)(cb + i) * N + ch]);     // stored by this thread
+            uint32_t cw = q4_code(x, af, bma) << sh;
+            cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 1);
+            cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 8);
+            cw |= __shfl_xor_sync(0xFFFFFFFFu, cw, 16);
+            if ((lane & 0x19) == 0) *kv_codes_at(ea.kv, kcol, kr) = cw;
+          }
+        }
       }
       if (fail) break;
       it += L;
@@ -533,8 +561,13 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
 cudaError_t launch_gemm_stream(const GemmPlan& p, const fg_q4mat& W, const CUtensorMap& tmX,
                                const EpiArgs& ea, cudaStream_t st) {
   if (p.tn > TN_MAX || p.tiles_t != 1) return cudaErrorInvalidValue;
-  static cudaError_t attr_err = cudaFuncSetAttribute(
-      gemm_q4_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static cudaError_t attr_err = [] {
+    cudaError_t e0 = cudaFuncSetAttribute(gemm_q4_stream_kernel<false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e1 = cudaFuncSetAttribute(gemm_q4_stream_kernel<true>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    return e0 != cudaSuccess ? e0 : e1;
+  }();
   if (attr_err != cudaSuccess) return attr_err;
   // X ring: one slot per A stage; code ring: the rest of shared memory (the HBM stream)
   const int xb = p.tn * 128;
@@ -555,7 +588,9 @@ cudaError_t launch_gemm_stream(const GemmPlan& p, const fg_q4mat& W, const CUten
   const int nbuf = (2 * NI * p.tn <= (int)ACC_COLS) ? 2 : 1;
   const SArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tn, idesc, p.tiles_c, p.kblocks,
                  p.kb_per_split, (int)p.units, rx, rc, nbuf, W.codes, W.ab};
-  return launch_pdl(gemm_q4_stream_kernel, dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st,
+  const bool with_kv = ea.kv.k_codes != nullptr && p.splits == 1;
+  return launch_pdl(with_kv ? gemm_q4_stream_kernel<true> : gemm_q4_stream_kernel<false>,
+                    dim3((unsigned)p.grid), dim3(THREADS), SMEM_BYTES, st,
                     tmX, tmC4, tmS4, ka, ea);
 }
 

@@ -109,22 +109,33 @@ __device__ __forceinline__ uint4 restore8(uint32_t w, uint32_t s16, uint32_t c) 
 }
 
 // Epilogue of a GEMM launch: Y = epi(acc + bias), or fp32 partials for a split-K reduce.
-// Destination of the group slice that starts at column n (n >= h) of row r.
-struct KvDst {
-  uint8_t* codes;      // the slice's first code byte
-  uint32_t* ab;        // the group's statistics word
+// Destination of a K/V value: slot = (b*H + head)*cap + pos + t splits into a row part
+// (b*H*cap + pos + t, from the GEMM row r = b*T + t; B*H*cap < 2^31 is checked on the host)
+// and a column part (head*cap, the channel within the head), so an epilogue computes the
+// row part once per token and the column part once per tile.
+__device__ __forceinline__ int kv_row(const KvOut& kv, int r) {
+  const int b = r / kv.T;
+  return b * kv.H * kv.cap + kv.pos + (r - b * kv.T);
+}
+struct KvCol {
+  uint8_t* codes;      // the code byte of column n at row part 0
+  uint32_t* ab;        // the statistics word of column n's group at row part 0
 };
-__device__ __forceinline__ KvDst kv_dst(const KvOut& kv, int64_t r, int64_t n) {
-  const bool isv = n >= 2 * (int64_t)kv.h;
-  const int c = (int)(n - (isv ? 2 * (int64_t)kv.h : (int64_t)kv.h));
+__device__ __forceinline__ KvCol kv_col(const KvOut& kv, int n) {
+  const bool isv = n >= 2 * kv.h;
+  const int c = n - (isv ? 2 * kv.h : kv.h);
   const int head = c / kv.d, cin = c - head * kv.d;
-  const int64_t b = r / kv.T;
-  const int t = (int)(r - b * kv.T);
-  const int64_t slot = (b * kv.H + head) * (int64_t)kv.cap + kv.pos + t;
-  KvDst o;
-  o.codes = (isv ? kv.v_codes : kv.k_codes) + slot * (kv.d / 2) + cin / 2;
-  o.ab = (isv ? kv.v_ab : kv.k_ab) + slot * (kv.d / 64) + cin / 64;
+  const int64_t hs = (int64_t)head * kv.cap;
+  KvCol o;
+  o.codes = (isv ? kv.v_codes : kv.k_codes) + hs * (kv.d / 2) + cin / 2;
+  o.ab = (isv ? kv.v_ab : kv.k_ab) + hs * (kv.d / 64) + cin / 64;
   return o;
+}
+__device__ __forceinline__ uint32_t* kv_codes_at(const KvOut& kv, const KvCol& col, int row) {
+  return reinterpret_cast<uint32_t*>(col.codes + (int64_t)row * (kv.d / 2));
+}
+__device__ __forceinline__ uint32_t* kv_ab_at(const KvOut& kv, const KvCol& col, int row) {
+  return col.ab + (int64_t)row * (kv.d / 64);
 }
 
 struct EpiArgs {

@@ -259,6 +259,47 @@ def test_gemm_kv_append(fg, B, T, pos, h, H, K, cap, path):
         assert not got_c[:, untouched].any() and not got_ab[:, untouched].any()
 
 
+@pytest.mark.parametrize("B,K,path", [(64, 256, "stream"), (16, 4096, "split"), (200, 256, "tiled")])
+def test_gemm_kv_append_ties(fg, B, K, path):
+    """Codes exactly at half-integers go to the exact division in every epilogue path.
+
+    X = 0 makes Y = bias exactly; the K and V columns of the bias hold groups whose minimum
+    is 0 and maximum 15 * 2^-e, the other values (k + 1/2) * 2^-e, so (x - a) * 15 / (b - a)
+    is a tie k + 1/2 that rounds to the even neighbour."""
+    h, H = 256, 2
+    M, N = B, 3 * h
+    r = np.random.default_rng(B + K)
+    bias16 = r.standard_normal(N).astype(np.float16)
+    for g0 in range(h, N, 64):
+        e = float(2.0 ** -int(r.integers(0, 4)))
+        vals = (r.integers(0, 15, size=64) + 0.5) * e
+        vals[r.choice(64, 2, replace=False)] = [0.0, 15.0 * e]
+        bias16[g0:g0 + 64] = vals.astype(np.float16)
+    W = fg.Q4Weight.from_fp16(dev(fg_synth.random_fp16((K, N), B, 0.02)))
+    X = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+    cache = fg.KVCacheQ4(B, 16, h, H)
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    try:
+        fg.fg_dequant_gemm_q4_kv(X, W, dev(bias16), Y, cache, 1, 5, ws)
+        fg.fg_check_device_error()
+    finally:
+        fg.fg_prof_enable(False)
+    n_red = fg.fg_prof_query(fg.K_GEMM_REDUCE)["launches"]
+    n_stream = fg.fg_prof_query(fg.K_GEMM_STREAM)["launches"]
+    assert (path == "split") == (n_red == 1) and (path == "tiled") == (n_stream == 0)
+    y16 = host(Y).view(np.float16)
+    assert np.array_equal(y16, np.broadcast_to(bias16, (M, N)))
+    for src, codes_t, ab_t in ((y16[:, h:2 * h], cache.k_codes, cache.k_ab),
+                               (y16[:, 2 * h:], cache.v_codes, cache.v_ab)):
+        c_ref, ab_ref = oracle_packed(np.ascontiguousarray(src))
+        assert np.array_equal(cache_codes_to_rows(host(codes_t))[:, 5], c_ref)
+        assert np.array_equal(cache_codes_to_rows(host(ab_t)).view(np.uint32)[:, 5], ab_ref)
+
+
 def test_gemm_kv_append_rejects_bad_shapes(fg):
     h, H, B = 256, 2, 4
     W = fg.Q4Weight.from_fp16(torch.zeros((256, 3 * h), dtype=torch.float16, device="cuda"))
