@@ -535,11 +535,12 @@ int fg_decode_attn_q4kv_topk(const uint16_t* q, int64_t q_stride, const fg_kvcac
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FG_ERR_ARG;
   const size_t need = fg_decode_attn_topk_workspace_bytes(kv, len);
   if (ws_bytes < need || !ws || !aligned16(ws)) return FG_ERR_WORKSPACE;
-  rc = check_device(nullptr);
+  int sms = 0;
+  rc = check_device(&sms);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Span sp(st);
-  cudaError_t e = launch_decode_attn_topk(q, q_stride, *kv, len, k, scale, out, sel, ws, st);
+  cudaError_t e = launch_decode_attn_topk(q, q_stride, *kv, len, k, scale, out, sel, ws, sms, st);
   if (e != cudaSuccess) return set_cuda_error(e);
   sp.stop(FG_K_DECODE_ATTN_TOPK,
           work_decode_attn_topk(kv->B, kv->H, len, k, kv->h));

@@ -57,21 +57,25 @@ constexpr int kWarps = 4;
 constexpr int kTile = 16;                 // positions per mma step
 constexpr int kSub = 3;                   // tiles per ring slot
 constexpr int kSlotPos = kSub * kTile;    // positions per ring slot
-constexpr int kRing = 2;                  // slots per warp
+constexpr int kRing = 2;                  // slots per warp (K and V)
+constexpr int kRingScores = 4;            // slots per warp of the scores-only instance (K)
 constexpr int kPlanWarpsPerSm = 16;       // resident warps per SM assumed by the split plan
 constexpr long long kWaitCycles = 1ll << 32;
 
-template <int D>
+// A slot holds K codes, V codes, K statistics, V statistics (SC: K codes and statistics).
+template <int D, bool SC>
 struct Ring {
   static constexpr int NG = D / 64;                     // groups per head
   static constexpr int ROW_CODE = D / 2;                // code bytes of one position
   static constexpr int ROW_AB = NG * 4;                 // statistics bytes of one position
-  static constexpr int ROW_BYTES = 2 * ROW_CODE + 2 * ROW_AB;   // K and V
+  static constexpr int ROW_BYTES = (SC ? 1 : 2) * (ROW_CODE + ROW_AB);
   static constexpr int CODE_BYTES = kSlotPos * ROW_CODE;
   static constexpr int AB_BYTES = kSlotPos * ROW_AB;
+  static constexpr int KAB_OFF = (SC ? 1 : 2) * CODE_BYTES;     // K statistics in a slot
+  static constexpr int DEPTH = SC ? kRingScores : kRing;
   static constexpr int SLOT = kSlotPos * ROW_BYTES;
-  static constexpr int WARP_BYTES = kRing * SLOT;
-  static constexpr int CTA_BYTES = kWarps * WARP_BYTES + kWarps * kRing * 8;
+  static constexpr int WARP_BYTES = DEPTH * SLOT;
+  static constexpr int CTA_BYTES = kWarps * WARP_BYTES + kWarps * DEPTH * 8;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -161,14 +165,19 @@ __device__ __forceinline__ Item item_of(int item, int H, int len, int splits, in
 }
 
 // D = head dim; NW = 32-bit code words per lane per row (D/32); NG = groups per head.
-template <int D>
+// SC: the scores-only instance (top-K attention): no V; every valid score goes to keys
+// (order keys of the base-2 scores, row b*H + hd of len) and each work item's softmax state
+// (m, l) to ml; out and partial are unused.
+template <int D, bool SC>
 __global__ void __launch_bounds__(kWarps * 32, 4)
 decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
                    const uint8_t* __restrict__ kc, const uint8_t* __restrict__ vc,
                    const uint32_t* __restrict__ kab, const uint32_t* __restrict__ vab, int B,
                    int H, int cap, int len, int splits, int tps, float scale_log2,
-                   uint16_t* __restrict__ out, float* __restrict__ partial) {
-  using R = Ring<D>;
+                   uint16_t* __restrict__ out, float* __restrict__ partial,
+                   uint32_t* __restrict__ keys, float2* __restrict__ ml) {
+  using R = Ring<D, SC>;
+  constexpr int kRing = R::DEPTH;
   constexpr int NW = D / 32;
   constexpr int NG = D / 64;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -204,10 +213,12 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     bar_expect_tx(bar, (uint32_t)(rows * R::ROW_BYTES));
     bulk_copy(smem_u32(slot), kc + row0 * R::ROW_CODE, rows * R::ROW_CODE, bar);
-    bulk_copy(smem_u32(slot + R::CODE_BYTES), vc + row0 * R::ROW_CODE, rows * R::ROW_CODE, bar);
-    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES), kab + row0 * NG, rows * R::ROW_AB, bar);
-    bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES + R::AB_BYTES), vab + row0 * NG,
-              rows * R::ROW_AB, bar);
+    bulk_copy(smem_u32(slot + R::KAB_OFF), kab + row0 * NG, rows * R::ROW_AB, bar);
+    if constexpr (!SC) {
+      bulk_copy(smem_u32(slot + R::CODE_BYTES), vc + row0 * R::ROW_CODE, rows * R::ROW_CODE, bar);
+      bulk_copy(smem_u32(slot + 2 * R::CODE_BYTES + R::AB_BYTES), vab + row0 * NG,
+                rows * R::ROW_AB, bar);
+    }
     ++issued;
     if (++is == kRing) is = 0;
     if (++islot == iitem.nslots) {
@@ -260,12 +271,20 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
         for (int r = 0; r < 2; ++r) {
           const int row = sub * kTile + gid + 8 * r;
           load_words<NW>(slot + row * R::ROW_CODE + tig * 4 * NW, kw[r]);
-          load_words<NG>(slot + 2 * R::CODE_BYTES + row * R::ROW_AB, ka[r]);
+          load_words<NG>(slot + R::KAB_OFF + row * R::ROW_AB, ka[r]);
         }
         float t_sc[2];
         q4attn::tile_scores<D>(kw, ka, qf, t_sc);
         sc[sub][0] = valid(sub, 0) ? t_sc[0] : -INFINITY;
         sc[sub][1] = valid(sub, 1) ? t_sc[1] : -INFINITY;
+        if constexpr (SC) {
+          // every lane of a row holds its score; lane tig == 0 stores it
+          if (tig == 0) {
+            uint32_t* kr = keys + ((int64_t)it.b * H + it.hd) * len + ts + sub * kTile;
+            if (valid(sub, 0)) kr[gid] = q4attn::order_key_f32(t_sc[0]);
+            if (valid(sub, 1)) kr[gid + 8] = q4attn::order_key_f32(t_sc[1]);
+          }
+        }
       }
       // ---- phase 2: lazy rescaling: the reference maximum moves only when a score
       // exceeds it by more than 2^8, so p stays <= 256 and the accumulators rarely need
@@ -298,6 +317,7 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       }
       // ---- phase 3: V weights w_tg = p_t (b - a)_tg / 15 (fp16), the offset term
       // sum_t p_t a_tg, and the V codes (channel rows, position columns)
+      if constexpr (!SC) {
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub) {
         uint32_t vw[2][NW], va[2][NG];
@@ -309,6 +329,7 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
         }
         const bool vr[2] = {valid(sub, 0), valid(sub, 1)};
         q4attn::v_tile<D>(vw, va, p[sub], vr, lane, acc, asum);
+      }
       }
     };
 
@@ -343,6 +364,11 @@ decode_attn_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 4);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 8);
       asum[g] += __shfl_xor_sync(0xFFFFFFFFu, asum[g], 16);
+    }
+    if constexpr (SC) {
+      if (lane == 0) ml[ci] = make_float2(m_run, l);
+      __syncwarp();
+      continue;
     }
     const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
     uint16_t* o = out + (int64_t)it.b * H * D + (int64_t)it.hd * D;
@@ -404,16 +430,17 @@ decode_combine_kernel(const float* __restrict__ partial, int64_t nbh, int H, int
   for (int c = 0; c < D / 32; ++c) op[c * 32 + lane] = f2h(o[c] * inv);
 }
 
-template <int D>
+template <int D, bool SC>
 int resident_ctas() {
   static int occ = [] {
     int n = 0;
     // the rings exceed the 48 KB default; prefer the carveout that admits the most CTAs
-    cudaFuncSetAttribute(decode_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Ring<D>::CTA_BYTES);
-    cudaFuncSetAttribute(decode_attn_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<D>, kWarps * 32,
-                                                      Ring<D>::CTA_BYTES) != cudaSuccess ||
+    cudaFuncSetAttribute(decode_attn_kernel<D, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Ring<D, SC>::CTA_BYTES);
+    cudaFuncSetAttribute(decode_attn_kernel<D, SC>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<D, SC>, kWarps * 32,
+                                                      Ring<D, SC>::CTA_BYTES) != cudaSuccess ||
         n < 1)
       n = 1;
     return n;
@@ -474,18 +501,20 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
   float* partial = static_cast<float*>(ws);
   const int64_t want = (items + kWarps - 1) / kWarps;
   if (d == 128) {
-    const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<128>());
-    cudaError_t e0 = launch_pdl(decode_attn_kernel<128>, dim3(grid), dim3(kWarps * 32),
-                                Ring<128>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes,
-                                kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2, out,
-                                partial);
+    const unsigned grid =
+        (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<128, false>());
+    cudaError_t e0 = launch_pdl(decode_attn_kernel<128, false>, dim3(grid), dim3(kWarps * 32),
+                                Ring<128, false>::CTA_BYTES, st, q, q_stride, kv.k_codes,
+                                kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps,
+                                sl2, out, partial, nullptr, nullptr);
     if (e0 != cudaSuccess) return e0;
   } else {
-    const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<64>());
-    cudaError_t e0 = launch_pdl(decode_attn_kernel<64>, dim3(grid), dim3(kWarps * 32),
-                                Ring<64>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes,
-                                kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2, out,
-                                partial);
+    const unsigned grid =
+        (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<64, false>());
+    cudaError_t e0 = launch_pdl(decode_attn_kernel<64, false>, dim3(grid), dim3(kWarps * 32),
+                                Ring<64, false>::CTA_BYTES, st, q, q_stride, kv.k_codes,
+                                kv.v_codes, kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps,
+                                sl2, out, partial, nullptr, nullptr);
     if (e0 != cudaSuccess) return e0;
   }
   cudaError_t e = cudaGetLastError();
@@ -504,6 +533,34 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
     *kernels_out = 2;
   }
   return e;
+}
+
+cudaError_t launch_decode_attn_scores(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
+                                      int32_t len, float scale, uint32_t* keys, float2* ml,
+                                      int nsm, cudaStream_t st, int* splits_out) {
+  const int d = kv.h / kv.H;
+  const int splits = decode_attn_splits(kv, len, nsm);
+  const int ntiles = (len + kTile - 1) / kTile;
+  const int tps = (ntiles + splits - 1) / splits;
+  const int64_t items = (int64_t)kv.B * kv.H * splits;
+  if (items >= (1ll << 31)) return cudaErrorInvalidValue;   // work items are 32-bit
+  *splits_out = splits;
+  const float sl2 = scale * 1.4426950408889634f;
+  const int64_t want = (items + kWarps - 1) / kWarps;
+  if (d == 128) {
+    const unsigned grid =
+        (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<128, true>());
+    return launch_pdl(decode_attn_kernel<128, true>, dim3(grid), dim3(kWarps * 32),
+                      Ring<128, true>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes,
+                      kv.k_ab, kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2,
+                      (uint16_t*)nullptr, (float*)nullptr, keys, ml);
+  }
+  const unsigned grid =
+      (unsigned)std::min<int64_t>(want, (int64_t)nsm * resident_ctas<64, true>());
+  return launch_pdl(decode_attn_kernel<64, true>, dim3(grid), dim3(kWarps * 32),
+                    Ring<64, true>::CTA_BYTES, st, q, q_stride, kv.k_codes, kv.v_codes, kv.k_ab,
+                    kv.v_ab, kv.B, kv.H, kv.cap, len, splits, tps, sl2, (uint16_t*)nullptr,
+                    (float*)nullptr, keys, ml);
 }
 
 cudaError_t attn_read_error(unsigned int* out) {

@@ -24,6 +24,15 @@
 namespace fg {
 namespace q4attn {
 
+// float -> unsigned key with the same order (negative values reversed below the positives)
+__device__ __forceinline__ uint32_t order_key_f32(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_f32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // The four pairs (c_i, c_{i+4}) of a code word as fp16 subnormals: pairs 0 and 2 hold
 // c * 2^-24, pairs 1 and 3 hold 16c * 2^-24.
 __device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {

@@ -11,19 +11,19 @@
 // kernel's; K is read whole.
 //
 // Two kernels:
-//   topk_scores_kernel  a warp per sixteen 16-position tiles of one (b, hd): the scores on the
-//                       tensor cores from the 4-bit K (the dense kernel's arithmetic), in
-//                       base 2, into the workspace
-//   topk_attend_kernel  one warp per (b, hd): the scores read once into shared memory as
-//                       order-preserving keys; the softmax maximum and denominator over all
-//                       positions; the k-th largest key by radix selection, eight bits per
-//                       round from the top (a 256-bin histogram of the keys that share the
-//                       bits found so far, then the bin holding the remaining rank);
-//                       the selected positions compacted in position order (keys above T,
-//                       then keys equal to T from the lowest position); then the V rows of
-//                       the selected positions gathered 16 at a time into the dense
-//                       kernel's tensor-core tile (weights 2^(s - m), the softmax
-//                       denominator applied at the end).
+//   scores   the dense decode kernel's scores-only instance (attn_decode.cu): K streamed
+//            through its shared-memory ring, the scores on the tensor cores in base 2, each
+//            written as an order-preserving key, and each work item's online-softmax state
+//            (reference maximum m, sum l) kept for the denominator
+//   topk_attend_kernel  one warp per (b, hd): the softmax denominator from the work items'
+//                       (m, l); the keys once into shared memory; the k-th largest key by
+//                       radix selection, eight bits per round from the top (a 256-bin
+//                       histogram of the keys that share the bits found so far, then the bin
+//                       holding the remaining rank); the selected positions compacted in
+//                       position order (keys above T, then keys equal to T from the lowest
+//                       position); then the V rows of the selected positions gathered 16 at a
+//                       time into the dense kernel's tensor-core tile (weights 2^(s - M), the
+//                       softmax denominator applied at the end).
 #include <math.h>
 
 #include "attn_q4.cuh"
@@ -34,19 +34,7 @@ namespace fg {
 
 namespace {
 
-constexpr int kScoreWarps = 4;            // warps per CTA of the score kernel
-constexpr int kScoreTiles = 4;            // 16-position tiles loaded together
-constexpr int kScoreBatches = 4;          // batches of kScoreTiles per warp
-
-// float -> unsigned key with the same order (negative values reversed below the positives)
-__device__ __forceinline__ uint32_t order_key_f32(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_to_f32(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
+using q4attn::key_to_f32;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -62,76 +50,12 @@ __device__ __forceinline__ float warp_sum_gid(float v) {
   return v;
 }
 
-// One warp per kScoreBatches x kScoreTiles consecutive 16-position tiles of one (b, hd),
-// kScoreTiles at a time, one query fragment for all of them: the K rows
-// straight from global memory (lane (gid, tig): 16 bytes of rows gid and gid+8, a tile is one
-// contiguous 1 KB run for d = 128), the scores on the tensor cores, lanes with tig == 0
-// writing their two rows.  The loads of a batch are issued before its arithmetic.
-template <int D>
-__global__ void __launch_bounds__(kScoreWarps * 32)
-topk_scores_kernel(const uint16_t* __restrict__ q, int64_t q_stride,
-                   const uint8_t* __restrict__ kc, const uint32_t* __restrict__ kab, int H,
-                   int cap, int len, float scale_log2, float* __restrict__ scores) {
-  constexpr int NW = D / 32, NG = D / 64;
-  pdl_launch_dependents();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int bh = blockIdx.x;
-  const int b = bh / H, hd = bh - b * H;
-  const int ntiles = (len + 15) / 16;
-  const int tile_w = (blockIdx.y * kScoreWarps + warp) * kScoreTiles * kScoreBatches;
-  if (tile_w >= ntiles) return;
-  q4attn::QFrag<D> qf;
-  q4attn::load_q_frag<D>(q + (int64_t)b * q_stride + (int64_t)hd * D, lane, scale_log2, qf);
-#pragma unroll 1
-  for (int tile0 = tile_w; tile0 < min(ntiles, tile_w + kScoreTiles * kScoreBatches);
-       tile0 += kScoreTiles) {
-    // tiles are whole 16 positions: rows past len stay below cap (a multiple of 16)
-    uint32_t kw[kScoreTiles][2][NW], ka[kScoreTiles][2][NG];
-#pragma unroll
-    for (int i = 0; i < kScoreTiles; ++i) {
-      if (tile0 + i >= ntiles) break;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int64_t row = (int64_t)bh * cap + (tile0 + i) * 16 + gid + 8 * r;
-        const uint8_t* kp = kc + row * (D / 2) + tig * 4 * NW;
-        if constexpr (NW == 4) {
-          const uint4 u = ldg_nc_v4(kp);
-          kw[i][r][0] = u.x; kw[i][r][1] = u.y; kw[i][r][2 % NW] = u.z; kw[i][r][3 % NW] = u.w;
-        } else {
-          const uint2 u = *reinterpret_cast<const uint2*>(kp);
-          kw[i][r][0] = u.x; kw[i][r][1 % NW] = u.y;
-        }
-        if constexpr (NG == 2) {
-          const uint2 u = *reinterpret_cast<const uint2*>(kab + row * NG);
-          ka[i][r][0] = u.x; ka[i][r][NG - 1] = u.y;
-        } else {
-          ka[i][r][0] = kab[row];
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kScoreTiles; ++i) {
-      if (tile0 + i >= ntiles) break;
-      float sc[2];
-      q4attn::tile_scores<D>(kw[i], ka[i], qf, sc);
-      if (tig == 0) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int t = (tile0 + i) * 16 + gid + 8 * r;
-          if (t < len) scores[(int64_t)bh * len + t] = sc[r];
-        }
-      }
-    }
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(32)
-topk_attend_kernel(const float* __restrict__ scores, const uint8_t* __restrict__ vc,
-                   const uint32_t* __restrict__ vab, int H, int cap, int len, int k,
-                   uint16_t* __restrict__ out, int32_t* __restrict__ sel_out) {
+topk_attend_kernel(const uint32_t* __restrict__ keys_g, const float2* __restrict__ ml,
+                   int splits, const uint8_t* __restrict__ vc, const uint32_t* __restrict__ vab,
+                   int H, int cap, int len, int k, uint16_t* __restrict__ out,
+                   int32_t* __restrict__ sel_out) {
   constexpr int NW = D / 32, NG = D / 64;
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);            // 256 radix counters
@@ -141,20 +65,17 @@ topk_attend_kernel(const float* __restrict__ scores, const uint8_t* __restrict__
   pdl_wait();
   const int lane = threadIdx.x;
   const int bh = blockIdx.x;
-  const float* sc = scores + (int64_t)bh * len;
-  // ---- the scores once, as order keys in shared memory; the largest key
-  uint32_t kmax = 0u;
-  for (int t = lane; t < len; t += 32) {
-    const uint32_t key = order_key_f32(sc[t]);
-    keys[t] = key;
-    kmax = max(kmax, key);
-  }
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-  const float m = key_to_f32(kmax);
+  // ---- the softmax denominator from the work items' states: M = max m_s,
+  // z = sum_s l_s 2^(m_s - M) (splits <= 16 < 32 lanes; every item saw a valid position)
+  const float2 st = (lane < splits) ? ml[(int64_t)bh * splits + lane] : make_float2(-INFINITY, 0.0f);
+  float m = st.x;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const float z = warp_sum((lane < splits) ? st.y * exp2f(st.x - m) : 0.0f);
+  // ---- the keys once into shared memory
+  const uint32_t* kg = keys_g + (int64_t)bh * len;
+  for (int t = lane; t < len; t += 32) keys[t] = kg[t];
   __syncwarp();
-  float z = 0.0f;                                     // softmax denominator (base 2)
-  for (int t = lane; t < len; t += 32) z += exp2f(key_to_f32(keys[t]) - m);
-  z = warp_sum(z);
   // ---- the k-th largest key, eight bits per round from the top: a histogram of the keys
   // that share the bits found so far, then the bin that holds the remaining rank
   uint32_t prefix = 0u, pmask = 0u;
@@ -225,7 +146,8 @@ topk_attend_kernel(const float* __restrict__ scores, const uint8_t* __restrict__
   if (sel_out)
     for (int i = lane; i < k; i += 32) sel_out[(int64_t)bh * k + i] = sel[i];
   // ---- values of the selected positions, 16 per tile on the tensor cores (the dense
-  // kernel's arithmetic) with weights 2^(s - m) <= 1; the denominator divides at the end
+  // kernel's arithmetic) with weights 2^(s - M) <= 2^8 (M trails the largest score by at
+  // most 8, the lazy rescaling bound); the denominator divides at the end
   const int gid = lane >> 2, tig = lane & 3;
   float acc[2 * NW][4];
 #pragma unroll
@@ -273,43 +195,46 @@ topk_attend_kernel(const float* __restrict__ scores, const uint8_t* __restrict__
 }
 
 template <int D>
-cudaError_t launch_topk_d(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv, int32_t len,
-                          int32_t k, float scale, uint16_t* out, int32_t* sel, float* ws,
+cudaError_t launch_attend(const fg_kvcache& kv, int32_t len, int32_t k, uint16_t* out,
+                          int32_t* sel, const uint32_t* keys, const float2* ml, int splits,
                           cudaStream_t st) {
   const int64_t nbh = (int64_t)kv.B * kv.H;
-  const float sl2 = scale * 1.4426950408889634f;
-  const int ntiles = (len + 15) / 16;
-  const int per_cta = kScoreWarps * kScoreTiles * kScoreBatches;
-  const dim3 g1((unsigned)nbh, (unsigned)((ntiles + per_cta - 1) / per_cta));
-  cudaError_t e = launch_pdl(topk_scores_kernel<D>, g1, dim3(kScoreWarps * 32), 0, st, q, q_stride,
-                             kv.k_codes, reinterpret_cast<const uint32_t*>(kv.k_ab), kv.H,
-                             kv.cap, len, sl2, ws);
-  if (e != cudaSuccess) return e;
   const size_t smem = 1024 + (size_t)len * 4 + (size_t)k * 4;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(topk_attend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(topk_attend_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(topk_attend_kernel<D>, dim3((unsigned)nbh), dim3(32), smem, st,
-                    static_cast<const float*>(ws), kv.v_codes,
-                    reinterpret_cast<const uint32_t*>(kv.v_ab), kv.H, kv.cap, len, k, out, sel);
+  return launch_pdl(topk_attend_kernel<D>, dim3((unsigned)nbh), dim3(32), smem, st, keys, ml,
+                    splits, kv.v_codes, reinterpret_cast<const uint32_t*>(kv.v_ab), kv.H, kv.cap,
+                    len, k, out, sel);
+}
+
+// Workspace: the keys [B*H][len], then (16-byte aligned) the work items' (m, l).
+size_t keys_bytes(const fg_kvcache& kv, int32_t len) {
+  return ((size_t)kv.B * kv.H * (size_t)len * sizeof(uint32_t) + 15) & ~size_t(15);
 }
 
 }  // namespace
 
 size_t decode_attn_topk_ws_bytes(const fg_kvcache& kv, int32_t len) {
-  return (size_t)kv.B * kv.H * (size_t)len * sizeof(float);
+  // the split count is at most the plan for kMaxSms SMs (decode_attn_splits)
+  const int splits = decode_attn_splits(kv, len, kMaxSms);
+  return keys_bytes(kv, len) + (size_t)kv.B * kv.H * splits * sizeof(float2);
 }
 
 cudaError_t launch_decode_attn_topk(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
                                     int32_t len, int32_t k, float scale, uint16_t* out,
-                                    int32_t* sel, void* ws, cudaStream_t st) {
+                                    int32_t* sel, void* ws, int nsm, cudaStream_t st) {
   if ((int64_t)kv.B * kv.H >= (1ll << 31)) return cudaErrorInvalidValue;
-  float* w = static_cast<float*>(ws);
+  uint32_t* keys = static_cast<uint32_t*>(ws);
+  float2* ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + keys_bytes(kv, len));
+  int splits = 1;
+  cudaError_t e = launch_decode_attn_scores(q, q_stride, kv, len, scale, keys, ml, nsm, st, &splits);
+  if (e != cudaSuccess) return e;
   const int d = kv.h / kv.H;
-  return (d == 128) ? launch_topk_d<128>(q, q_stride, kv, len, k, scale, out, sel, w, st)
-                    : launch_topk_d<64>(q, q_stride, kv, len, k, scale, out, sel, w, st);
+  return (d == 128) ? launch_attend<128>(kv, len, k, out, sel, keys, ml, splits, st)
+                    : launch_attend<64>(kv, len, k, out, sel, keys, ml, splits, st);
 }
 
 }  // namespace fg

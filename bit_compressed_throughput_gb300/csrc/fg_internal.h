@@ -56,12 +56,18 @@ cudaError_t launch_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvc
                                int num_sms, cudaStream_t st, int* kernels_out,
                                cudaEvent_t mid_event);
 
-// Top-K sparse decode attention: score workspace bytes; launches the score and the
+// Scores-only decode attention (top-K): the dense kernel's K stream and scores, each score
+// as an order key into keys [B*H][len], each work item's softmax state (m, l) into ml
+// [B*H][splits]; *splits_out receives the split count.
+cudaError_t launch_decode_attn_scores(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
+                                      int32_t len, float scale, uint32_t* keys, float2* ml,
+                                      int nsm, cudaStream_t st, int* splits_out);
+// Top-K sparse decode attention: workspace bytes; launches the score and the
 // select-and-attend kernels.
 size_t decode_attn_topk_ws_bytes(const fg_kvcache& kv, int32_t len);
 cudaError_t launch_decode_attn_topk(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv,
                                     int32_t len, int32_t k, float scale, uint16_t* out,
-                                    int32_t* sel, void* ws, cudaStream_t st);
+                                    int32_t* sel, void* ws, int nsm, cudaStream_t st);
 
 // Dequant-fused GEMM plan: tn tokens x 128 channels per tile, split-K factor and
 // workspace.  kind 0: the tiled kernel (restored weights in shared memory); kind 1: the
