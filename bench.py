@@ -41,10 +41,11 @@ from bit_compressed_throughput_gb300 import replicas  # noqa: E402
 
 METRIC = "generated tokens/s per OPT-shaped layer stack at 1 GB300; decode-attn HBM GB/s % peak"
 UNIT = "tokens/s"
-# DRAM bytes (read + write) per GEMM launch: the mean over the 560 GEMM launches of one
-# generation pass of this workload, from an ncu capture of dram__bytes_read.sum and
-# dram__bytes_write.sum; reset to None whenever the GEMM kernel changes
-GEMM_TRAFFIC_PER_LAUNCH = None
+# DRAM bytes (read + write) per launch of the tiled GEMM (the prefill GEMMs; decode runs the
+# streaming kernel): the mean over its 64 launches in one generation pass of this workload,
+# from an ncu capture of dram__bytes_read.sum and dram__bytes_write.sum; reset to None
+# whenever the GEMM kernel changes
+GEMM_TRAFFIC_PER_LAUNCH = 501274876
 
 
 def peaks():
