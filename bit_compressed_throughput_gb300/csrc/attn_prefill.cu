@@ -4,10 +4,14 @@
 // [FlexGen paper explainer, "Problem Formulation", Figure 2].  Prefill attends over the
 // fp16 K/V the projection just produced (the cache keeps the 4-bit copy for decoding).
 //
-// Flash-style: a CTA owns 64 query rows of one (sequence, head), 4 warps x 16 rows; K/V
-// tiles of 64 keys stream through a double-buffered cp.async ring; S = Q K^T and O += P V
-// run on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with an online base-2 softmax.
-// Q, K, V are read in place from the [rows][3h] QKV buffer.
+// Flash-style: a CTA owns 128 query rows of one (sequence, head), 8 warps x 16 rows, so each
+// K/V tile of 64 keys serves 128 rows; the tiles stream through a double-buffered cp.async
+// ring; S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with an
+// online base-2 softmax.  Q fragments are reloaded from shared memory for every tile rather
+// than held in registers, so a thread stays within 128 registers and two CTAs (16 warps)
+// share an SM.  A warp skips the key tiles that lie wholly above its rows (causal), and the
+// CTAs of the last query tiles, which see the most keys, are scheduled first.  Q, K, V are
+// read in place from the [rows][3h] QKV buffer.
 #include <math.h>
 
 #include "fg_common.cuh"
@@ -16,8 +20,9 @@
 namespace fg {
 namespace {
 
-constexpr int kRows = 64;      // query rows per CTA
+constexpr int kRows = 128;     // query rows per CTA
 constexpr int kKeys = 64;      // keys per tile
+constexpr int kWarpsA = kRows / 16;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;
@@ -52,12 +57,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 template <int D>
 struct Smem {
   static constexpr int LD = D + 8;                  // padded row (halves)
-  static constexpr int TILE = kRows * LD;           // halves per tile
-  static constexpr int BYTES = 5 * TILE * 2;        // Q, K[2], V[2]
+  static constexpr int QTILE = kRows * LD;          // halves of the Q tile
+  static constexpr int TILE = kKeys * LD;           // halves of a K or V tile
+  static constexpr int BYTES = (QTILE + 4 * TILE) * 2;   // Q, K[2], V[2]
 };
 
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kWarpsA * 32, 2)
 prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_log2,
                     uint16_t* __restrict__ out) {
   constexpr int LD = Smem<D>::LD;
@@ -66,20 +72,21 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
   pdl_launch_dependents();
   pdl_wait();
   uint16_t* sQ = sm;
-  uint16_t* sK = sm + TILE;            // 2 tiles
-  uint16_t* sV = sm + 3 * TILE;        // 2 tiles
+  uint16_t* sK = sm + Smem<D>::QTILE;  // 2 tiles
+  uint16_t* sV = sK + 2 * TILE;        // 2 tiles
 
-  const int qt = blockIdx.x, hd = blockIdx.y, seq = blockIdx.z;
+  // heaviest query tiles first
+  const int qt = gridDim.x - 1 - blockIdx.x, hd = blockIdx.y, seq = blockIdx.z;
   const int h = H * D;
   const int64_t row0 = (int64_t)seq * s;       // first row of this sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int q0 = qt * kRows;
 
-  // ---- async loads: a tile is 64 rows x D halves = 64 * D/8 16-byte chunks
-  auto load_tile = [&](uint16_t* dst, int col, int r0) {
+  // ---- async loads: a tile is `rows` rows x D halves = rows * D/8 16-byte chunks
+  auto load_tile = [&](uint16_t* dst, int col, int r0, int rows) {
     constexpr int CPR = D / 8;
-    for (int c = threadIdx.x; c < kRows * CPR; c += 128) {
+    for (int c = threadIdx.x; c < rows * CPR; c += kWarpsA * 32) {
       const int r = c / CPR, cc = c % CPR;
       const int pos = r0 + r;
       const bool valid = pos < s;
@@ -88,42 +95,39 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
                  valid);
     }
   };
-  load_tile(sQ, hd * D, q0);
-  load_tile(sK, h + hd * D, 0);
-  load_tile(sV, 2 * h + hd * D, 0);
+  load_tile(sQ, hd * D, q0, kRows);
+  load_tile(sK, h + hd * D, 0, kKeys);
+  load_tile(sV, 2 * h + hd * D, 0, kKeys);
   cp_commit();
 
-  const int nkt = min(qt + 1, (s + kKeys - 1) / kKeys);   // causal: tiles 0..qt
+  // causal: key tiles up to the one holding the CTA's last row
+  const int nkt = min((q0 + kRows - 1) / kKeys + 1, (s + kKeys - 1) / kKeys);
+  const int wrow_last = q0 + warp * 16 + 15;              // this warp's last row
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i)
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[i][c] = 0.0f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-  uint32_t qf[D / 16][4];
 
   for (int kt = 0; kt < nkt; ++kt) {
     const int buf = kt & 1;
     if (kt + 1 < nkt) {
-      load_tile(sK + (buf ^ 1) * TILE, h + hd * D, (kt + 1) * kKeys);
-      load_tile(sV + (buf ^ 1) * TILE, 2 * h + hd * D, (kt + 1) * kKeys);
+      load_tile(sK + (buf ^ 1) * TILE, h + hd * D, (kt + 1) * kKeys, kKeys);
+      load_tile(sV + (buf ^ 1) * TILE, 2 * h + hd * D, (kt + 1) * kKeys, kKeys);
     }
     cp_commit();
     cp_wait<1>();
     __syncthreads();
-    if (kt == 0) {
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int c = ks * 16 + 8 * (lane >> 4);
-        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(sQ + r * LD + c)), qf[ks][0],
-                qf[ks][1], qf[ks][2], qf[ks][3]);
-      }
+    // a tile whose first key lies past this warp's last row is fully masked for it
+    if (kt * kKeys > wrow_last) {
+      __syncthreads();   // the buffer is refilled by the next iteration's loads
+      continue;
     }
     const uint16_t* kb = sK + buf * TILE;
     const uint16_t* vb = sV + buf * TILE;
 
-    // ---- S = Q K^T for 16 rows x 64 keys
+    // ---- S = Q K^T for 16 rows x 64 keys (Q fragments from shared memory)
     float sc[kKeys / 8][4];
 #pragma unroll
     for (int nb = 0; nb < kKeys / 8; ++nb)
@@ -131,6 +135,13 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
       for (int c = 0; c < 4; ++c) sc[nb][c] = 0.0f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t qf[4];
+      {
+        const int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int c = ks * 16 + 8 * (lane >> 4);
+        ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(sQ + r * LD + c)), qf[0], qf[1],
+                qf[2], qf[3]);
+      }
 #pragma unroll
       for (int nb = 0; nb < kKeys / 8; nb += 2) {
         const int i = lane >> 3;
@@ -139,8 +150,8 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
         uint32_t b0, b1, b2, b3;
         ldsm_x4(static_cast<uint32_t>(__cvta_generic_to_shared(kb + key * LD + c)), b0, b1, b2,
                 b3);
-        mma16816(sc[nb], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-        mma16816(sc[nb + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+        mma16816(sc[nb], qf[0], qf[1], qf[2], qf[3], b0, b1);
+        mma16816(sc[nb + 1], qf[0], qf[1], qf[2], qf[3], b2, b3);
       }
     }
     // ---- mask (causal and sequence tail), online softmax in base 2
@@ -237,14 +248,14 @@ cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, in
     static cudaError_t attr = cudaFuncSetAttribute(
         prefill_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
     if (attr != cudaSuccess) return attr;
-    return launch_pdl(prefill_attn_kernel<128>, grid, dim3(128), Smem<128>::BYTES, st, qkv, s, H,
-                      sl2, out);
+    return launch_pdl(prefill_attn_kernel<128>, grid, dim3(kWarpsA * 32), Smem<128>::BYTES, st,
+                      qkv, s, H, sl2, out);
   } else {
     static cudaError_t attr = cudaFuncSetAttribute(
         prefill_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
     if (attr != cudaSuccess) return attr;
-    return launch_pdl(prefill_attn_kernel<64>, grid, dim3(128), Smem<64>::BYTES, st, qkv, s, H, sl2,
-                      out);
+    return launch_pdl(prefill_attn_kernel<64>, grid, dim3(kWarpsA * 32), Smem<64>::BYTES, st, qkv,
+                      s, H, sl2, out);
   }
 }
 
