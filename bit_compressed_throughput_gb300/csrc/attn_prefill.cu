@@ -54,6 +54,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 2^x on the special-function unit (inputs <= 0 here; results below 2^-126 flush to zero,
+// far below the fp16 P fed to the P V product).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
 struct Smem {
   static constexpr int LD = D + 8;                  // padded row (halves)
@@ -157,16 +165,29 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
     // ---- mask (causal and sequence tail), online softmax in base 2
     const int qrow[2] = {q0 + warp * 16 + gid, q0 + warp * 16 + gid + 8};
     float mx[2] = {-INFINITY, -INFINITY};
+    // only a tile reaching past this warp's first row, or past the sequence, needs the mask
+    if (kt * kKeys + kKeys - 1 > q0 + warp * 16 || kt * kKeys + kKeys > s) {
 #pragma unroll
-    for (int nb = 0; nb < kKeys / 8; ++nb) {
+      for (int nb = 0; nb < kKeys / 8; ++nb) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int key = kt * kKeys + nb * 8 + 2 * tig + (c & 1);
-        const int r = c >> 1;
-        float v = sc[nb][c] * scale_log2;
-        if (key > qrow[r] || key >= s) v = -INFINITY;
-        sc[nb][c] = v;
-        mx[r] = fmaxf(mx[r], v);
+        for (int c = 0; c < 4; ++c) {
+          const int key = kt * kKeys + nb * 8 + 2 * tig + (c & 1);
+          const int r = c >> 1;
+          float v = sc[nb][c] * scale_log2;
+          if (key > qrow[r] || key >= s) v = -INFINITY;
+          sc[nb][c] = v;
+          mx[r] = fmaxf(mx[r], v);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int nb = 0; nb < kKeys / 8; ++nb) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float v = sc[nb][c] * scale_log2;
+          sc[nb][c] = v;
+          mx[c >> 1] = fmaxf(mx[c >> 1], v);
+        }
       }
     }
     float corr[2];
@@ -175,7 +196,7 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
       const float m_new = fmaxf(m_run[r], mx[r]);
-      corr[r] = (m_run[r] == -INFINITY) ? 0.0f : exp2f(m_run[r] - m_new);
+      corr[r] = (m_run[r] == -INFINITY) ? 0.0f : ex2(m_run[r] - m_new);
       m_run[r] = m_new;
     }
     float ls[2] = {0.0f, 0.0f};
@@ -184,7 +205,7 @@ prefill_attn_kernel(const uint16_t* __restrict__ qkv, int s, int H, float scale_
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int r = c >> 1;
-        const float p = (m_run[r] == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - m_run[r]);
+        const float p = (m_run[r] == -INFINITY) ? 0.0f : ex2(sc[nb][c] - m_run[r]);
         sc[nb][c] = p;
         ls[r] += p;
       }
