@@ -443,6 +443,8 @@ int fg_dequant_gemm_q4_kv(const uint16_t* X, int64_t M, const fg_q4mat* W, const
   // Y = [Q | K | V]: three h-wide column blocks, each a whole number of 128-channel tiles
   if (W->N != 3 * (int64_t)kv->h || kv->h % 128 != 0) return FG_ERR_SHAPE;
   if (T <= 0 || pos < 0 || M != (int64_t)kv->B * T || M > (1ll << 31) - 1) return FG_ERR_SHAPE;
+  // the epilogues address cache slots (b*H + head)*cap + pos + t in 32 bits
+  if ((int64_t)kv->B * kv->H * kv->cap > (1ll << 31) - 1) return FG_ERR_SHAPE;
   if ((int64_t)pos + T > kv->cap) return FG_ERR_CAPACITY;
   if (M == 0) return FG_OK;
   if (!X || !Y || !aligned16(X) || !aligned16(Y) || (bias && !aligned16(bias))) return FG_ERR_ARG;

@@ -144,7 +144,7 @@ size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
  * and (a, b) as fg_kv_append_q4 gives for those rows) and written at position pos + t.
  * One launch (two when M is small enough for a split-K sum): the fp16 K/V are not read
  * back from memory.  h = kv->h, a multiple of 128; W->N == 3h; M == kv->B * T; T >= 1;
- * pos + T <= kv->cap.  Y is still written in full (prefill attention reads the fp16 K/V).
+ * pos + T <= kv->cap; kv->B * kv->H * kv->cap < 2^31.  Y is still written in full (prefill attention reads the fp16 K/V).
  * ws as for fg_dequant_gemm_q4.  Errors as fg_dequant_gemm_q4, plus FG_ERR_CAPACITY.
  * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": K/V grouped 64
  *  along the hidden dimension] */

@@ -38,6 +38,7 @@ def test_status_strings(fg):
 
 FAKE = 0x10000          # aligned, never dereferenced: validation fails before any use
 MISALIGNED = 0x10008
+FAKE2 = 0x20000         # a second aligned, never dereferenced address
 
 
 def q4(K, N, codes=FAKE, ab=FAKE):
@@ -71,6 +72,39 @@ def test_gemm_validation(fg):
     assert need > 0                                  # one tile of 256: split K
     assert call(q4(4096, 256), M=64, ws=FAKE, wsb=need - 1) == fg.FG_ERR_WORKSPACE
     assert fg.fg_gemm_workspace_bytes(8192, 4096, 12288) == 0      # full grid: no split
+
+
+def test_fused_gemm_validation(fg):
+    """The QKV + K/V-append and GEMM + LayerNorm entries reject bad calls on the host."""
+    L = fg.lib
+    kv = kvs(B=4, cap=16, h=256, H=2)
+    w3 = q4(256, 768)
+    kvcall = lambda W=w3, M=4, T=1, pos=0, k=kv, X=FAKE, Y=FAKE: \
+        L.fg_dequant_gemm_q4_kv(X, M, C.byref(W), None, Y, C.byref(k), T, pos, None, 0, None)
+    assert kvcall(W=q4(256, 512)) == fg.FG_ERR_SHAPE            # N != 3h
+    assert kvcall(M=3) == fg.FG_ERR_SHAPE                       # M != B*T
+    assert kvcall(T=0, M=0) == fg.FG_ERR_SHAPE
+    assert kvcall(pos=16) == fg.FG_ERR_CAPACITY                 # pos + T > cap
+    assert kvcall(k=kvs(B=1 << 16, cap=1 << 14, h=256, H=2), M=1 << 16) == fg.FG_ERR_SHAPE
+    assert kvcall(X=MISALIGNED) == fg.FG_ERR_ARG
+    lncall = lambda M=4, Y=FAKE, Yln=FAKE2, g=FAKE, eps=1e-5, epi=0: \
+        L.fg_dequant_gemm_q4_ln(FAKE, M, C.byref(q4(256, 256)), None, epi, None, Y, g, FAKE,
+                                eps, Yln, None, 0, None)
+    assert lncall(Yln=FAKE) == fg.FG_ERR_ARG                    # Y_ln aliases Y
+    assert lncall(g=None) == fg.FG_ERR_ARG
+    assert lncall(eps=0.0) == fg.FG_ERR_ARG
+    assert lncall(epi=fg.FG_EPI_RESIDUAL) == fg.FG_ERR_ARG      # residual missing
+    assert L.fg_dequant_gemm_q4_ln(FAKE, 4, C.byref(q4(256, 16640)), None, 0, None, FAKE, FAKE,
+                                   FAKE, 1e-5, FAKE2, None, 0, None) == fg.FG_ERR_SHAPE  # N > 16384
+    tk = kvs(B=2, cap=64, h=256, H=2)
+    topk = lambda length=32, k=4, ws=FAKE, wsb=1 << 30: \
+        L.fg_decode_attn_q4kv_topk(FAKE, 256, C.byref(tk), length, k, 0.1, FAKE, None, ws, wsb,
+                                   None)
+    assert topk(k=0) == fg.FG_ERR_SHAPE
+    assert topk(k=33) == fg.FG_ERR_SHAPE                        # k > len
+    assert topk(length=65) == fg.FG_ERR_CAPACITY
+    assert topk(wsb=L.fg_decode_attn_topk_workspace_bytes(C.byref(tk), 32) - 1) \
+        == fg.FG_ERR_WORKSPACE
 
 
 def kvs(B=2, cap=32, h=256, H=2):
