@@ -15,7 +15,9 @@
 //            through its shared-memory ring, the scores on the tensor cores in base 2, each
 //            written as an order-preserving key, and each work item's online-softmax state
 //            (reference maximum m, sum l) kept for the denominator
-//   topk_attend_kernel  one warp per (b, hd): the softmax denominator from the work items'
+//   topk_attend_kernel  one warp per (b, hd), no barriers (29 independent warps per SM,
+//                       which this latency-bound work needs): the softmax denominator from
+//                       the work items'
 //                       (m, l); the keys once into shared memory; the k-th largest key by
 //                       radix selection, eight bits per round from the top (a 256-bin
 //                       histogram of the keys that share the bits found so far, then the bin
