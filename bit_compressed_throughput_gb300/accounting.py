@@ -76,6 +76,13 @@ def decode_attn_bytes(B: int, length: int, h: int) -> float:
     return 2.0 * q4_bytes(B * length * h) + 4.0 * B * h
 
 
+def decode_attn_topk_bytes(B: int, H: int, length: int, k: int, h: int) -> float:
+    """Top-K decode attention: the whole INT4 K, the INT4 V of the k kept positions per
+    head, a 4-byte score key written and read back per position and head, q in and out."""
+    return (q4_bytes(B * length * h) + q4_bytes(B * k * h) + 8.0 * B * H * length
+            + 4.0 * B * h)
+
+
 def decode_attn_flops(B: int, length: int, h: int) -> float:
     return 4.0 * B * length * h
 

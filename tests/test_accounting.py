@@ -3,6 +3,8 @@ print (tests/golden/flexgen_closed_forms.json, each entry cited there)."""
 import json
 import os
 
+import pytest
+
 from bit_compressed_throughput_gb300 import accounting as A
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
@@ -49,3 +51,15 @@ def test_average_kv_over_decoding():
     bls, s, n, h1 = 8, 512, 32, 64
     exact = sum(4.0 * bls * (s + t) * h1 for t in range(n + 1)) / (n + 1)
     assert abs(A.kv_cache_bytes_avg_decode(bls, s, n, h1) - exact) / exact < 1e-12
+
+
+def test_topk_attention_bytes():
+    # keeping every position reads what dense attention reads, plus the score keys; keeping
+    # a tenth saves 90% of the V bytes (the KV-dominated workload: 512 x 56 heads x 1056)
+    B, H, d, T = 512, 56, 128, 1056
+    h = H * d
+    dense = A.decode_attn_bytes(B, T, h)
+    assert A.decode_attn_topk_bytes(B, H, T, T, h) == pytest.approx(dense + 8.0 * B * H * T)
+    v = A.q4_bytes(B * T * h)
+    saved = dense + 8.0 * B * H * T - A.decode_attn_topk_bytes(B, H, T, 106, h)
+    assert saved == pytest.approx(v * (1 - 106 / T))
