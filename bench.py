@@ -65,8 +65,10 @@ def dist_env():
 
 
 def workload_desc(wl):
+    scale = getattr(wl, "layer_scale", 1.0)
+    tail = (f", time x{scale:g} for the whole stack ({wl.L} layers run)" if scale != 1.0 else "")
     return (f"{wl.name}: h{wl.h} H{wl.H}x{wl.d} f{wl.f} L{wl.L} B{wl.B} (g{wl.g} m{wl.m}) "
-            f"s{wl.s} n{wl.n}, int4 g64 weights + KV, fp16 compute")
+            f"s{wl.s} n{wl.n}, int4 g64 weights + KV, fp16 compute{tail}")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -282,7 +284,10 @@ def run_gpu(args, wl):
     a_ = prof["q4kv_decode_attn"]
     attn_gbs = a_["work"] / (a_["ms"] * 1e-3) / 1e9 if a_["ms"] else None
     total_kernel_ms = sum(p["ms"] for p in prof.values())
-    value = replicas.total_tokens(world, wl.B, wl.n, args.steps) / (ms * 1e-3)
+    # a workload that keeps a slice of its layers resident reports its time scaled to the
+    # whole stack (the 175B shape: 8 of 96 layers, time x 96/8)
+    scale = getattr(wl, "layer_scale", 1.0)
+    value = replicas.total_tokens(world, wl.B, wl.n, args.steps) / (ms * 1e-3 * scale)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
@@ -319,7 +324,7 @@ def run_gpu(args, wl):
         "eager_ms_per_step": round(ms_eager / args.steps, 3),
         "gpu_launches": launches,
         "e2e": {"value": round(replicas.total_tokens(world, wl.B, wl.n, args.steps)
-                               / (ms_e2e * 1e-3), 2),
+                               / (ms_e2e * 1e-3 * scale), 2),
                 "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
     }
@@ -362,7 +367,7 @@ def cpu_baseline(wl, samples=1):
     layer of the workload (prefill + n-1 decode steps), scaled to the L-layer stack."""
     layers = oracle_setup(wl, 1)
     secs = [oracle_sample_step(wl, layers, s) for s in range(samples)]
-    per_seq_stack = statistics.mean(secs) * wl.L
+    per_seq_stack = statistics.mean(secs) * wl.L * getattr(wl, "layer_scale", 1.0)
     return {"value": round(wl.n / per_seq_stack, 4), "unit": UNIT, "cores": cores(),
             "kind": "oracle",
             "sample": f"1 sequence x 1 layer of {wl.name} (prefill {wl.s} + {wl.n - 1} decode "
@@ -377,7 +382,8 @@ def run_reference(args, wl):
     for i in range(args.warmup):
         oracle_sample_step(wl, layers, i)
     t = sum(oracle_sample_step(wl, layers, args.warmup + i) for i in range(args.steps))
-    per_step = t / args.steps * wl.L          # one sequence through the L-layer stack
+    # one sequence through the L-layer stack (scaled to the whole stack as the GPU arm is)
+    per_step = t / args.steps * wl.L * getattr(wl, "layer_scale", 1.0)
     value = wl.n / per_step
     cb = {"value": round(value, 4), "unit": UNIT, "cores": cores(), "kind": "oracle",
           "sample": f"each step: 1 sequence x 1 layer of {wl.name} (prefill {wl.s} + "
