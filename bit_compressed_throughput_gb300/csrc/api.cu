@@ -40,6 +40,8 @@ struct DevInfo {
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
 
+}  // namespace
+
 int check_device(int* sms_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -64,6 +66,8 @@ int check_device(int* sms_out) {
   if (sms_out) *sms_out = di.sms;
   return FG_OK;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- profiling
 struct ProfRec {
@@ -153,6 +157,8 @@ int check_q4mat(const fg_q4mat* W) {
   return FG_OK;
 }
 
+}  // namespace
+
 int check_kv(const fg_kvcache* kv) {
   if (!kv || !kv->k_codes || !kv->v_codes || !kv->k_ab || !kv->v_ab) return FG_ERR_ARG;
   if (!aligned16(kv->k_codes) || !aligned16(kv->v_codes) || !aligned16(kv->k_ab) ||
@@ -166,6 +172,25 @@ int check_kv(const fg_kvcache* kv) {
   if (d != 64 && d != 128) return FG_ERR_SHAPE;
   return FG_OK;
 }
+
+int check_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,
+                      float scale, const uint16_t* out, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  int rc = check_kv(kv);
+  if (rc) return rc;
+  if (len <= 0) return FG_ERR_SHAPE;
+  if (len > kv->cap) return FG_ERR_CAPACITY;
+  if (q_stride < kv->h || q_stride % 8 != 0) return FG_ERR_SHAPE;
+  if (!(scale > 0.0f) || !isfinite(scale)) return FG_ERR_ARG;
+  if (kv->B == 0) {
+    *nothing_to_do = true;
+    return FG_OK;
+  }
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return FG_ERR_ARG;
+  return FG_OK;
+}
+
+namespace {
 
 int check_dims(const fg_dims* dm) {
   if (!dm) return FG_ERR_ARG;
@@ -278,6 +303,8 @@ int run_kv_append(const uint16_t* k, const uint16_t* v, int64_t stride, int T, i
   return FG_OK;
 }
 
+}  // namespace
+
 int run_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv, int len,
                     float scale, uint16_t* out, void* ws, int sms, cudaStream_t st) {
   Span sp(st);
@@ -296,6 +323,8 @@ int run_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv, i
   }
   return FG_OK;
 }
+
+namespace {
 
 int run_prefill_attn(const uint16_t* qkv, int nseq, int s, int H, int d, float scale,
                      uint16_t* out, cudaStream_t st) {
@@ -501,14 +530,9 @@ size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len) {
 
 int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,
                         float scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
-  int rc = check_kv(kv);
-  if (rc) return rc;
-  if (len <= 0) return FG_ERR_SHAPE;
-  if (len > kv->cap) return FG_ERR_CAPACITY;
-  if (q_stride < kv->h || q_stride % 8 != 0) return FG_ERR_SHAPE;
-  if (!(scale > 0.0f) || !isfinite(scale)) return FG_ERR_ARG;
-  if (kv->B == 0) return FG_OK;
-  if (!q || !out || !aligned16(q) || !aligned16(out)) return FG_ERR_ARG;
+  bool noop = false;
+  int rc = check_decode_attn(q, q_stride, kv, len, scale, out, &noop);
+  if (rc || noop) return rc;
   const size_t need = fg_decode_attn_workspace_bytes(kv, len);
   if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return FG_ERR_WORKSPACE;
   int sms = 0;
@@ -590,7 +614,7 @@ static int check_layer(const fg_dims* dm, const fg_layer* L) {
   return FG_OK;
 }
 
-size_t fg_layer_workspace_bytes(const fg_dims* dm, int32_t g, int32_t m, int32_t s_max) {
+size_t fg_workspace_bytes(const fg_dims* dm, int32_t g, int32_t m, int32_t s_max) {
   if (!dm || check_dims(dm) != FG_OK || g <= 0 || m <= 0 || s_max <= 0) return 0;
   const int64_t Mp = (int64_t)g * s_max;       // prefill rows per GPU batch
   const int64_t Md = (int64_t)g * m;           // decode rows (whole block)
@@ -603,6 +627,10 @@ size_t fg_layer_workspace_bytes(const fg_dims* dm, int32_t g, int32_t m, int32_t
     best = std::max(best, layer_ws(*dm, Md, &kv, len).total);
   best = std::max(best, layer_ws(*dm, Md, &kv, s_max).total);
   return best;
+}
+
+size_t fg_layer_workspace_bytes(const fg_dims* dm, int32_t g, int32_t m, int32_t s_max) {
+  return fg_workspace_bytes(dm, g, m, s_max);
 }
 
 int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const uint16_t* x,

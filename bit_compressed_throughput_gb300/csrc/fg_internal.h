@@ -46,6 +46,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Message returned by fg_last_error() on this thread.
 void set_last_error(const std::string& msg);
 
+// Host validation shared by the entry points (FG_OK or a negative fg_status; no CUDA call
+// except in check_device).  check_device: the current device is sm_103; *sms_out receives
+// its SM count capped at kMaxSms.  check_decode_attn: the arguments of a decode-attention
+// call; *nothing_to_do is set when the cache holds no sequences.
+int check_device(int* sms_out);
+int check_kv(const fg_kvcache* kv);
+int check_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,
+                      float scale, const uint16_t* out, bool* nothing_to_do);
+// Decode attention with per-kernel event timing (when profiling is on); ws holds at least
+// decode_attn_ws_bytes(kv, len, sms) bytes.  Returns FG_OK or FG_ERR_CUDA.
+int run_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv, int len,
+                    float scale, uint16_t* out, void* ws, int sms, cudaStream_t st);
+
 // Decode attention: number of sequence splits used for (kv, len); workspace bytes.
 int decode_attn_splits(const fg_kvcache& kv, int32_t len, int num_sms);
 size_t decode_attn_ws_bytes(const fg_kvcache& kv, int32_t len, int num_sms);

@@ -76,6 +76,7 @@ _SIGS = {
                           _I32, _I32, _I32, _P, _SZ, _P], C.c_int),
     "fg_layer_decode": ([C.POINTER(fg_dims), C.POINTER(fg_layer), C.POINTER(fg_kvcache), _P, _P,
                          _I32, _I32, _I32, _P, _SZ, _P], C.c_int),
+    "fg_workspace_bytes": ([C.POINTER(fg_dims), _I32, _I32, _I32], _SZ),
     "fg_layer_workspace_bytes": ([C.POINTER(fg_dims), _I32, _I32, _I32], _SZ),
     "fg_status_string": ([C.c_int], C.c_char_p),
     "fg_last_error": ([], C.c_char_p),
@@ -305,9 +306,13 @@ def fg_layernorm(x, gamma, beta, eps: float, y, stream=None):
                                             _ptr(y), _stream(stream)))
 
 
-def fg_layer_workspace_bytes(layer: LayerQ4, g: int, m: int, s_max: int) -> int:
+def fg_workspace_bytes(layer: LayerQ4, g: int, m: int, s_max: int) -> int:
+    """Scratch bytes of fg_layer_prefill / fg_layer_decode for this layer's dims."""
     dm = layer.dims()
-    return int(lib.fg_layer_workspace_bytes(C.byref(dm), g, m, s_max))
+    return int(lib.fg_workspace_bytes(C.byref(dm), g, m, s_max))
+
+
+fg_layer_workspace_bytes = fg_workspace_bytes
 
 
 def fg_layer_prefill(layer: LayerQ4, cache: KVCacheQ4, x, y, g: int, m: int, s: int, ws,
@@ -359,7 +364,7 @@ class StackEngine:
         L0 = layers[0]
         self.B = g * m
         self.caches = [KVCacheQ4(self.B, cap, L0.h, L0.H, device) for _ in layers]
-        wsb = max(fg_layer_workspace_bytes(L, g, m, max(s_max, cap)) for L in layers)
+        wsb = max(fg_workspace_bytes(L, g, m, max(s_max, cap)) for L in layers)
         self.ws = torch.empty((wsb + 255) // 256 * 256, dtype=torch.uint8, device=device)
 
     def prefill(self, x, y, s: int, stream=None):

@@ -135,6 +135,9 @@ int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64
 int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
                        int epilogue, const uint16_t* residual, uint16_t* Y, void* ws,
                        size_t ws_bytes, void* stream);
+/* Scratch bytes fg_dequant_gemm_q4 needs for an M x K by K x N product (split-K fp32
+ * partials when M is small; 0 when the plan does not split).  Host computation only; the
+ * pages have no counterpart (their GEMMs run in PyTorch). */
 size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* The QKV projection with the KV quantise-and-append in its epilogue:
@@ -191,6 +194,8 @@ int fg_kv_append_q4(const uint16_t* k_new, const uint16_t* v_new, int64_t row_st
  *  over the KV cache] */
 int fg_decode_attn_q4kv(const uint16_t* q, int64_t q_stride, const fg_kvcache* kv, int32_t len,
                         float scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+/* Scratch bytes fg_decode_attn_q4kv needs (split-sequence partials, planned for up to 192
+ * SMs; 0 when no split is planned).  Host computation only; no counterpart on the pages. */
 size_t fg_decode_attn_workspace_bytes(const fg_kvcache* kv, int32_t len);
 
 /* Decode attention exactly as fg_decode_attn_q4kv, for callers that cannot allocate
@@ -236,7 +241,10 @@ int fg_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, int
 /* ---------------------------------------------------------------------- LayerNorm */
 
 /* y[rows][h] = (x - mean) / sqrt(var + eps) * gamma + beta, fp32 statistics (population
- * variance), fp16 in and out.  h % 64 == 0, h <= 16384.  (Pre-LN of the OPT layer.) */
+ * variance), fp16 in and out.  x, gamma, beta, y: device fp16 (gamma, beta [h]); h % 64
+ * == 0, h <= 16384, eps > 0; rows == 0 is a no-op.  The pages name no normalisation: this
+ * is the pre-LN of the OPT decoder layer the workloads specify (LN1 before attention, LN2
+ * before the MLP); the pages have no counterpart of the call itself. */
 int fg_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* gamma,
                  const uint16_t* beta, float eps, uint16_t* y, void* stream);
 
@@ -262,8 +270,16 @@ int fg_layer_decode(const fg_dims* dims, const fg_layer* layer, fg_kvcache* kv,
                     const uint16_t* x, uint16_t* y, int32_t g, int32_t m, int32_t pos,
                     void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace for fg_layer_prefill with prompts up to s_max, and for fg_layer_decode with
- * caches up to s_max positions (the larger of the two uses). */
+/* Workspace bytes for fg_layer_prefill with prompts up to s_max and for fg_layer_decode
+ * with caches up to s_max positions (the larger of the two uses): per GPU batch of g
+ * sequences the LayerNorm output, the [g*s][3h] QKV, the attention output, h1 and the
+ * [g*s][f] FFN activation, plus GEMM split-K partials and, for decode over the whole block
+ * of g*m sequences, the split-sequence attention partials.  Returns 0 for invalid dims
+ * or g, m, s_max <= 0.  A pure host computation (no CUDA call).
+ * [FlexGen paper explainer, "Compute Schedule": a layer runs over every GPU batch of the
+ *  block, so the scratch is sized by g, m and the sequence length, not by the stack] */
+size_t fg_workspace_bytes(const fg_dims* dims, int32_t g, int32_t m, int32_t s_max);
+/* The same value as fg_workspace_bytes, under the name of the layer calls it sizes. */
 size_t fg_layer_workspace_bytes(const fg_dims* dims, int32_t g, int32_t m, int32_t s_max);
 
 /* ---------------------------------------------------------------------- runtime */

@@ -28,6 +28,20 @@ def test_exports_every_declared_symbol(fg):
     assert len(names) >= 19
     missing = [n for n in names if not hasattr(fg.lib, n)]
     assert missing == []
+    # the boundary's calls by the names the scope table gives them
+    for n in ("fg_quantize_g64", "fg_dequant_gemm_q4", "fg_kv_append_q4", "fg_decode_attn_q4kv",
+              "fg_layer_prefill", "fg_layer_decode", "fg_workspace_bytes", "fg_status_string"):
+        assert n in names, n
+
+
+def test_workspace_bytes_names_agree(fg):
+    for h, H, f, g, m, s in ((256, 4, 1024, 2, 2, 20), (4096, 32, 16384, 16, 4, 544),
+                             (7168, 56, 0, 128, 4, 1056)):
+        dm = fg.fg_dims(h, H, h // H, f, 1e-5)
+        a = fg.lib.fg_workspace_bytes(fg.C.byref(dm), g, m, s)
+        assert a > 0 and a == fg.lib.fg_layer_workspace_bytes(fg.C.byref(dm), g, m, s)
+    bad = fg.fg_dims(100, 4, 25, 0, 1e-5)
+    assert fg.lib.fg_workspace_bytes(fg.C.byref(bad), 2, 2, 16) == 0
 
 
 def test_status_strings(fg):

@@ -259,3 +259,100 @@ def test_planted_layer_mistakes_are_caught():
     finally:
         OL._mlp_and_residual = orig_mlp
     assert not np.allclose(good, bad, rtol=1e-6, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- the stack
+
+
+def stack_loop(layers, wl, xp, xs):
+    """The generation loop in pure Python, one sequence and one token at a time: prefill
+    runs layer l over the prompt rows that layer l-1 produced; decode step t feeds
+    x_steps[t-1] to layer 0 and each layer's output to the next, at cache length
+    s + t - 1; each layer keeps its own K/V rows (fp16 in prefill, the restored 4-bit
+    cache in decode) (FlexGen paper explainer, "Compute Schedule" and Algorithm 1: every
+    layer over the block, then the next layer; readings R5, R9, R10)."""
+    S_, s, h = xp.shape
+    zero = [[0.0] * h]
+    prefill = [[None] * s for _ in range(S_)]
+    steps = [[None] * S_ for _ in range(xs.shape[0])]
+    for b in range(S_):
+        rows16 = [[] for _ in layers]          # per layer: fp16 (k, v) rows by position
+        ys = [tolist(xp[b, i]) for i in range(s)]
+        for l, L in enumerate(layers):
+            for i in range(s):
+                _, qkv = layer_loop(L, wl, ys[i], zero, zero)
+                rows16[l].append((np.array(qkv[h:2 * h]).astype(np.float16),
+                                  np.array(qkv[2 * h:]).astype(np.float16)))
+            K = [r[0].astype(np.float64).tolist() for r in rows16[l]]
+            V = [r[1].astype(np.float64).tolist() for r in rows16[l]]
+            ys = [layer_loop(L, wl, ys[i], K[:i + 1], V[:i + 1])[0] for i in range(s)]
+        prefill[b] = ys
+        for t in range(1, xs.shape[0] + 1):
+            y = tolist(xs[t - 1, b])
+            for l, L in enumerate(layers):
+                _, qkv = layer_loop(L, wl, y, zero, zero)
+                rows16[l].append((np.array(qkv[h:2 * h]).astype(np.float16),
+                                  np.array(qkv[2 * h:]).astype(np.float16)))
+                assert len(rows16[l]) == s + t           # positions 0 .. s+t-1
+                khat = Q.dequant_g64(*Q.quantize_g64(np.stack([r[0] for r in rows16[l]])))
+                vhat = Q.dequant_g64(*Q.quantize_g64(np.stack([r[1] for r in rows16[l]])))
+                y, _ = layer_loop(L, wl, y, tolist(khat), tolist(vhat))
+            steps[t - 1][b] = y
+    return np.array(prefill), np.array(steps)
+
+
+def _stack_case():
+    wl = fg_synth.WORKLOADS["tiny"].with_(h=128, H=2, d=64, f=128, s=3, n=3, g=1, m=2, L=2)
+    layers = [OL.QuantLayer(fg_synth.layer_params(wl, l, True), wl.H, wl.d, wl.ln_eps)
+              for l in range(wl.L)]
+    return wl, layers, fg_synth.prompt_states(wl), fg_synth.step_states(wl)
+
+
+def test_run_stack_matches_pure_python_loop():
+    wl, layers, xp, xs = _stack_case()
+    assert xs.shape[0] == 2 and len(layers) == 2
+    out = OL.run_stack(layers, xp, xs, cap=wl.cap)
+    pre, st = stack_loop(layers, wl, xp, xs)
+    assert np.allclose(out["prefill"], pre, rtol=1e-10, atol=1e-10)
+    assert np.allclose(out["steps"], st, rtol=1e-10, atol=1e-10)
+    # the layers differ, so a stack that ran one of them twice would not agree
+    assert not np.allclose(layers[0].w_hat["wqkv"], layers[1].w_hat["wqkv"])
+
+
+def test_planted_stack_mistakes_are_caught():
+    """Mistakes planted in the oracle's loop (on the CPU) that the pure-Python loop must
+    catch: every layer fed the stack's input instead of the previous layer's output, and
+    decode appending one position too far."""
+    wl, layers, xp, xs = _stack_case()
+    pre, st = stack_loop(layers, wl, xp, xs)
+
+    orig_pre, orig_dec = OL.layer_prefill, OL.layer_decode
+    first = {}
+
+    def pre_fed_input(L, x, cache, dt=np.float64):
+        if L is layers[0]:
+            first["p"] = x
+        return orig_pre(L, first["p"], cache, dt)
+
+    def dec_fed_input(L, x, cache, pos, dt=np.float64):
+        if L is layers[0]:
+            first["d"] = x
+        return orig_dec(L, first["d"], cache, pos, dt)
+
+    def dec_shifted(L, x, cache, pos, dt=np.float64):
+        return orig_dec(L, x, cache, pos + 1, dt)
+
+    try:
+        OL.layer_prefill = pre_fed_input
+        bad = OL.run_stack(layers, xp, xs, cap=wl.cap + 1)
+        assert not np.allclose(bad["prefill"], pre, rtol=1e-6, atol=1e-6)
+        OL.layer_prefill = orig_pre
+        OL.layer_decode = dec_fed_input
+        bad = OL.run_stack(layers, xp, xs, cap=wl.cap + 1)
+        assert np.allclose(bad["prefill"], pre, rtol=1e-10, atol=1e-10)
+        assert not np.allclose(bad["steps"], st, rtol=1e-6, atol=1e-6)
+        OL.layer_decode = dec_shifted
+        bad = OL.run_stack(layers, xp, xs, cap=wl.cap + 1)
+        assert not np.allclose(bad["steps"], st, rtol=1e-6, atol=1e-6)
+    finally:
+        OL.layer_prefill, OL.layer_decode = orig_pre, orig_dec
