@@ -6,16 +6,20 @@ whole block (FlexGen's block schedule).  tokens per step = B * n (the prefill yi
 first token; FlexGen paper explainer, "Analytical Cost Model": T = Tpre*l + Tgen*(n-1)*l;
 throughput = generated tokens / (prefill + decode) time, FlexGen review (jaehun.me)).
 
-Default workload: OPT-6.7B-shaped stack (hidden 4096, 32 heads x 128, FFN 16384, 4
-layers, B = 64 = 16 x 4, prompt 512, 32 generated tokens), weights N(0, 0.02) and KV
-cache in 4-bit groups of 64.  Inputs are seeded synthetic hidden states N(0, 1).
+Default workload: the OPT-175B-shaped stack, the largest configuration that fits one GPU
+(hidden 12288, 96 heads x 128, FFN 49152, B = 144 = 36 x 4, prompt 512, 32 generated
+tokens), 8 layers resident with the time scaled by 96/8 to the whole stack, weights
+N(0, 0.02) and KV cache in 4-bit groups of 64; inputs are seeded synthetic hidden states
+N(0, 1).  The other workloads (OPT-6.7B, OPT-30B and the KV-dominated decode) run after
+it for a few steps each and are reported under ``per_config``; the KV-dominated one gives
+the metric's second half, decode-attention HBM GB/s as a fraction of peak.
 
-`value` times K steps replayed from one CUDA graph (inputs resident in HBM);
-per-kernel roofline figures come from an eager pass over the same K steps with CUDA
-events around every launch.  `e2e` times the same K steps with every step's inputs copied from
-pinned host memory and its generated hidden states copied back inside the timed region, the
-copies of neighbouring steps overlapping the compute on their own streams.
-`--impl reference` times the CPU oracle on a bounded sample of the same workload.
+`value` times K steps replayed from one CUDA graph (inputs resident in HBM); per-kernel
+roofline figures come from eager passes (prefill and decode apart) with CUDA events around
+every launch.  `e2e` times K steps with every step's inputs copied from pinned host memory
+and its generated hidden states copied back inside the timed region, the copies of
+neighbouring steps overlapping the compute on their own streams.  `--impl reference` and
+`cpu_baseline` time the CPU oracle on a bounded sample of the same workload.
 
 Multi-GPU (torchrun): every rank runs its own block of sequences (sequences never
 interact, so there is no data-path collective); `value` is all ranks' tokens over the
@@ -42,11 +46,17 @@ from bit_compressed_throughput_gb300 import replicas  # noqa: E402
 
 METRIC = "generated tokens/s per OPT-shaped layer stack at 1 GB300; decode-attn HBM GB/s % peak"
 UNIT = "tokens/s"
-# DRAM bytes (read + write) per launch of the tiled GEMM (the prefill GEMMs; decode runs the
-# streaming kernel): the mean over its 64 launches in one generation pass of this workload,
-# from an ncu capture of dram__bytes_read.sum and dram__bytes_write.sum; reset to None
-# whenever the GEMM kernel changes
-GEMM_TRAFFIC_PER_LAUNCH = 501274876
+DEFAULT_CONFIG = "opt-175b"
+SUB_CONFIGS = ("opt-6.7b", "opt-30b", "kv-decode")
+# Nominal GB300 figures (context for the measured-peak fractions): HBM3e 7.9 TB/s, dense
+# fp16/bf16 tensor 2.25 PFLOP/s
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_F16_TFLOPS = 2250.0
+# DRAM bytes (read + write) per launch of the tiled GEMM, by workload: from one-kernel ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum) of the workload's prefill GEMM
+# shapes, averaged over one pass's launch mix; a workload without a capture of the current
+# kernel reports null
+GEMM_TRAFFIC_PER_LAUNCH = {}
 
 
 def peaks():
@@ -139,6 +149,7 @@ def build_stack(wl, device, seed_offset=0):
                     wl.outlier_frac * K)))]
                 w[rows] *= wl.outlier_scale
             params[name] = w.half()
+            del w
         h, f = wl.h, wl.f
         params.update({"bqkv": torch.zeros(3 * h), "bo": torch.zeros(h), "ln1_g": torch.ones(h),
                        "ln1_b": torch.zeros(h), "ln2_g": torch.ones(h), "ln2_b": torch.zeros(h)})
@@ -167,11 +178,17 @@ class Runner:
                                device=device)                          # decode outputs
         self.graph = None
 
-    def step(self):
+    def prefill(self):
+        self.eng.prefill(self.x, self.y, self.wl.s)
+
+    def decode_all(self):
         wl = self.wl
-        self.eng.prefill(self.x, self.y, wl.s)
         for t in range(1, wl.n):
             self.eng.decode(self.xs[t - 1], self.out[t - 1], wl.s + t - 1)
+
+    def step(self):
+        self.prefill()
+        self.decode_all()
 
     def capture(self):
         import torch
@@ -272,10 +289,145 @@ def cost_model_line(wl, value):
             "peaks": "measured HBM copy and sustained bf16"}
 
 
+def profile_phase(fg, fn, steps):
+    """Per-kernel launches, milliseconds and algorithmic work of `steps` eager runs of fn
+    (CUDA events around every launch on its stream)."""
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    ms = time_region(fn, steps)
+    fg.fg_prof_enable(False)
+    return ms, {fg.KINDS[k]: fg.fg_prof_query(k) for k in range(len(fg.KINDS))}
+
+
+def roof(kernel, p, pk, bound, steps, extra=None):
+    """Roofline entry of one kernel kind from its profile record: achieved = algorithmic
+    work / event time, against the measured peak (copy bandwidth, or sustained bf16 for a
+    kernel timed inside a long pass) and against the nominal one."""
+    if not p or not p["launches"] or not p["ms"]:
+        return None
+    if bound == "hbm":
+        a, unit, peak, nom = p["work"] / (p["ms"] * 1e-3) / 1e9, "GB/s", pk["hbm_gbs"], \
+            NOMINAL_HBM_GBS
+        src = f"{pk['source']} HBM copy"
+    else:
+        a, unit, peak, nom = p["work"] / (p["ms"] * 1e-3) / 1e12, "TFLOP/s", \
+            pk["bf16_sustained"], NOMINAL_F16_TFLOPS
+        src = f"{pk['source']} bf16 sustained (fp16 dense rate equal)"
+    r = {"kernel": kernel, "bound": bound, "achieved": round(a, 1), "peak": peak, "unit": unit,
+         "frac": round(a / peak, 4), "peak_source": src, "peak_nominal": nom,
+         "frac_of_nominal": round(a / nom, 4), "launches_per_step": p["launches"] // steps,
+         "ms_per_step": round(p["ms"] / steps, 3)}
+    if extra:
+        r.update(extra)
+    return r
+
+
+def kernel_table(prof, steps):
+    return {k: {"launches_per_step": v["launches"] // steps, "ms_per_step": round(v["ms"] / steps, 3)}
+            for k, v in prof.items() if v["launches"]}
+
+
+def phase_rooflines(wl, pre, dec, pk, psteps):
+    """Rooflines of the prefill and decode kernels of one workload."""
+    out = {"prefill_gemm": roof("q4_dequant_gemm_tc", pre["q4_dequant_gemm_tc"], pk, "tensor",
+                                psteps),
+           "prefill_attn": roof("prefill_attn", pre["prefill_attn"], pk, "tensor", psteps),
+           "decode_attn": roof("q4kv_decode_attn", dec["q4kv_decode_attn"], pk, "hbm", psteps,
+                               {"lengths": f"{wl.s + 1}..{wl.s + wl.n - 1}",
+                                "sequences_x_heads": wl.B * wl.H})}
+    ds = dec["q4_dequant_gemm_stream"]
+    dt = dec["q4_dequant_gemm_tc"]
+    if ds["launches"]:
+        out["decode_gemm"] = roof("q4_dequant_gemm_stream", ds, pk, "hbm", psteps,
+                                  {"M": wl.B, "kernel_kind": "weight-streaming (M <= 128)"})
+    if dt["launches"]:
+        # M = B tokens: 3.56*M flop per weight byte, above the ridge for M >= 144
+        wb = 0.5625 * (4 * wl.h * wl.h + 2 * wl.h * wl.f) * wl.L * (wl.n - 1) * psteps
+        out["decode_gemm"] = roof("q4_dequant_gemm_tc", dt, pk, "tensor", psteps,
+                                  {"M": wl.B, "kernel_kind": "tiled (M > 128)",
+                                   "weight_gbs": round(wb / (dt["ms"] * 1e-3) / 1e9, 1)})
+    return out
+
+
+def run_config(wl, device, steps, warmup, dist=None, rank=0, full=False, pk=None):
+    """Build one workload's stack on the device and time it: the graph-replayed pass,
+    eager per-kernel profiles of prefill and decode, and (full) the e2e pass with host I/O."""
+    import torch
+    from bit_compressed_throughput_gb300 import fg
+    layers, x, xs = build_stack(wl, device, seed_offset=rank)
+    run = Runner(wl, layers, x, xs, device)
+    for _ in range(warmup):
+        run.step()
+    torch.cuda.synchronize()
+    fg.fg_check_device_error()
+    run.capture()
+    run.replay()
+    torch.cuda.synchronize()
+
+    clk = ClockSampler(torch.cuda.current_device())
+    ms = time_region(run.replay, steps, dist)
+    clocks = clk.stop()
+    fg.fg_check_device_error()
+
+    psteps = max(1, min(steps, 3))
+    ms_pre, pre = profile_phase(fg, run.prefill, psteps)
+    ms_dec, dec = profile_phase(fg, run.decode_all, psteps)
+    launches_per_step = (sum(p["launches"] for p in pre.values())
+                         + sum(p["launches"] for p in dec.values())) // psteps
+    scale = getattr(wl, "layer_scale", 1.0)
+    world = dist.get_world_size() if dist is not None else 1
+    value = replicas.total_tokens(world, wl.B, wl.n, steps) / (ms * 1e-3 * scale)
+    res = {"workload": workload_desc(wl), "value": round(value, 2), "unit": UNIT,
+           "ms_per_step": round(ms / steps, 3), "steps": steps, "warmup": warmup,
+           "eager_ms_per_step": {"prefill": round(ms_pre / psteps, 3),
+                                 "decode": round(ms_dec / psteps, 3)},
+           "rooflines": phase_rooflines(wl, pre, dec, pk, psteps),
+           "kernels": {"prefill": kernel_table(pre, psteps), "decode": kernel_table(dec, psteps)},
+           "cost_model": cost_model_line(wl, value),
+           "gpu_launches_per_step": launches_per_step, "clocks": clocks}
+    extra = {"pre": pre, "psteps": psteps}
+
+    if full:
+        # end to end: every step's inputs copied in from pinned host memory and its generated
+        # hidden states copied back, inside the region; two buffer sets (each with its own
+        # engine and graph) let step i+1's inputs and step i's outputs move on copy streams
+        # while step i computes
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hxs = torch.empty(xs.shape, dtype=xs.dtype, pin_memory=True)
+        hx.copy_(x)
+        hxs.copy_(xs)
+        hout = torch.empty(run.out.shape, dtype=run.out.dtype, pin_memory=True)
+        hlast = torch.empty((wl.B, wl.h), dtype=torch.float16, pin_memory=True)
+        run_b = Runner(wl, layers, torch.empty_like(x), torch.empty_like(xs), device)
+        run_b.step()
+        torch.cuda.synchronize()
+        run_b.capture()
+        ms_e2e = time_e2e_pipelined([run, run_b], hx, hxs, hout, hlast, steps, dist)
+        extra["e2e"] = {
+            "value": round(replicas.total_tokens(world, wl.B, wl.n, steps)
+                           / (ms_e2e * 1e-3 * scale), 2),
+            "unit": UNIT, "h2d_bytes_per_step": (hx.numel() + hxs.numel()) * 2,
+            "d2h_bytes_per_step": (hout.numel() + hlast.numel()) * 2,
+            "copies": "every step's inputs in and outputs out on copy streams, overlapped "
+                      "with the neighbouring steps' compute (two buffer sets)"}
+        del run_b
+    del run, layers, x, xs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res, extra
+
+
 def run_gpu(args, wl):
     import torch
     world, rank, local = dist_env()
     dist = None
+    # the CPU baseline's oracle set-up (weight draws and quantisation, one host core) runs
+    # in a child process while the GPU works; its timed sample runs after the GPU part
+    child = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        child = subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-child",
+                                  "--config", wl.name], stdin=subprocess.PIPE,
+                                 stdout=subprocess.PIPE, text=True)
     if world > 1:
         import torch.distributed as D
         torch.cuda.set_device(local)
@@ -286,110 +438,63 @@ def run_gpu(args, wl):
     device = torch.device("cuda", torch.cuda.current_device())
     import __graft_entry__
     __graft_entry__.build()
-    from bit_compressed_throughput_gb300 import fg
 
-    layers, x, xs = build_stack(wl, device, seed_offset=rank)
-    run = Runner(wl, layers, x, xs, device)
-    for _ in range(args.warmup):
-        run.step()
-    torch.cuda.synchronize()
-    fg.fg_check_device_error()
-    run.capture()
-    run.replay()
-    torch.cuda.synchronize()
-
-    tokens_per_step = wl.B * wl.n
-    clk = ClockSampler(torch.cuda.current_device())
-    ms = time_region(run.replay, args.steps, dist)
-    clocks = clk.stop()
-    fg.fg_check_device_error()
-
-    # eager pass over the same K steps with per-launch events (roofline figures)
-    fg.fg_prof_reset()
-    fg.fg_prof_enable(True)
-    ms_eager = time_region(run.step, args.steps, dist)
-    fg.fg_prof_enable(False)
-    prof = {fg.KINDS[k]: fg.fg_prof_query(k) for k in range(len(fg.KINDS))}
-    launches = sum(p["launches"] for p in prof.values())
-
-    # end to end: every step's inputs copied in from pinned host memory and its generated
-    # hidden states copied back, inside the region; two buffer sets (each with its own
-    # engine and graph) let step i+1's inputs and step i's outputs move on copy streams while
-    # step i computes
-    hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    hxs = torch.empty(xs.shape, dtype=xs.dtype, pin_memory=True)
-    hx.copy_(x)
-    hxs.copy_(xs)
-    hout = torch.empty(run.out.shape, dtype=run.out.dtype, pin_memory=True)
-    hlast = torch.empty((wl.B, wl.h), dtype=torch.float16, pin_memory=True)
-    run_b = Runner(wl, layers, torch.empty_like(x), torch.empty_like(xs), device)
-    run_b.step()
-    torch.cuda.synchronize()
-    run_b.capture()
-    ms_e2e = time_e2e_pipelined([run, run_b], hx, hxs, hout, hlast, args.steps, dist)
-    h2d = (hx.numel() + hxs.numel()) * 2
-    d2h = (hout.numel() + hlast.numel()) * 2
+    pk = peaks()
+    main, extra = run_config(wl, device, args.steps, args.warmup, dist, rank, full=True, pk=pk)
+    per_config = {}
+    if not args.no_sub_configs and world == 1:
+        for name in SUB_CONFIGS:
+            if name == wl.name:
+                continue
+            sub, _ = run_config(fg_synth.WORKLOADS[name], device, min(args.steps, 5), 3, None,
+                                rank, full=False, pk=pk)
+            per_config[name] = sub
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return None
-    pk = peaks()
-    g_ = prof["q4_dequant_gemm_tc"]
-    gemm_tflops = g_["work"] / (g_["ms"] * 1e-3) / 1e12 if g_["ms"] else None
-    d_ = prof["q4_dequant_gemm_stream"]
-    dgemm_gbs = d_["work"] / (d_["ms"] * 1e-3) / 1e9 if d_["ms"] else None
-    a_ = prof["q4kv_decode_attn"]
-    attn_gbs = a_["work"] / (a_["ms"] * 1e-3) / 1e9 if a_["ms"] else None
-    total_kernel_ms = sum(p["ms"] for p in prof.values())
-    # a workload that keeps a slice of its layers resident reports its time scaled to the
-    # whole stack (the 175B shape: 8 of 96 layers, time x 96/8)
-    scale = getattr(wl, "layer_scale", 1.0)
-    value = replicas.total_tokens(world, wl.B, wl.n, args.steps) / (ms * 1e-3 * scale)
+    rl = main["rooflines"]
+    gemm = dict(rl["prefill_gemm"]) if rl["prefill_gemm"] else {}
+    if gemm:
+        gemm.pop("ms_per_step", None)
+        gemm["traffic"] = GEMM_TRAFFIC_PER_LAUNCH.get(wl.name)
+        gemm["traffic_note"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch"
+                                if gemm["traffic"] else
+                                "no one-kernel capture of the current GEMM at this workload")
+        gemm["share_of_kernel_time"] = round(
+            extra["pre"]["q4_dequant_gemm_tc"]["ms"] / extra["psteps"]
+            / max(1e-9, main["eager_ms_per_step"]["prefill"] + main["eager_ms_per_step"]["decode"]),
+            4)
+    kvw = per_config.get("kv-decode", main if wl.name == "kv-decode" else None)
+    attn_kv = kvw["rooflines"]["decode_attn"] if kvw else None
     res = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
+        "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded N(0,1) hidden states, N(0,0.02) weights, random init)",
-        "config": {"workload": workload_desc(wl), "tokens_per_step": tokens_per_step,
+        "config": {"workload": main["workload"], "tokens_per_step": wl.B * wl.n,
                    "parallelism": f"replicas x{world} (one block of B={wl.B} per GPU)",
                    "graph": "one CUDA graph per generation pass",
                    "l2": "no flush: per-step working set (4-bit weights "
                          f"{wl.L * 0.5625 * (4 * wl.h * wl.h + 2 * wl.h * wl.f) / 1e6:.0f} MB, "
                          f"KV {wl.L * 2 * 0.5625 * wl.B * wl.cap * wl.h / 1e6:.0f} MB, "
                          f"prompt {wl.B * wl.s * wl.h * 2 / 1e6:.0f} MB) exceeds the 129 MB L2"},
-        "roofline": {"kernel": "q4_dequant_gemm_tc", "bound": "tensor",
-                     "achieved": round(gemm_tflops, 1) if gemm_tflops else None,
-                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / pk["bf16_sustained"], 4) if gemm_tflops else None,
-                     "peak_source": f"{pk['source']} bf16 sustained (fp16 dense rate equal)",
-                     "traffic": GEMM_TRAFFIC_PER_LAUNCH,
-                     "share_of_kernel_time": round(g_["ms"] / total_kernel_ms, 4)
-                     if total_kernel_ms else None},
-        "decode_gemm_roofline": {"kernel": "q4_dequant_gemm_stream", "bound": "hbm",
-                                 "achieved": round(dgemm_gbs, 1) if dgemm_gbs else None,
-                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                 "frac": round(dgemm_gbs / pk["hbm_gbs"], 4) if dgemm_gbs else None,
-                                 "launches": d_["launches"]},
-        "decode_attn_roofline": {"kernel": "q4kv_decode_attn", "bound": "hbm",
-                                 "achieved": round(attn_gbs, 1) if attn_gbs else None,
-                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                 "frac": round(attn_gbs / pk["hbm_gbs"], 4) if attn_gbs else None,
-                                 "launches": a_["launches"]},
-        "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)}
-                    for k, v in prof.items() if v["launches"]},
-        "cost_model": cost_model_line(wl, value),
-        "eager_ms_per_step": round(ms_eager / args.steps, 3),
-        "gpu_launches": launches,
-        "e2e": {"value": round(replicas.total_tokens(world, wl.B, wl.n, args.steps)
-                               / (ms_e2e * 1e-3 * scale), 2),
-                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "every step's inputs in and outputs out on copy streams, overlapped "
-                          "with the neighbouring steps' compute (two buffer sets)"},
-        "clocks": clocks,
+        "roofline": gemm or None,
+        "decode_gemm_roofline": rl.get("decode_gemm"),
+        "decode_attn_roofline": rl["decode_attn"],
+        "decode_attn_hbm_kv_workload": attn_kv,
+        "prefill_attn_roofline": rl["prefill_attn"],
+        "kernels": main["kernels"],
+        "cost_model": main["cost_model"],
+        "eager_ms_per_step": main["eager_ms_per_step"],
+        "gpu_launches": main["gpu_launches_per_step"] * args.steps,
+        "e2e": extra["e2e"],
+        "clocks": main["clocks"],
+        "per_config": per_config,
     }
-    if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wl, samples=1)
+    if child is not None:
+        res["cpu_baseline"] = finish_oracle_child(child)
     if dist is not None:
         dist.destroy_process_group()
     return res
@@ -404,15 +509,39 @@ def oracle_setup(wl, n_layers):
     return [oracle.QuantLayer(p, wl.H, wl.d, wl.ln_eps, keep_codes=False) for p in params]
 
 
-def oracle_sample_step(wl, layers, seq: int):
-    """One sequence through the sampled layers: prefill over the prompt, n-1 decode
-    steps.  Returns seconds."""
+def oracle_sample(wl, layer, seq: int):
+    """One sequence through one layer: the prefill over the prompt, then the first decode
+    step.  Returns (seconds of the prefill, seconds of the decode step)."""
     import oracle
     xp = fg_synth.prompt_states(wl, np.array([seq]))
     xs = fg_synth.step_states(wl, np.array([seq]))
+    cache = oracle.KVCache(1, wl.cap, wl.h)
     t0 = time.perf_counter()
-    oracle.run_stack(layers, xp, xs, cap=wl.cap, dt=np.float32)
-    return time.perf_counter() - t0
+    oracle.layer_prefill(layer, xp, cache, np.float32)
+    t1 = time.perf_counter()
+    oracle.layer_decode(layer, xs[0], cache, wl.s, np.float32)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def oracle_tokens_per_s(wl, t_pre, t_dec):
+    """Throughput of the stack from one sequence-layer sample, by the pages' cost model
+    T = Tpre*l + Tgen*(n-1)*l (FlexGen paper explainer, "Analytical Cost Model"): the
+    oracle's decode step costs the same at every cache length of these workloads (its time
+    is the weight products), so one decode step stands for each of the n-1."""
+    per_seq_stack = (t_pre + (wl.n - 1) * t_dec) * wl.L * getattr(wl, "layer_scale", 1.0)
+    return wl.n / per_seq_stack
+
+
+SAMPLE_DESC = ("1 sequence x 1 layer of {name}: the prefill over the {s}-token prompt and the "
+               "first decode step, numpy float32, BLAS threads default; tokens/s = n / ((Tpre + "
+               "(n-1)*Tdec) x {L} layers{scale}) (the pages' cost model)")
+
+
+def sample_desc(wl):
+    sc = getattr(wl, "layer_scale", 1.0)
+    return SAMPLE_DESC.format(name=wl.name, s=wl.s, L=wl.L,
+                              scale=f" x {sc:g}" if sc != 1.0 else "")
 
 
 def cores():
@@ -422,37 +551,57 @@ def cores():
         return os.cpu_count()
 
 
-def cpu_baseline(wl, samples=1):
-    """The oracle (numpy, float32 products) on the host cores: one sequence through one
-    layer of the workload (prefill + n-1 decode steps), scaled to the L-layer stack."""
-    layers = oracle_setup(wl, 1)
-    secs = [oracle_sample_step(wl, layers, s) for s in range(samples)]
-    per_seq_stack = statistics.mean(secs) * wl.L * getattr(wl, "layer_scale", 1.0)
-    return {"value": round(wl.n / per_seq_stack, 4), "unit": UNIT, "cores": cores(),
-            "kind": "oracle",
-            "sample": f"1 sequence x 1 layer of {wl.name} (prefill {wl.s} + {wl.n - 1} decode "
-                      f"steps), time x{wl.L} layers; numpy float32, BLAS threads default"}
+def oracle_child(wl):
+    """Child process of the GPU arm: builds the oracle's quantised layer, says "ready",
+    waits for a line on stdin (sent once the GPU part is done), times one sample and
+    prints it as JSON."""
+    layer = oracle_setup(wl, 1)[0]
+    print("ready", flush=True)
+    sys.stdin.readline()
+    t_pre, t_dec = oracle_sample(wl, layer, 0)
+    print(json.dumps({"t_pre": t_pre, "t_dec": t_dec}), flush=True)
+
+
+def finish_oracle_child(child):
+    """Tells the child to time its sample and returns its (t_pre, t_dec) record."""
+    out, _ = child.communicate("go\n", timeout=1800)
+    lines = [ln for ln in out.strip().splitlines() if ln.startswith("{")]
+    if child.returncode != 0 or not lines:
+        return {"value": None, "unit": UNIT, "kind": "oracle", "error": "oracle child failed"}
+    return json.loads(lines[-1])
+
+
+def cpu_baseline_line(wl, d):
+    v = oracle_tokens_per_s(wl, d["t_pre"], d["t_dec"])
+    return {"value": round(v, 5), "unit": UNIT, "cores": cores(), "kind": "oracle",
+            "sample": sample_desc(wl), "sample_seconds": round(d["t_pre"] + d["t_dec"], 3)}
 
 
 def run_reference(args, wl):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    layers = oracle_setup(wl, 1)
+    layer = oracle_setup(wl, 1)[0]
     for i in range(args.warmup):
-        oracle_sample_step(wl, layers, i)
-    t = sum(oracle_sample_step(wl, layers, args.warmup + i) for i in range(args.steps))
-    # one sequence through the L-layer stack (scaled to the whole stack as the GPU arm is)
-    per_step = t / args.steps * wl.L * getattr(wl, "layer_scale", 1.0)
-    value = wl.n / per_step
-    cb = {"value": round(value, 4), "unit": UNIT, "cores": cores(), "kind": "oracle",
-          "sample": f"each step: 1 sequence x 1 layer of {wl.name} (prefill {wl.s} + "
-                    f"{wl.n - 1} decode steps), time x{wl.L} layers; numpy float32"}
+        oracle_sample(wl, layer, i)
+    pre, dec = [], []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        a, b = oracle_sample(wl, layer, args.warmup + i)
+        pre.append(a)
+        dec.append(b)
+    wall = time.perf_counter() - t0
+    value = oracle_tokens_per_s(wl, statistics.mean(pre), statistics.mean(dec))
+    cb = {"value": round(value, 5), "unit": UNIT, "cores": cores(), "kind": "oracle",
+          "sample": "each step: " + sample_desc(wl)}
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(per_step * 1e3, 1), "higher_is_better": True,
+            "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded)", "config": {"workload": workload_desc(wl)},
+            "sample_scaling": "ms_per_step is the measured time of one step's sample; value "
+                              "scales it to the workload by the cost model stated in "
+                              "cpu_baseline.sample",
             "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -464,13 +613,25 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", default="opt-6.7b", choices=sorted(fg_synth.WORKLOADS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(fg_synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-configs", action="store_true",
+                    help="time only --config (skip the other workloads' per_config lines)")
+    ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    wl = fg_synth.WORKLOADS[args.config]
+    if args.oracle_child:
+        oracle_child(wl)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    wl = fg_synth.WORKLOADS[args.config]
-    res = run_reference(args, wl) if args.impl == "reference" else run_gpu(args, wl)
+    if args.impl == "reference":
+        res = run_reference(args, wl)
+    else:
+        res = run_gpu(args, wl)
+        if res is not None and isinstance(res.get("cpu_baseline"), dict) \
+                and "t_pre" in res["cpu_baseline"]:
+            res["cpu_baseline"] = cpu_baseline_line(wl, res["cpu_baseline"])
     if res is not None:
         print(json.dumps(res), flush=True)
 

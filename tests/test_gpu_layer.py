@@ -129,3 +129,35 @@ def test_kv_decode_layer_sampled(fg):
 @pytest.mark.slow
 def test_opt175b_layer_sampled(fg):
     sampled_full_size(fg, "opt-175b", n=2)
+
+
+def test_opt67b_stack_free_running(fg):
+    """The engine's own generation loop at full size: a 2-layer opt-6.7b stack over the whole
+    block (64 sequences, prompt 512), prefill then 3 decode steps, each layer fed the
+    previous layer's output and each step appending its own K/V -- no cache is copied in
+    from the oracle.  The oracle runs the same loop (run_stack) on two sampled sequences.
+    The caches the GPU built itself (prefill and decode appends, both layers) must hold the
+    oracle's codes except at rounding boundaries: >= 97% identical, never off by more than
+    one step."""
+    wl = fg_synth.WORKLOADS["opt-6.7b"].with_(L=2, n=4)
+    params = [fg_synth.layer_params(wl, l) for l in range(wl.L)]
+    xp, xs = fg_synth.prompt_states(wl), fg_synth.step_states(wl)
+    seqs = fg_synth.sample_sequences(wl)
+    pre, steps, eng = run_gpu(fg, wl, params, xp, xs)
+    ol = [oracle.QuantLayer(p, wl.H, wl.d, wl.ln_eps, keep_codes=False) for p in params]
+    del params
+    ref = oracle.run_stack(ol, xp[seqs], xs[:, seqs], cap=wl.cap, dt=np.float32)
+    assert_close(pre[seqs], ref["prefill"], "opt-6.7b 2-layer prefill")
+    for t in range(xs.shape[0]):
+        assert_close(steps[t][seqs], ref["steps"][t], f"opt-6.7b 2-layer decode step {t + 1}")
+    used = wl.s + wl.n - 1
+    for l, (c_gpu, c_ref) in enumerate(zip(eng.caches, ref["caches"])):
+        for name, codes_t, q_ref in (("K", c_gpu.k_codes, c_ref.qk), ("V", c_gpu.v_codes, c_ref.qv)):
+            got = oracle.unpack_nibbles(cache_codes_to_rows(host(codes_t[seqs])))[:, :used]
+            want = q_ref[:, :used]
+            same = np.mean(got == want)
+            assert same > 0.97, f"layer {l} {name}: only {same:.4f} of codes agree"
+            assert np.abs(got.astype(int) - want.astype(int)).max() <= 1, f"layer {l} {name}"
+            # the prompt's codes come from the prefill append, the rest from decode appends
+            assert np.mean(got[:, :wl.s] == want[:, :wl.s]) > 0.97
+            assert np.mean(got[:, wl.s:] == want[:, wl.s:]) > 0.97
