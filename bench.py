@@ -327,25 +327,36 @@ def kernel_table(prof, steps):
             for k, v in prof.items() if v["launches"]}
 
 
+TENSOR_GEMMS = ("q4_dequant_gemm_pair", "q4_dequant_gemm_tc")
+
+
+def merged_gemm(prof):
+    """The tensor-bound GEMM launches of a phase (CTA-pair and one-CTA tiled kernels) as one
+    record, named by the kinds that ran."""
+    kinds = [k for k in TENSOR_GEMMS if prof[k]["launches"]]
+    rec = {f: sum(prof[k][f] for k in kinds) for f in ("launches", "ms", "work")}
+    return "+".join(kinds) or TENSOR_GEMMS[0], rec
+
+
 def phase_rooflines(wl, pre, dec, pk, psteps):
     """Rooflines of the prefill and decode kernels of one workload."""
-    out = {"prefill_gemm": roof("q4_dequant_gemm_tc", pre["q4_dequant_gemm_tc"], pk, "tensor",
-                                psteps),
+    pname, prec = merged_gemm(pre)
+    out = {"prefill_gemm": roof(pname, prec, pk, "tensor", psteps),
            "prefill_attn": roof("prefill_attn", pre["prefill_attn"], pk, "tensor", psteps),
            "decode_attn": roof("q4kv_decode_attn", dec["q4kv_decode_attn"], pk, "hbm", psteps,
                                {"lengths": f"{wl.s + 1}..{wl.s + wl.n - 1}",
                                 "sequences_x_heads": wl.B * wl.H})}
     ds = dec["q4_dequant_gemm_stream"]
-    dt = dec["q4_dequant_gemm_tc"]
+    dname, drec = merged_gemm(dec)
     if ds["launches"]:
         out["decode_gemm"] = roof("q4_dequant_gemm_stream", ds, pk, "hbm", psteps,
                                   {"M": wl.B, "kernel_kind": "weight-streaming (M <= 128)"})
-    if dt["launches"]:
+    if drec["launches"]:
         # M = B tokens: 3.56*M flop per weight byte, above the ridge for M >= 144
         wb = 0.5625 * (4 * wl.h * wl.h + 2 * wl.h * wl.f) * wl.L * (wl.n - 1) * psteps
-        out["decode_gemm"] = roof("q4_dequant_gemm_tc", dt, pk, "tensor", psteps,
+        out["decode_gemm"] = roof(dname, drec, pk, "tensor", psteps,
                                   {"M": wl.B, "kernel_kind": "tiled (M > 128)",
-                                   "weight_gbs": round(wb / (dt["ms"] * 1e-3) / 1e9, 1)})
+                                   "weight_gbs": round(wb / (drec["ms"] * 1e-3) / 1e9, 1)})
     return out
 
 
@@ -463,7 +474,7 @@ def run_gpu(args, wl):
                                 if gemm["traffic"] else
                                 "no one-kernel capture of the current GEMM at this workload")
         gemm["share_of_kernel_time"] = round(
-            extra["pre"]["q4_dequant_gemm_tc"]["ms"] / extra["psteps"]
+            merged_gemm(extra["pre"])[1]["ms"] / extra["psteps"]
             / max(1e-9, main["eager_ms_per_step"]["prefill"] + main["eager_ms_per_step"]["decode"]),
             4)
     kvw = per_config.get("kv-decode", main if wl.name == "kv-decode" else None)

@@ -236,13 +236,13 @@ KvOut kv_out(const fg_kvcache& kv, int T, int pos) {
 int run_gemm(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bias, int epi,
              const uint16_t* residual, uint16_t* Y, void* ws, int sms, cudaStream_t st,
              const KvOut* kv = nullptr) {
-  const GemmPlan p = gemm_plan(M, W.K, W.N, sms);
+  const GemmPlan p = gemm_plan(M, W.K, W.N, sms, kv == nullptr);
   Span sp(st);
   cudaEvent_t mid = (p.splits > 1) ? sp.mid_event() : nullptr;
   cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, kv);
   if (e != cudaSuccess) return set_cuda_error(e);
   const bool stream = (p.kind == kGemmStream);
-  const int kind = stream ? FG_K_GEMM_STREAM : FG_K_GEMM;
+  const int kind = stream ? FG_K_GEMM_STREAM : (p.kind == kGemmPair ? FG_K_GEMM_PAIR : FG_K_GEMM);
   // the streaming kernel's work is bytes: with the append, also the 4-bit K/V written
   const double w = stream ? work_gemm_stream(M, W.N, W.K) + (kv ? 2.0 * M * kv->h * 0.5625 : 0.0)
                           : work_gemm(M, W.N, W.K);
@@ -282,7 +282,7 @@ int run_gemm_ln(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t*
   cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, nullptr, &ln);
   if (e != cudaSuccess) return set_cuda_error(e);
   const bool stream = (p.kind == kGemmStream);
-  const int kind = stream ? FG_K_GEMM_STREAM : FG_K_GEMM;
+  const int kind = stream ? FG_K_GEMM_STREAM : (p.kind == kGemmPair ? FG_K_GEMM_PAIR : FG_K_GEMM);
   const double w = stream ? work_gemm_stream(M, W.N, W.K) : work_gemm(M, W.N, W.K);
   if (mid) {
     sp.close(kind, w, mid);
@@ -348,11 +348,11 @@ LayerWs layer_ws(const fg_dims& dm, int64_t M, const fg_kvcache* kv_for_decode, 
   w.att = round_up((size_t)M * h * 2);
   w.h1 = round_up((size_t)M * h * 2);
   w.mid = round_up((size_t)M * f * 2);
-  size_t g = gemm_plan(M, h, 3 * h, kMaxSms).ws_bytes;
-  g = std::max(g, gemm_plan(M, h, h, kMaxSms).ws_bytes);
+  size_t g = gemm_ws_bytes(M, h, 3 * h);
+  g = std::max(g, gemm_ws_bytes(M, h, h));
   if (f > 0) {
-    g = std::max(g, gemm_plan(M, h, f, kMaxSms).ws_bytes);
-    g = std::max(g, gemm_plan(M, f, h, kMaxSms).ws_bytes);
+    g = std::max(g, gemm_ws_bytes(M, h, f));
+    g = std::max(g, gemm_ws_bytes(M, f, h));
   }
   w.gemm = round_up(g);
   w.attn = kv_for_decode ? round_up(decode_attn_ws_bytes(*kv_for_decode, len, kMaxSms)) : 0;
@@ -393,6 +393,9 @@ int fg_check_device_error(void* stream) {
   e = gemm_read_error(&flag);
   if (e != cudaSuccess) return set_cuda_error(e);
   e = gemm_stream_read_error(&sflag);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  flag |= sflag;
+  e = gemm_pair_read_error(&sflag);
   if (e != cudaSuccess) return set_cuda_error(e);
   flag |= sflag;
   e = attn_read_error(&aflag);
@@ -438,8 +441,7 @@ int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64
 }
 
 size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N) {
-  if (M <= 0 || K <= 0 || N <= 0) return 0;
-  return gemm_plan(M, K, N, kMaxSms).ws_bytes;
+  return gemm_ws_bytes(M, K, N);
 }
 
 int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const uint16_t* bias,
@@ -755,7 +757,7 @@ const char* fg_kernel_name(int kind) {
   static const char* names[FG_K_COUNT] = {
       "q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
       "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn",
-      "layernorm", "q4_dequant_gemm_stream", "q4kv_decode_attn_topk"};
+      "layernorm", "q4_dequant_gemm_stream", "q4kv_decode_attn_topk", "q4_dequant_gemm_pair"};
   return (kind >= 0 && kind < FG_K_COUNT) ? names[kind] : "unknown";
 }
 

@@ -84,9 +84,12 @@ cudaError_t launch_decode_attn_topk(const uint16_t* q, int64_t q_stride, const f
 
 // Dequant-fused GEMM plan: tn tokens x 128 channels per tile, split-K factor and
 // workspace.  kind 0: the tiled kernel (restored weights in shared memory); kind 1: the
-// weight-streaming kernel for M <= 128 (restored weights in tensor memory).
+// weight-streaming kernel for M <= 128 (restored weights in tensor memory); kind 2: the
+// tiled product on CTA pairs (256 channels x 256 tokens per 2-CTA tile) for M >= 256 with
+// little token padding.
 constexpr int kGemmTiled = 0;
 constexpr int kGemmStream = 1;
+constexpr int kGemmPair = 2;
 constexpr int kStreamStage = 4;          // k-blocks of 64 per code stage of the streaming kernel
 struct GemmPlan {
   int kind;
@@ -111,7 +114,10 @@ struct KvOut {
   int h, H, d, cap, T, pos;
 };
 
-GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms);
+// allow_pair = false keeps to the one-CTA kernels (the K/V-append epilogue exists there only).
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int num_sms, bool allow_pair = true);
+// Workspace bytes that cover every plan of an M x K x N product on up to kMaxSms SMs.
+size_t gemm_ws_bytes(int64_t M, int64_t K, int64_t N);
 // LayerNorm of the GEMM's output rows, fused into the split-K reduce: y = LN(Y) with
 // (gamma, beta, eps), N <= 16384.
 struct LnOut {
@@ -129,6 +135,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
 // Device error words of the bounded waits (GEMM, decode attention): read-and-clear.
 cudaError_t gemm_read_error(unsigned int* out);
 cudaError_t gemm_stream_read_error(unsigned int* out);
+cudaError_t gemm_pair_read_error(unsigned int* out);
 cudaError_t attn_read_error(unsigned int* out);
 
 // Algorithmic work of one launch (bytes for memory-bound kernels, flops for the GEMM and

@@ -90,6 +90,14 @@ static_assert((2 * RA_MAX + 2 * RC_MAX + 5) * 8 + 8 <= XCH_OFF, "barrier space")
 static_assert(TMEM_COLS == 512, "TMEM budget");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
 static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
+// The code ring's depth is a multiple of the restore groups (launch_gemm rounds it down), so
+// stage c always goes to group c % RG and a group waits on every lap of its stages in order.
+// Otherwise a group could wait on lap L of a stage whose lap L - 1 (another group's k-block)
+// had not landed yet: a parity wait cannot tell lap L from lap L - 2 and would pass at once
+// on stale codes, since TMA loads complete in any order.  The restored-A ring needs ra >= RG
+// instead: MMAs complete in order, so a group that saw the MMAs of k-block it - RG - ra done
+// has seen the slot's previous lap (k-block it - 2 ra) done as well.
+static_assert(RC_MAX % RG == 0, "code ring depth in whole restore-group rounds");
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int SWZ_GROUP = 8;                // token tiles per raster group
 
@@ -838,11 +846,49 @@ static void stream_plan(GemmPlan& p, int nsm) {
   p.grid = (int)std::min<int64_t>(p.units, nsm);
 }
 
-GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm) {
+// CTA-pair plan: 256-token tiles x 256-channel pairs, one pair of CTAs per two SMs; K is
+// split, as for one-CTA tiles, only when the tiles leave over a quarter of the pairs idle.
+static bool pair_fits(int64_t M, int64_t N) {
+  if (M < 256 || N % 256 != 0) return false;
+  const int64_t tiles = (M + 255) / 256;
+  return (tiles * 256 - M) * 8 <= M;          // at most 1/8 of the token rows are padding
+}
+
+static void pair_plan(GemmPlan& p, int nsm) {
+  p.kind = kGemmPair;
+  p.tn = 256;
+  p.tiles_t = (int)((p.M + 255) / 256);
+  p.tiles_c = (int)(p.N / TCH);               // pairs = tiles_c / 2
+  p.kblocks = (int)((p.K + BK - 1) / BK);
+  const int ncl = std::max(1, nsm / 2);
+  const int64_t tiles = (int64_t)p.tiles_t * (p.tiles_c / 2);
+  int splits = 1;
+  if (tiles * 4 < (int64_t)ncl * 3) {
+    splits = (int)std::max<int64_t>(1, ncl / tiles);
+    splits = std::min(splits, std::max(1, p.kblocks / 8));
+  }
+  p.kb_per_split = std::max(1, (p.kblocks + splits - 1) / splits);
+  p.splits = std::max(1, (p.kblocks + p.kb_per_split - 1) / p.kb_per_split);
+  p.ws_bytes = (p.splits > 1) ? (size_t)p.splits * p.M * p.N * sizeof(float) : 0;
+  p.units = tiles * p.splits;
+  p.grid = (int)(2 * std::min<int64_t>(p.units, ncl));
+}
+
+size_t gemm_ws_bytes(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  return std::max(gemm_plan(M, K, N, kMaxSms, true).ws_bytes,
+                  gemm_plan(M, K, N, kMaxSms, false).ws_bytes);
+}
+
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int nsm, bool allow_pair) {
   GemmPlan p{};
   p.M = M; p.N = N; p.K = K;
   if (M > 0 && M <= 128) {
     stream_plan(p, nsm);
+    return p;
+  }
+  if (allow_pair && pair_fits(M, N)) {
+    pair_plan(p, nsm);
     return p;
   }
   p.kind = kGemmTiled;
@@ -911,6 +957,13 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   const EpiArgs final_ea{bias, residual, Y, nullptr, epi, kv ? *kv : KvOut{}};
   EpiArgs ea = final_ea;
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
+  if (p.kind == kGemmPair) {
+    if (kv && kv->k_codes) return cudaErrorInvalidValue;   // the append lives in kind 0/1
+    e = launch_gemm_pair(p, W, X, ea, st);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    if (mid_event) cudaEventRecord(mid_event, st);
+    return launch_reduce(p, ws, final_ea, ln, st);
+  }
   if (p.kind == kGemmStream) {
     e = launch_gemm_stream(p, W, tmX, ea, st);
     if (e != cudaSuccess || p.splits == 1) return e;
@@ -937,8 +990,10 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   } else {
     ra = std::min(RA_MAX, (POOL_BYTES - rc_target * CS_BYTES - rx * xb) / W_BYTES);
   }
-  const int rc = std::min(RC_MAX, (POOL_BYTES - ra * W_BYTES - rx * xb) / CS_BYTES);
-  if (ra < 3 || rx < 2 || rx > ra || rc < 2) return cudaErrorInvalidConfiguration;
+  const int rc = std::min(RC_MAX, (POOL_BYTES - ra * W_BYTES - rx * xb) / CS_BYTES) / RG * RG;
+  if (ra < RG || rx < 2 || rx > ra || rc < RG || rc % RG != 0 ||
+      ra * W_BYTES + rx * xb + rc * CS_BYTES > POOL_BYTES)
+    return cudaErrorInvalidConfiguration;
   // two MMA issuers when the token tile fits two accumulators per buffer and every unit
   // has at least one k-block for each
   const int last_unit_kb = p.kblocks - (p.splits - 1) * p.kb_per_split;

@@ -203,6 +203,26 @@ def test_gemm_stream(fg, M, K, N, epi, bias):
 # fp16 output (Y); Y itself matches the plain GEMM bit for bit and the oracle GEMM within
 # the float tolerance.  Cases cover the streaming kernel unsplit and split-K (the reduce
 # kernel appends), and the tiled kernel with ragged token tiles; d = 64 and 128.
+@pytest.mark.parametrize("M,K,N,epi,bias", [
+    (256, 64, 256, 0, False),       # one 2-CTA tile: one pair, one k-block
+    (512, 320, 512, 1, True),       # two token tiles x two pairs, five k-blocks
+    (1000, 256, 768, 2, True),      # ragged last token tile (the odd CTA's half past M), 3 pairs
+    (2048, 1024, 1024, 0, True),    # 8 tiles x 4 pairs
+    (4352, 512, 2304, 1, False),    # 17 tiles x 9 pairs: several tiles per pair, two raster groups
+    (512, 8192, 256, 2, True),      # few tiles: K split over the pairs, then the reduce
+])
+def test_gemm_pair(fg, M, K, N, epi, bias):
+    """M >= 256 with little token padding runs on CTA pairs (2-CTA tensor-core tiles)."""
+    fg.fg_prof_reset()
+    fg.fg_prof_enable(True)
+    try:
+        gemm_case(fg, M, K, N, epi, bias, seed=M * 13 + K + N)
+    finally:
+        fg.fg_prof_enable(False)
+    assert fg.fg_prof_query(fg.K_GEMM_PAIR)["launches"] == 1
+    assert fg.fg_prof_query(fg.K_GEMM)["launches"] == 0
+
+
 @pytest.mark.parametrize("B,T,pos,h,H,K,cap,path", [
     (64, 1, 7, 512, 4, 256, 16, "stream"),          # decode: one new token per sequence
     (16, 1, 0, 256, 4, 4096, 16, "split"),         # long K: split-K, appended by the reduce
@@ -414,9 +434,11 @@ def test_gemm_full_size_sampled(fg, M, K, N, epi):
 
 
 @pytest.mark.parametrize("M,K,N,epi", [
-    (8192, 4096, 4096, 2),         # prefill O projection with residual, 1024 tiles
-    (18432, 12288, 4096, 0),       # long K: 192 k-blocks per tile
+    (8192, 4096, 4096, 2),         # prefill O projection with residual (CTA pairs)
+    (18432, 12288, 4096, 0),       # long K: 192 k-blocks per tile (CTA pairs)
+    (144, 12288, 4096, 1),         # decode M = 144: one-CTA tiled kernel
     (64, 16384, 4096, 2),          # decode FC2: split K + reduce
+    (512, 8192, 256, 2),           # CTA pairs with split K
 ])
 def test_gemm_repeat_bit_identical(fg, M, K, N, epi):
     """The pipelined GEMM is deterministic: repeated launches on the same inputs give the
