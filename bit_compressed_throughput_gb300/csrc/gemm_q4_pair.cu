@@ -106,9 +106,9 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(TN >> 3) << 17)
                             ((uint32_t)(2 * TCH >> 4) << 24);
 
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_test_cl(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_cl(bar, parity)) {
+  while (!mbar_try(bar, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -122,7 +122,7 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile in
 // Wait for a phase whatever the abort flag says (draining copies or MMAs in flight).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_cl(bar, parity)) {
+  while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(&g_gemm_pair_error, 2u);
       return;
@@ -403,7 +403,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         mbar_arrive(free_c(cc_));                     // the code stage's words are consumed
         // the restored stores become visible to the tensor core's (async) proxy; once this
         // CTA's X half of the k-block has landed too, one arrival per warp on CTA 0's
-        // barrier of the k-block (cluster scope: CTA 0's MMA reads this CTA's slots)
+        // barrier of the k-block, whose MMA then makes this SM's tensor core read the slots
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         int good = 1;

@@ -89,28 +89,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier of any CTA of the cluster (cluster-window address), releasing this
-// thread's prior writes at cluster scope.
+// Arrive on an mbarrier of any CTA of the cluster (cluster-window address).  The arrive
+// releases at CTA scope: a thread's prior stores to its own shared memory are performed
+// before the arrival reaches the other CTA.  That is all the pair kernel needs: the data an
+// arrival announces (a restored A slot, a read-out accumulator) belongs to the arriving CTA
+// and is read by its own SM's tensor core, after the other CTA's thread has seen the
+// barrier complete and issued the MMA.  A cluster-scope release here cost about 1900 cycles
+// per k-block on a GB300 (a membar stall), which starved the tensor pipe.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
-               : "memory");
-}
-// Waits on a local barrier whose arrivals may come from the other CTA of the pair.
-__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
-      "selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
-      "selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
 // One MMA of the pair (issued by one thread of the even CTA): D[256][N] += A[256][16] *
 // B[16][N], A rows 0..127 and TMEM lanes of D in the even CTA, rows 128..255 in the odd one;
