@@ -846,30 +846,41 @@ static void stream_plan(GemmPlan& p, int nsm) {
   p.grid = (int)std::min<int64_t>(p.units, nsm);
 }
 
-// CTA-pair plan: 256-token tiles x 256-channel pairs, one pair of CTAs per two SMs; K is
-// split, as for one-CTA tiles, only when the tiles leave over a quarter of the pairs idle.
-static bool pair_fits(int64_t M, int64_t N) {
-  if (M < 256 || N % 256 != 0) return false;
-  const int64_t tiles = (M + 255) / 256;
-  return (tiles * 256 - M) * 8 <= M;          // at most 1/8 of the token rows are padding
-}
+// CTA-pair plan: tiles of 256 channels (a pair) x tn tokens, tn = 2 tnh the smallest multiple
+// of 16 that covers M in ceil(M / 256) tiles (M = 144 -> one tile of 144).  K is split when
+// the tiles leave clusters idle: the split count minimises the busiest cluster's k-blocks
+// (units taken round-robin, about two k-blocks of ramp per unit and 24 for a split's partials
+// and reduce).  The count is capped independently of the SM count (at most 8, at least 8
+// k-blocks per split, no more units than two rounds of the largest cluster count planned for)
+// and the workspace is sized for the cap, so a workspace sized by the query covers any device.
+static bool pair_fits(int64_t M, int64_t N) { return M > 128 && N % 256 == 0; }
 
 static void pair_plan(GemmPlan& p, int nsm) {
   p.kind = kGemmPair;
-  p.tn = 256;
   p.tiles_t = (int)((p.M + 255) / 256);
+  const int64_t per = (p.M + p.tiles_t - 1) / p.tiles_t;
+  p.tn = (int)std::min<int64_t>(256, (per + 15) / 16 * 16);
   p.tiles_c = (int)(p.N / TCH);               // pairs = tiles_c / 2
   p.kblocks = (int)((p.K + BK - 1) / BK);
-  const int ncl = std::max(1, nsm / 2);
   const int64_t tiles = (int64_t)p.tiles_t * (p.tiles_c / 2);
-  int splits = 1;
-  if (tiles * 4 < (int64_t)ncl * 3) {
-    splits = (int)std::max<int64_t>(1, ncl / tiles);
-    splits = std::min(splits, std::max(1, p.kblocks / 8));
+  const int64_t ncl = std::max(1, nsm / 2);
+  const int64_t cap = std::max<int64_t>(
+      1, std::min<int64_t>({8, p.kblocks / 8, (2 * (kMaxSms / 2) + tiles - 1) / tiles}));
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int s = 1; s <= cap; ++s) {
+    const int kbs = (p.kblocks + s - 1) / s;
+    if (s > 1 && (int64_t)(s - 1) * kbs >= p.kblocks) break;   // an empty split
+    const int64_t rounds = (tiles * s + ncl - 1) / ncl;
+    const int64_t cost = rounds * (kbs + 2) + (s > 1 ? 24 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
   }
-  p.kb_per_split = std::max(1, (p.kblocks + splits - 1) / splits);
-  p.splits = std::max(1, (p.kblocks + p.kb_per_split - 1) / p.kb_per_split);
-  p.ws_bytes = (p.splits > 1) ? (size_t)p.splits * p.M * p.N * sizeof(float) : 0;
+  p.kb_per_split = (p.kblocks + best - 1) / best;
+  p.splits = (p.kblocks + p.kb_per_split - 1) / p.kb_per_split;
+  p.ws_bytes = (cap > 1) ? (size_t)cap * p.M * p.N * sizeof(float) : 0;
   p.units = tiles * p.splits;
   p.grid = (int)(2 * std::min<int64_t>(p.units, ncl));
 }

@@ -1,26 +1,31 @@
-// Dequant-fused GEMM on CTA pairs (sm_103a): the tiled product of gemm_q4.cu for many
-// tokens, with each 2-CTA cluster sharing one 256 x 256 tensor-core tile.
+// Dequant-fused GEMM on CTA pairs (sm_103a): the tiled product for more than 128 tokens,
+// with each 2-CTA cluster sharing one tensor-core tile of 256 channels x up to 256 tokens.
 //   Y[M][N] = epi( X[M][K] * W^[K][N] + bias ),  W^ restored from 4-bit codes grouped 64
 //   along the output channel with per-group (a, b) [FlexGen review (jaehun.me), "4-bit
 //   압축은 정수 연산 가속과 같은가"].
 //
 // As in gemm_q4.cu the tensor core computes Y^T = W^T X^T, restored weights as the MMA's A
 // operand (MN-major, 128B swizzle) and activations as its B operand (K-major, 128B swizzle).
-// A cluster of two CTAs on two SMs owns a tile of 256 output channels x 256 tokens:
+// A cluster of two CTAs on two SMs owns a tile of 256 output channels x tn = 2 tnh tokens
+// (tnh <= 128, chosen per launch so that the tiles cover M with little padding: 144 tokens
+// make one tile of 144):
 //   CTA r (r = 0, 1) restores channels c0 + 128 r .. + 127 into its own shared memory (its
-//   half of the MMA's M = 256) and loads tokens t0 + 128 r .. + 127 of X (its half of the
-//   MMA's N = 256).  One thread of CTA 0 issues tcgen05.mma.cta_group::2: each SM's tensor
+//   half of the MMA's M = 256) and loads tokens t0 + tnh r .. + tnh - 1 of X (its half of
+//   the MMA's N = tn).  One thread of CTA 0 issues tcgen05.mma.cta_group::2: each SM's tensor
 //   core multiplies its own A half by both B halves, so every SM reads from shared memory
-//   its 16 KB A slot and its 16 KB X half per k-block, against 16 + 32 KB for the 128 x 256
-//   tile of one CTA, and each X element is loaded once per 256 channels instead of once per
-//   128.  Each CTA's TMEM holds its 128 channels x 256 tokens of the accumulator, which its
-//   own epilogue reads.
+//   its 16 KB A slot and its X half (16 KB at tnh = 128) per k-block, against 16 + 32 KB for
+//   the 128 x 256 tile of one CTA, and each X element is loaded once per 256 channels instead
+//   of once per 128.  Each CTA's TMEM holds its 128 channels x tn tokens of the accumulator,
+//   which its own epilogue reads.
+// Ring depths are set per launch: many token tiles (prefill) reuse each code tile from L2 and
+// take 6 k-block slots and 4 code stages; one or two token tiles (decode) stream the 4-bit
+// weights from HBM and take 12 code stages over 5 or 6 slots.
 //
 // Roles (15 warps per CTA):
-//   warp 0      TMA producer of this CTA's X half (128 tokens x 64 k) into the k-block ring;
+//   warp 0      TMA producer of this CTA's X half (tnh tokens x 64 k) into the k-block ring;
 //               owns the pair's TMEM (tcgen05.alloc.cta_group::2, 512 columns = two
 //               256-column accumulators)
-//   warp 1      CTA 0 only: issues the pair's MMAs (M = 256, N = 256, K = 16) and commits each
+//   warp 1      CTA 0 only: issues the pair's MMAs (M = 256, N = tn, K = 16) and commits each
 //               k-block to the k-block barrier of both CTAs
 //   warp 2      TMA producer of this CTA's code tiles and group statistics
 //   warps 3-10  four restore groups of two warps, group g restoring the k-blocks it == g
@@ -54,11 +59,11 @@ __device__ unsigned int g_gemm_pair_error = 0;
 namespace {
 
 constexpr int TCH = 128;                    // output channels per CTA (half of the MMA's M)
-constexpr int TNH = 128;                    // tokens per CTA (half of the MMA's N)
-constexpr int TN = 2 * TNH;                 // tokens per tile
+constexpr int TNH_MAX = 128;                // tokens per CTA (half of the MMA's N), run time
+constexpr int ACC_COLS = 256;               // TMEM columns per accumulator buffer (N <= 256)
 constexpr int BK = 64;
-constexpr int R = 6;                        // k-block ring: A slot + X half, freed by one commit
-constexpr int RC = 4;                       // code ring: codes + group statistics
+constexpr int R_MAX = 8;                    // k-block ring (A slot + X half), run-time depth
+constexpr int RC_MAX = 16;                  // code ring (codes + group statistics), run time
 constexpr int RW = 8;                       // restore warps
 constexpr int RT = RW * 32;
 constexpr int RG = 4;                       // restore groups
@@ -68,7 +73,6 @@ constexpr int RW0 = 3;                      // first restore warp
 constexpr int EW0 = RW0 + RW;               // first epilogue warp
 constexpr int THREADS = (EW0 + 4) * 32;
 constexpr int W_BYTES = TCH * BK * 2;       // 16 KB restored A slot
-constexpr int X_BYTES = TNH * BK * 2;       // 16 KB X half
 constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
 constexpr int CS_BYTES = C_BYTES + S_BYTES; // one code stage
@@ -78,13 +82,12 @@ constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 // barriers: full[R] (CTA 0: the k-block's A and X halves of both CTAs), xfull[R] (this CTA's
 // X half landed), mma_done[R] (the k-block's MMAs done: slot reusable), full_c[RC], free_c[RC],
 // acc_full[2], acc_empty[2] (CTA 0: both CTAs' epilogues read the accumulator), drain
-constexpr int NBARS = 3 * R + 2 * RC + 5;
-constexpr uint32_t TMEM_COLS = 2 * TN;      // two accumulator buffers of 256 columns
+constexpr int NBARS = 3 * R_MAX + 2 * RC_MAX + 5;
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;   // two accumulator buffers of 256 columns
 constexpr int FULL_ARRIVALS = 2 * (RTG / 32);   // one per restore warp of a group, both CTAs
 constexpr int EMPTY_ARRIVALS = 2 * 4;           // one per epilogue warp, both CTAs
-static_assert(R * (W_BYTES + X_BYTES) + RC * CS_BYTES <= POOL_BYTES, "shared memory carve-up");
 static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier space");
-static_assert(W_BYTES % 1024 == 0 && X_BYTES % 1024 == 0, "128B-swizzled slots stay 1024-aligned");
+static_assert(W_BYTES % 1024 == 0, "128B-swizzled slots stay 1024-aligned");
 static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
 static_assert(RTG % 32 == 0, "restore groups are whole warps");
@@ -92,18 +95,20 @@ static_assert(RTG % 32 == 0, "restore groups are whole warps");
 // stages in order.  Otherwise a group could wait on lap L of a stage whose lap L - 1 (another
 // group's k-block) had not landed yet: a parity wait cannot tell lap L from lap L - 2 and
 // would pass at once on stale codes (TMA loads complete in any order).
-static_assert(RC % RG == 0, "each code stage belongs to one restore group");
-// The A-slot waits need no such rule: MMAs complete in order, and with R >= RG a group has
-// seen the MMAs of k-block it - RG - R done before it waits on those of it - R.
-static_assert(R >= RG, "a group has seen the slot's previous lap complete");
+// (The host picks the code ring depth rc as a multiple of RG.)
+static_assert(RC_MAX % RG == 0, "code ring depth in whole restore-group rounds");
+// The A-slot waits need no such rule: MMAs complete in order, and with a ring depth r >= RG
+// (checked on the host) a group has seen the MMAs of k-block it - RG - r done before it waits
+// on those of it - r.
 static_assert(TMEM_COLS == 512, "TMEM budget: two 256-column accumulators");
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int SWZ_GROUP = 8;                // token tiles per raster group
 
 // instruction descriptor: D f32, A and B f16, A MN-major, B K-major, M = 256 (the pair),
-// N = 256
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(TN >> 3) << 17) |
-                            ((uint32_t)(2 * TCH >> 4) << 24);
+// N = tn (both CTAs' tokens)
+__host__ __device__ constexpr uint32_t pair_idesc(int tn) {
+  return (1u << 4) | (1u << 15) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(2 * TCH >> 4) << 24);
+}
 
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_test(bar, parity)) return true;
@@ -161,7 +166,7 @@ struct PUnit {
 
 // Work unit u -> token tile, channel pair and k-block range; SWZ_GROUP token tiles share a
 // wave of channel pairs.
-__device__ __forceinline__ PUnit pair_unit(int u, int tiles_t, int pairs, int kblocks,
+__device__ __forceinline__ PUnit pair_unit(int u, int tn, int tiles_t, int pairs, int kblocks,
                                            int kb_per_split) {
   PUnit r;
   const int tiles = tiles_t * pairs;
@@ -172,7 +177,7 @@ __device__ __forceinline__ PUnit pair_unit(int u, int tiles_t, int pairs, int kb
   const int first_t = grp * SWZ_GROUP;
   const int gt = min(SWZ_GROUP, tiles_t - first_t);
   const int within = lin - grp * group_span;
-  r.t0 = (first_t + within % gt) * TN;
+  r.t0 = (first_t + within % gt) * tn;
   r.c0 = (within / gt) * (2 * TCH);
   r.kb_begin = r.split * kb_per_split;
   r.kb_end = min(kblocks, r.kb_begin + kb_per_split);
@@ -182,6 +187,10 @@ __device__ __forceinline__ PUnit pair_unit(int u, int tiles_t, int pairs, int kb
 struct PArgs {
   int M, N, K;
   int tiles_t, pairs, kblocks, kb_per_split, units;
+  int tnh;             // tokens per CTA: a multiple of 8, <= 128 (the MMA's N = 2 tnh)
+  int r;               // k-block ring depth, RG <= r <= R_MAX
+  int rc;              // code ring depth, a multiple of RG, <= RC_MAX
+  int xslot;           // bytes per X slot: tnh * 128 rounded up to 1024
 };
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -190,9 +199,10 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  const int R = ka.r, RC = ka.rc, TNH = ka.tnh, TN = 2 * ka.tnh, XS = ka.xslot;
   uint8_t* sW = smem;                                  // R x W_BYTES (restored weights)
-  uint8_t* sX = sW + R * W_BYTES;                      // R x X_BYTES (this CTA's X half)
-  uint8_t* sC = sX + R * X_BYTES;                      // RC x CS_BYTES (codes | statistics)
+  uint8_t* sX = sW + R * W_BYTES;                      // R x XS (this CTA's X half)
+  uint8_t* sC = sX + R * XS;                           // RC x CS_BYTES (codes | statistics)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + POOL_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -202,13 +212,13 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int r) { return bar0 + 8u * r; };
-  auto xfull = [&](int r) { return bar0 + 8u * (R + r); };
-  auto mma_done = [&](int r) { return bar0 + 8u * (2 * R + r); };
-  auto full_c = [&](int c) { return bar0 + 8u * (3 * R + c); };
-  auto free_c = [&](int c) { return bar0 + 8u * (3 * R + RC + c); };
-  auto acc_full = [&](int a) { return bar0 + 8u * (3 * R + 2 * RC + a); };
-  auto acc_empty = [&](int a) { return bar0 + 8u * (3 * R + 2 * RC + 2 + a); };
-  const uint32_t drain = bar0 + 8u * (3 * R + 2 * RC + 4);
+  auto xfull = [&](int r) { return bar0 + 8u * (R_MAX + r); };
+  auto mma_done = [&](int r) { return bar0 + 8u * (2 * R_MAX + r); };
+  auto full_c = [&](int c) { return bar0 + 8u * (3 * R_MAX + c); };
+  auto free_c = [&](int c) { return bar0 + 8u * (3 * R_MAX + RC_MAX + c); };
+  auto acc_full = [&](int a) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 2 + a); };
+  const uint32_t drain = bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 4);
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < R; ++r) {
@@ -254,7 +264,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       int it = 0, s = 0;
       uint32_t ph = 0;                                // lap parity of slot s
       for (int u = cl; u < ka.units; u += ncl) {
-        const PUnit w = pair_unit(u, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+        const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
         const int c0 = w.c0 + (int)rank * TCH;
         bool ok = true;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
@@ -265,9 +275,8 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             break;
           }
           if (is_x) {
-            mbar_expect_tx(xfull(s), (uint32_t)X_BYTES);
-            tma_load_2d(smem_u32(sX + s * X_BYTES), &tmX, kb * BK, w.t0 + (int)rank * TNH,
-                        xfull(s));
+            mbar_expect_tx(xfull(s), (uint32_t)(TNH * BK * 2));
+            tma_load_2d(smem_u32(sX + s * XS), &tmX, kb * BK, w.t0 + (int)rank * TNH, xfull(s));
           } else {
             uint8_t* cs = sC + s * CS_BYTES;
             mbar_expect_tx(full_c(s), (uint32_t)CS_BYTES);
@@ -293,15 +302,16 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       // start-address field (all addresses are below 256 KB)
       const uint64_t adesc0 = smem_desc(smem_u32(sW), 64 * 128, 1024);
       const uint64_t bdesc0 = smem_desc(smem_u32(sX), 16, 1024);
+      const uint32_t idesc = pair_idesc(TN);
       int tl = 0, r = 0;
       uint32_t ph = 0;
       bool ok = true, issued = false;
       for (int u = cl; u < ka.units && ok; u += ncl, ++tl) {
-        const PUnit w = pair_unit(u, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+        const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
         const int acc = tl & 1;
         if (tl >= 2 && !pwait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t tacc = tmem + acc * TN;
+        const uint32_t tacc = tmem + acc * ACC_COLS;
         uint32_t accumulate = 0u;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!pwait(full(r), ph, abort_flag)) {
@@ -310,11 +320,11 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
           }
           tc_fence_after();
           const uint64_t ad = adesc0 + (uint64_t)r * (W_BYTES >> 4);
-          const uint64_t bd = bdesc0 + (uint64_t)r * (X_BYTES >> 4);
-          umma2_f16(tacc, ad, bd, kIdesc, accumulate);
-          umma2_f16(tacc, ad + 128, bd + 2, kIdesc, 1u);
-          umma2_f16(tacc, ad + 256, bd + 4, kIdesc, 1u);
-          umma2_f16(tacc, ad + 384, bd + 6, kIdesc, 1u);
+          const uint64_t bd = bdesc0 + (uint64_t)r * (uint64_t)(XS >> 4);
+          umma2_f16(tacc, ad, bd, idesc, accumulate);
+          umma2_f16(tacc, ad + 128, bd + 2, idesc, 1u);
+          umma2_f16(tacc, ad + 256, bd + 4, idesc, 1u);
+          umma2_f16(tacc, ad + 384, bd + 6, idesc, 1u);
           umma2_commit_mc(mma_done(r), (uint16_t)0x3);
           issued = true;
           accumulate = 1u;
@@ -357,7 +367,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint32_t phc = 0, phr = 0;
     bool ok = true;
     for (int u = cl; u < ka.units && ok; u += ncl) {
-      const PUnit w = pair_unit(u, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+      const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
       const int g0 = ((w.c0 + (int)rank * TCH) >> 6) & 3;   // first group in the stats box
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
         const int cc_ = c, cr = r;
@@ -429,7 +439,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const uint32_t empty_cl[2] = {mapa_shared(acc_empty(0), 0), mapa_shared(acc_empty(1), 0)};
     int tl = 0;
     for (int u = cl; u < ka.units; u += ncl, ++tl) {
-      const PUnit w = pair_unit(u, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+      const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
       const int c0 = w.c0 + (int)rank * TCH;
       const int acc = tl & 1;
       const int ntok = min(TN, ka.M - w.t0);
@@ -446,7 +456,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       for (int cb = 0; cb < ntok; cb += 32) {
         uint32_t r[32];
         __syncwarp();
-        const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + acc * TN + cb;
+        const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + acc * ACC_COLS + cb;
         tmem_ld16(taddr, r);
         tmem_ld16(taddr + 16, r + 16);
         tmem_wait_ld();
@@ -548,13 +558,42 @@ int pair_max_clusters() {
   return g_max_clusters;
 }
 
+// Ring depths for a plan: with many token tiles (prefill) each code tile is reused from L2
+// by the token tiles of a raster group, and deep restored slots keep the tensor pipe fed;
+// with one or two token tiles (decode) the 4-bit weights stream from HBM, so the code ring
+// gets as many stages as fit (up to 12-16, ~60-80 KB in flight per SM) over at least RG slots.
+static bool pair_rings(int tnh, int tiles_t, int* r_out, int* rc_out, int* xslot_out) {
+  const int xslot = (tnh * BK * 2 + 1023) / 1024 * 1024;
+  auto rc_for = [&](int r) {
+    return std::min(RC_MAX, (POOL_BYTES - r * (W_BYTES + xslot)) / CS_BYTES) / RG * RG;
+  };
+  int r = 6, rc = 4;
+  if (tiles_t <= 2) {
+    for (r = 6; r > RG && rc_for(r) < 12; --r) {
+    }
+    rc = rc_for(r);
+  }
+  if (r < RG || r > R_MAX || rc < RG || rc % RG != 0 || rc > RC_MAX ||
+      r * (W_BYTES + xslot) + rc * CS_BYTES > POOL_BYTES)
+    return false;
+  *r_out = r;
+  *rc_out = rc;
+  *xslot_out = xslot;
+  return true;
+}
+
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,
                              const EpiArgs& ea, cudaStream_t st) {
   const int maxcl = pair_max_clusters();
   if (maxcl <= 0) return cudaErrorInvalidConfiguration;
+  const int tnh = p.tn / 2;
+  int r = 0, rc = 0, xslot = 0;
+  if (p.tn % 16 != 0 || tnh < 8 || tnh > TNH_MAX || p.tiles_c % 2 != 0 ||
+      !pair_rings(tnh, p.tiles_t, &r, &rc, &xslot))
+    return cudaErrorInvalidConfiguration;
   CUtensorMap tmX, tmC, tmS;
   cudaError_t e = make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K,
-                              (uint64_t)p.M, (uint64_t)p.K * 2, BK, TNH,
+                              (uint64_t)p.M, (uint64_t)p.K * 2, BK, (uint32_t)tnh,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(p.N / 2),
@@ -564,7 +603,7 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
                   (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const PArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
-                 p.kb_per_split, (int)p.units};
+                 p.kb_per_split, (int)p.units, tnh, r, rc, xslot};
   const int64_t clusters = std::min<int64_t>(p.units, maxcl);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config((unsigned)(2 * clusters), st, attr);
