@@ -91,6 +91,7 @@ constexpr int kGemmTiled = 0;
 constexpr int kGemmStream = 1;
 constexpr int kGemmPair = 2;
 constexpr int kStreamStage = 4;          // k-blocks of 64 per code stage of the streaming kernel
+constexpr int kPairStageKb = 4;          // k-blocks per code stage of the CTA-pair GEMM (decode)
 struct GemmPlan {
   int kind;
   int64_t M, N, K;

@@ -866,10 +866,13 @@ static void pair_plan(GemmPlan& p, int nsm) {
   const int64_t ncl = std::max(1, nsm / 2);
   const int64_t cap = std::max<int64_t>(
       1, std::min<int64_t>({8, p.kblocks / 8, (2 * (kMaxSms / 2) + tiles - 1) / tiles}));
+  // with one or two token tiles the weights stream from HBM in code stages of
+  // kPairStageKb k-blocks, so splits are whole stages when K allows
+  const int gran = (p.tiles_t <= 2 && p.kblocks % kPairStageKb == 0) ? kPairStageKb : 1;
   int best = 1;
   int64_t best_cost = -1;
   for (int s = 1; s <= cap; ++s) {
-    const int kbs = (p.kblocks + s - 1) / s;
+    const int kbs = ((p.kblocks + s - 1) / s + gran - 1) / gran * gran;
     if (s > 1 && (int64_t)(s - 1) * kbs >= p.kblocks) break;   // an empty split
     const int64_t rounds = (tiles * s + ncl - 1) / ncl;
     const int64_t cost = rounds * (kbs + 2) + (s > 1 ? 24 : 0);
@@ -878,7 +881,7 @@ static void pair_plan(GemmPlan& p, int nsm) {
       best_cost = cost;
     }
   }
-  p.kb_per_split = (p.kblocks + best - 1) / best;
+  p.kb_per_split = ((p.kblocks + best - 1) / best + gran - 1) / gran * gran;
   p.splits = (p.kblocks + p.kb_per_split - 1) / p.kb_per_split;
   p.ws_bytes = (cap > 1) ? (size_t)cap * p.M * p.N * sizeof(float) : 0;
   p.units = tiles * p.splits;

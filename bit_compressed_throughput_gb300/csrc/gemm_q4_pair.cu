@@ -21,21 +21,25 @@
 // take 6 k-block slots and 4 code stages; one or two token tiles (decode) stream the 4-bit
 // weights from HBM and take 12 code stages over 5 or 6 slots.
 //
-// Roles (15 warps per CTA):
-//   warp 0      TMA producer of this CTA's X half (tnh tokens x 64 k) into the k-block ring;
-//               owns the pair's TMEM (tcgen05.alloc.cta_group::2, 512 columns = two
-//               256-column accumulators)
+// Roles (16 warps per CTA; warp w issues on scheduler w % 4).  The MMA issuer shares its
+// scheduler only with the two single-thread producers and one epilogue warp: with restore
+// warps beside it, the four MMAs and the commit of a k-block took ~450 cycles to issue
+// against ~365 here (measured on a GB300).
 //   warp 1      CTA 0 only: issues the pair's MMAs (M = 256, N = tn, K = 16) and commits each
 //               k-block to the k-block barrier of both CTAs
-//   warp 2      TMA producer of this CTA's code tiles and group statistics
-//   warps 3-10  four restore groups of two warps, group g restoring the k-blocks it == g
-//               (mod 4) into A slot it % R, as in gemm_q4.cu; a group that has written its
-//               slot and seen its CTA's X half land arrives, one arrival per warp, on CTA 0's
-//               barrier of that k-block, which therefore completes when both CTAs' A and X
-//               halves are in place
-//   warps 11-14 epilogue of the previous tile from this CTA's TMEM, overlapped with the next
-//               tile through the double-buffered accumulator; each warp arrives on CTA 0's
-//               accumulator-empty barrier when it has read its lanes
+//   warp 5      TMA producer of this CTA's X half (tnh tokens x 64 k) into the k-block ring
+//   warp 9      TMA producer of this CTA's code tiles and group statistics
+//   warp 8      owns the pair's TMEM (tcgen05.alloc.cta_group::2, 512 columns = two
+//               256-column accumulators)
+//   warps 0, 2, 3, 4, 6, 7, 10, 11: four restore groups of two warps, group g restoring the
+//               k-blocks it == g (mod 4) into A slot it % r, as in gemm_q4.cu; a group that has
+//               written its slot and seen its CTA's X half land arrives, one arrival per warp,
+//               on CTA 0's barrier of that k-block, which therefore completes when both CTAs'
+//               A and X halves are in place
+//   warps 12-15 epilogue of the previous tile from this CTA's TMEM (warp w reads lane quarter
+//               w % 4), overlapped with the next tile through the double-buffered accumulator;
+//               each warp arrives on CTA 0's accumulator-empty barrier when it has read its
+//               lanes
 // Each CTA drains its own TMA loads (they complete on its own barriers), CTA 0 waits for the
 // last of its MMAs, and the pair meets at a cluster barrier before freeing TMEM together.
 //
@@ -69,9 +73,23 @@ constexpr int RT = RW * 32;
 constexpr int RG = 4;                       // restore groups
 constexpr int RTG = RT / RG;                // threads per restore group (two warps)
 constexpr int ITEMS = RG;                   // 16-byte code chunks per thread per k-block
-constexpr int RW0 = 3;                      // first restore warp
-constexpr int EW0 = RW0 + RW;               // first epilogue warp
-constexpr int THREADS = (EW0 + 4) * 32;
+constexpr int EW0 = 12;                     // first epilogue warp
+constexpr int THREADS = 16 * 32;
+constexpr int kMmaWarp = 1, kXWarp = 5, kCodeWarp = 9, kTmemWarp = 8;
+// Restore warps 0, 2, 3, 4, 6, 7, 10, 11 -> restore index 0..7 (-1: another role).
+__device__ __forceinline__ int restore_index(int warp) {
+  switch (warp) {
+    case 0: return 0;
+    case 2: return 1;
+    case 3: return 2;
+    case 4: return 3;
+    case 6: return 4;
+    case 7: return 5;
+    case 10: return 6;
+    case 11: return 7;
+    default: return -1;
+  }
+}
 constexpr int W_BYTES = TCH * BK * 2;       // 16 KB restored A slot
 constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
@@ -97,6 +115,8 @@ static_assert(RTG % 32 == 0, "restore groups are whole warps");
 // would pass at once on stale codes (TMA loads complete in any order).
 // (The host picks the code ring depth rc as a multiple of RG.)
 static_assert(RC_MAX % RG == 0, "code ring depth in whole restore-group rounds");
+static_assert(RG == kPairStageKb, "a code stage of several k-blocks gives one to each group");
+static_assert((RG & (RG - 1)) == 0, "stage positions by mask");
 // The A-slot waits need no such rule: MMAs complete in order, and with a ring depth r >= RG
 // (checked on the host) a group has seen the MMAs of k-block it - RG - r done before it waits
 // on those of it - r.
@@ -189,7 +209,8 @@ struct PArgs {
   int tiles_t, pairs, kblocks, kb_per_split, units;
   int tnh;             // tokens per CTA: a multiple of 8, <= 128 (the MMA's N = 2 tnh)
   int r;               // k-block ring depth, RG <= r <= R_MAX
-  int rc;              // code ring depth, a multiple of RG, <= RC_MAX
+  int rc;              // code ring depth in stages, <= RC_MAX (a multiple of RG when sk = 1)
+  int sk;              // k-blocks per code stage: 1, or RG (whole stages in every unit)
   int xslot;           // bytes per X slot: tnh * 128 rounded up to 1024
 };
 
@@ -200,9 +221,10 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int R = ka.r, RC = ka.rc, TNH = ka.tnh, TN = 2 * ka.tnh, XS = ka.xslot;
+  const int SK = ka.sk, SB = ka.sk * CS_BYTES;         // code stage: SK k-blocks
   uint8_t* sW = smem;                                  // R x W_BYTES (restored weights)
   uint8_t* sX = sW + R * W_BYTES;                      // R x XS (this CTA's X half)
-  uint8_t* sC = sX + R * XS;                           // RC x CS_BYTES (codes | statistics)
+  uint8_t* sC = sX + R * XS;                           // RC x SB (SK codes, SK statistics)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + POOL_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -228,7 +250,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
     for (int c = 0; c < RC; ++c) {
       mbar_init(full_c(c), 1);
-      mbar_init(free_c(c), RTG);
+      mbar_init(free_c(c), SK * RTG);            // the SK groups of the stage's k-blocks
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full(a), 1);
@@ -238,7 +260,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == kTmemWarp) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
@@ -255,21 +277,22 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   pdl_launch_dependents();
   pdl_wait();
 
-  if (warp == 0 || warp == 2) {
+  if (warp == kXWarp || warp == kCodeWarp) {
     // ------------------------------------------------------------ TMA producers
-    // warp 0: this CTA's X half into the k-block ring; warp 2: codes + statistics
+    // this CTA's X half into the k-block ring, or its codes + statistics into the code ring
     if (lane == 0) {
-      const bool is_x = (warp == 0);
+      const bool is_x = (warp == kXWarp);
       const int depth = is_x ? R : RC;
-      int it = 0, s = 0;
+      const int step = is_x ? 1 : SK;                 // k-blocks per load (X) or stage (codes)
+      int it = 0, s = 0;                              // loads issued; slot
       uint32_t ph = 0;                                // lap parity of slot s
       for (int u = cl; u < ka.units; u += ncl) {
         const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
         const int c0 = w.c0 + (int)rank * TCH;
         bool ok = true;
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+        for (int kb = w.kb_begin; kb < w.kb_end; kb += step, ++it) {
           // a slot is free once the MMAs of k-block it - R are done (X); a code stage once
-          // the restorers of k-block it - RC consumed it
+          // the restorers of the k-blocks of stage it - RC consumed it
           if (it >= depth && !pwait(is_x ? mma_done(s) : free_c(s), ph ^ 1, abort_flag)) {
             ok = false;
             break;
@@ -278,10 +301,11 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_expect_tx(xfull(s), (uint32_t)(TNH * BK * 2));
             tma_load_2d(smem_u32(sX + s * XS), &tmX, kb * BK, w.t0 + (int)rank * TNH, xfull(s));
           } else {
-            uint8_t* cs = sC + s * CS_BYTES;
-            mbar_expect_tx(full_c(s), (uint32_t)CS_BYTES);
+            // one box of SK x 64 code rows and one of their statistics
+            uint8_t* cs = sC + s * SB;
+            mbar_expect_tx(full_c(s), (uint32_t)SB);
             tma_load_2d(smem_u32(cs), &tmC, c0 / 2, kb * BK, full_c(s));
-            tma_load_2d(smem_u32(cs + C_BYTES), &tmS, (c0 / 256) * 4, kb * BK, full_c(s));
+            tma_load_2d(smem_u32(cs + SK * C_BYTES), &tmS, (c0 / 256) * 4, kb * BK, full_c(s));
           }
           if (++s == depth) {
             s = 0;
@@ -295,7 +319,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       for (int i = max(0, it - depth); i < it; ++i)
         drain_wait(is_x ? xfull(i % depth) : full_c(i % depth), (uint32_t)((i / depth) & 1));
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (CTA 0)
     if (lane == 0 && rank == 0) {
       // descriptors of slot 0; a slot offset, and the K16 step, add (bytes >> 4) to the
@@ -342,12 +366,12 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         drain_wait(drain, 0u);
       }
     }
-  } else if (warp < EW0) {
+  } else if (restore_index(warp) >= 0) {
     // ------------------------------------------------------------ restore codes -> A
     // Item -> (k-row, 16-byte code chunk = 32 channels) as in gemm_q4.cu: each 8-lane phase
     // takes the two chunks of one 64-channel group on four k-rows whose (k & 3) differ and
     // whose (k & 1, k & 4) differ (conflict-free 64B-swizzled loads and 128B-swizzled stores).
-    const int tid = threadIdx.x - 32 * RW0;
+    const int tid = 32 * restore_index(warp) + lane;
     const int grp = tid / RTG, tg = tid % RTG;
     int code_off[ITEMS], stat_k[ITEMS], w_off[ITEMS], sw[ITEMS], cl4[ITEMS];
 #pragma unroll
@@ -370,10 +394,14 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
       const int g0 = ((w.c0 + (int)rank * TCH) >> 6) & 3;   // first group in the stats box
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+        // code stage c holds SK consecutive k-blocks of the unit; this is its j-th.  With
+        // SK = RG each group takes one k-block of every stage (it == g mod RG), so every group
+        // waits on every lap of every stage in order
+        const int j = (kb - w.kb_begin) & (SK - 1);
         const int cc_ = c, cr = r;
         const uint32_t cphc = phc, cphr = phr;
         const bool mine = (rg == grp);
-        if (++c == RC) { c = 0; phc ^= 1; }
+        if (j == SK - 1 && ++c == RC) { c = 0; phc ^= 1; }
         if (++r == R) { r = 0; phr ^= 1; }
         if (++rg == RG) rg = 0;
         if (!mine) continue;
@@ -381,8 +409,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
           ok = false;
           break;
         }
-        const uint8_t* cs = sC + cc_ * CS_BYTES;
-        const uint32_t* ss = reinterpret_cast<const uint32_t*>(cs + C_BYTES);
+        const uint8_t* cs = sC + cc_ * SB + j * C_BYTES;
+        const uint32_t* ss =
+            reinterpret_cast<const uint32_t*>(sC + cc_ * SB + SK * C_BYTES + j * S_BYTES);
         uint4 cw[ITEMS];
         uint32_t abw[ITEMS];
 #pragma unroll
@@ -427,7 +456,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
       }
     }
-  } else {
+  } else if (warp >= EW0) {
     // ------------------------------------------------------------ epilogue
     // TMEM lane L of this CTA holds its restored row L: channel (L & ~7) + kPerm[L & 7] of
     // its 128, kPerm = (0,4,1,5,2,6,3,7); column n holds token t0 + n.
@@ -513,7 +542,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();
-  if (warp == 0) {
+  if (warp == kTmemWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
@@ -558,26 +587,35 @@ int pair_max_clusters() {
   return g_max_clusters;
 }
 
-// Ring depths for a plan: with many token tiles (prefill) each code tile is reused from L2
-// by the token tiles of a raster group, and deep restored slots keep the tensor pipe fed;
-// with one or two token tiles (decode) the 4-bit weights stream from HBM, so the code ring
-// gets as many stages as fit (up to 12-16, ~60-80 KB in flight per SM) over at least RG slots.
-static bool pair_rings(int tnh, int tiles_t, int* r_out, int* rc_out, int* xslot_out) {
+// Ring depths for a plan.  With many token tiles (prefill) each code tile is reused from L2
+// by the token tiles of a raster group: 6 k-block slots keep the tensor pipe fed and code
+// stages of one k-block (4 of them) suffice.  With one or two token tiles (decode) the 4-bit
+// weights stream from HBM: a thread that issues TMA copies from HBM manages one every
+// ~600 cycles whatever its size, so a code stage carries RG k-blocks (a 256-row code box and
+// its statistics: two copies per 4 k-blocks) and the ring gets at least 12 k-blocks of codes
+// in flight (~60 KB per SM) over 5 or 6 slots.  Stages of RG k-blocks need every unit to hold
+// whole stages (the planner rounds kb_per_split to RG when K allows).
+static bool pair_rings(const GemmPlan& p, int tnh, int* r_out, int* rc_out, int* sk_out,
+                       int* xslot_out) {
   const int xslot = (tnh * BK * 2 + 1023) / 1024 * 1024;
+  const bool stream = p.tiles_t <= 2;
+  const int sk = (stream && p.kblocks % RG == 0 && p.kb_per_split % RG == 0) ? RG : 1;
   auto rc_for = [&](int r) {
-    return std::min(RC_MAX, (POOL_BYTES - r * (W_BYTES + xslot)) / CS_BYTES) / RG * RG;
+    const int n = std::min(RC_MAX, (POOL_BYTES - r * (W_BYTES + xslot)) / (sk * CS_BYTES));
+    return sk == 1 ? n / RG * RG : n;
   };
   int r = 6, rc = 4;
-  if (tiles_t <= 2) {
-    for (r = 6; r > RG && rc_for(r) < 12; --r) {
+  if (stream) {
+    for (r = 6; r > RG && rc_for(r) * sk < 12; --r) {
     }
     rc = rc_for(r);
   }
-  if (r < RG || r > R_MAX || rc < RG || rc % RG != 0 || rc > RC_MAX ||
-      r * (W_BYTES + xslot) + rc * CS_BYTES > POOL_BYTES)
+  if (r < RG || r > R_MAX || rc < 2 || rc > RC_MAX || (sk == 1 && rc % RG != 0) ||
+      r * (W_BYTES + xslot) + rc * sk * CS_BYTES > POOL_BYTES)
     return false;
   *r_out = r;
   *rc_out = rc;
+  *sk_out = sk;
   *xslot_out = xslot;
   return true;
 }
@@ -587,9 +625,9 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
   const int maxcl = pair_max_clusters();
   if (maxcl <= 0) return cudaErrorInvalidConfiguration;
   const int tnh = p.tn / 2;
-  int r = 0, rc = 0, xslot = 0;
-  if (p.tn % 16 != 0 || tnh < 8 || tnh > TNH_MAX || p.tiles_c % 2 != 0 ||
-      !pair_rings(tnh, p.tiles_t, &r, &rc, &xslot))
+  int r = 0, rc = 0, sk = 1, xslot = 0;
+  if (p.tn % 16 != 0 || tnh < 72 || tnh > TNH_MAX || p.tiles_c % 2 != 0 ||
+      !pair_rings(p, tnh, &r, &rc, &sk, &xslot))
     return cudaErrorInvalidConfiguration;
   CUtensorMap tmX, tmC, tmS;
   cudaError_t e = make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)p.K,
@@ -597,13 +635,15 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.codes, (uint64_t)(p.N / 2),
-                  (uint64_t)p.K, (uint64_t)(p.N / 2), TCH / 2, BK, CU_TENSOR_MAP_SWIZZLE_64B);
+                  (uint64_t)p.K, (uint64_t)(p.N / 2), TCH / 2, (uint32_t)(BK * sk),
+                  CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   e = make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT32, W.ab, (uint64_t)(p.N / 64),
-                  (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+                  (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, (uint32_t)(BK * sk),
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const PArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
-                 p.kb_per_split, (int)p.units, tnh, r, rc, xslot};
+                 p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot};
   const int64_t clusters = std::min<int64_t>(p.units, maxcl);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config((unsigned)(2 * clusters), st, attr);
