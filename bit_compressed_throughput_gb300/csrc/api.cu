@@ -398,6 +398,9 @@ int fg_check_device_error(void* stream) {
   e = gemm_pair_read_error(&sflag);
   if (e != cudaSuccess) return set_cuda_error(e);
   flag |= sflag;
+  e = prefill_read_error(&sflag);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  flag |= sflag;
   e = attn_read_error(&aflag);
   if (e != cudaSuccess) return set_cuda_error(e);
   if (flag || aflag) {

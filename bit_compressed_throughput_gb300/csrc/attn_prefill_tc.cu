@@ -1,0 +1,486 @@
+// Causal prefill attention over fp16 Q/K/V on the 5th-generation tensor cores (sm_103a).
+//
+// The prefill step processes every prompt token at once and builds the KV cache
+// [FlexGen paper explainer, "Problem Formulation", Figure 2].  Prefill attends over the
+// fp16 K/V the projection just produced (the cache keeps the 4-bit copy for decoding).
+// For query row i of a sequence and head: o_i = sum_{j <= i} softmax_j(scale * q_i . k_j) v_j.
+//
+// A CTA owns a block of 256 query rows of one (sequence, head): two Q tiles of 128 rows (A and
+// B) that share every K/V tile of 128 keys.  Q, K and V are read in place from the [rows][3h]
+// QKV buffer by TMA (boxes of 64 columns x 128 rows, 128B swizzle; d = 128 takes two).
+//   S = Q K^T     tcgen05.mma kind::f16, M = 128 query rows, N = 128 keys, K = d: A = the Q
+//                 tile and B = the K tile, both K-major in shared memory; S (fp32) in TMEM
+//   softmax       one thread per query row (TMEM lane): the row of S from TMEM, causal mask on
+//                 the diagonal tile and past the sequence, online base-2 softmax with a lazily
+//                 moved reference maximum (rescale only when a row's maximum grows by more
+//                 than 2^8), P = 2^(s - m) rounded to fp16 and written back over the first 64
+//                 columns of the row's S (two fp16 per column)
+//   O += P V      tcgen05.mma with A = P read from TMEM (K = 128 keys), B = the V tile
+//                 (MN-major: keys are its K, the head dimension its N); O (fp32) in TMEM
+// The two Q tiles ping-pong: while one tile's softmax warps work on S, the tensor core runs the
+// other tile's products.  TMEM: S of A and B (128 columns each), O of A and B (d columns each).
+//   warp 0      TMA producer: the two Q tiles once, then K/V tiles into a 2-stage ring
+//   warp 1      MMA issuer: S_A(0), S_B(0); then per key tile j and Q tile t: P_t(j) V_j into
+//               O_t, then S_t(j + 1) (the tensor core runs one thread's MMAs in issue order, so
+//               S_t(j + 1) overwrites the columns of P_t(j) only after P_t(j) V_j has read them)
+//   warps 2-5   softmax of Q tile A (warp w owns TMEM lanes 32 (w % 4) ..)
+//   warps 6-9   softmax of Q tile B
+// A Q tile sees key tiles 0 .. (its last row) / 128; tiles wholly above its rows are skipped.
+// The CTAs of the last query blocks, which see the most keys, are scheduled first.
+//
+// Every mbarrier wait is bounded; on timeout the CTA sets the device error word (read by
+// fg_check_device_error), drains its copies and MMAs and frees TMEM.
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "fg_common.cuh"
+#include "fg_internal.h"
+#include "gemm_tc.cuh"
+
+namespace fg {
+
+__device__ unsigned int g_prefill_error = 0;
+
+namespace {
+
+constexpr int QT = 128;                     // query rows per Q tile (MMA M, TMEM lanes)
+constexpr int KT = 128;                     // keys per K/V tile
+constexpr int QB = 2 * QT;                  // query rows per CTA
+constexpr int STAGES = 2;                   // K/V ring
+constexpr int THREADS = 10 * 32;
+constexpr int SM_B0 = 6;                    // first softmax warp of Q tile B (A: warp 2)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr long long kWaitCycles = 1ll << 32;
+constexpr int BOX = QT * 128;               // bytes of one 64-column x 128-row box
+
+template <int D>
+struct PSmem {
+  static constexpr int TILE = (D / 64) * BOX;          // one Q, K or V tile
+  static constexpr int Q_OFF = 0;                      // Q_A, Q_B
+  static constexpr int K_OFF = 2 * TILE;               // K stages
+  static constexpr int V_OFF = K_OFF + STAGES * TILE;  // V stages
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE;
+  static constexpr int BYTES = BAR_OFF + 256 + 1024;   // barriers; 1024 for alignment
+};
+
+// barriers: q_full, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2], drain
+constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVFREE = 3, B_SFULL = 5, B_PFULL = 7, B_ODONE = 9,
+              B_DRAIN = 11, NBARS = 12;
+static_assert(NBARS * 8 + 8 <= 256, "barrier space");
+
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(&g_prefill_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_prefill_error, 2u);
+      return;
+    }
+  }
+}
+
+// D[tmem_d] (+)= A[tmem_a] * B[bdesc], A read from tensor memory.
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (x <= 0 here; results below 2^-126 flush to zero, far
+// below the fp16 P fed to the P V product).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// instruction descriptors: D f32, A and B f16, M = 128.  S = Q K^T: both operands K-major,
+// N = 128 keys.  O += P V: A (P, in TMEM) K-major, B (V) MN-major, N = d.
+constexpr uint32_t kIdescS = (1u << 4) | ((uint32_t)(KT >> 3) << 17) | ((uint32_t)(QT >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_pv(int d) {
+  return (1u << 4) | (1u << 16) | ((uint32_t)(d >> 3) << 17) | ((uint32_t)(QT >> 4) << 24);
+}
+
+struct PArgsA {
+  int nseq, s, H, h, qblocks;
+  float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA pa,
+                       uint16_t* __restrict__ out) {
+  using L = PSmem<D>;
+  constexpr int NB = D / 64;                           // 64-column boxes per tile
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heaviest blocks first: block index counts down through the query blocks
+  const int qb = pa.qblocks - 1 - (int)(blockIdx.x % pa.qblocks);
+  const int bh = (int)(blockIdx.x / pa.qblocks);
+  const int b = bh / pa.H, hd = bh % pa.H;
+  const int q0 = qb * QB;
+  const int s = pa.s;
+  // key tiles each Q tile sees (0 when the tile lies past the sequence)
+  auto ntile_of = [&](int t) {
+    const int r0 = q0 + t * QT;
+    return (r0 < s) ? (min(s, r0 + QT) + KT - 1) / KT : 0;
+  };
+  const int nt0 = ntile_of(0), nt1 = ntile_of(1);
+  const int nkv = max(nt0, nt1);                       // >= 1: the block starts below s
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(bar(B_KVFULL + i), 1);
+      mbar_init(bar(B_KVFREE + i), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(B_SFULL + t), 1);
+      mbar_init(bar(B_PFULL + t), 4);                  // one arrival per softmax warp
+      mbar_init(bar(B_ODONE + t), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM columns: S_A 0..127, S_B 128..255, O_A 256.., O_B 256 + D..
+  auto s_col = [&](int t) { return (uint32_t)(t * KT); };
+  auto o_col = [&](int t) { return (uint32_t)(2 * KT + t * D); };
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const int row_base = b * s;                          // first QKV row of the sequence
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(B_QFULL), (uint32_t)(2 * L::TILE));
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < NB; ++c)
+          tma_load_2d(smem_u32(smem + L::Q_OFF + t * L::TILE + c * BOX), &tmQKV,
+                      hd * D + 64 * c, row_base + q0 + t * QT, bar(B_QFULL));
+      int j = 0;
+      for (; j < nkv; ++j) {
+        const int st = j % STAGES;
+        if (j >= STAGES && !bwait(bar(B_KVFREE + st), ((j / STAGES) & 1) ^ 1, abort_flag)) break;
+        mbar_expect_tx(bar(B_KVFULL + st), (uint32_t)(2 * L::TILE));
+        for (int c = 0; c < NB; ++c) {
+          tma_load_2d(smem_u32(smem + L::K_OFF + st * L::TILE + c * BOX), &tmQKV,
+                      pa.h + hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
+          tma_load_2d(smem_u32(smem + L::V_OFF + st * L::TILE + c * BOX), &tmQKV,
+                      2 * pa.h + hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
+        }
+      }
+      // every issued copy has landed before the CTA exits
+      drain_wait(bar(B_QFULL), 0u);
+      for (int i = max(0, j - STAGES); i < j; ++i)
+        drain_wait(bar(B_KVFULL + i % STAGES), (uint32_t)((i / STAGES) & 1));
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t qbase = smem_u32(smem + L::Q_OFF), kbase = smem_u32(smem + L::K_OFF),
+                     vbase = smem_u32(smem + L::V_OFF);
+      const uint32_t idesc_o = idesc_pv(D);
+      bool ok = true, issued = false;
+      // S_t(j) = Q_t K_j^T over K = D: k-step i reads 16 columns, 32 bytes into box i / 4
+      auto issue_s = [&](int t, int j) {
+        const int st = j % STAGES;
+        const uint64_t qd = smem_desc(qbase + t * L::TILE, 16, 1024);
+        const uint64_t kd = smem_desc(kbase + st * L::TILE, 16, 1024);
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const uint64_t off = (uint64_t)(((i >> 2) * BOX + (i & 3) * 32) >> 4);
+          umma_f16(tmem + s_col(t), qd + off, kd + off, kIdescS, i > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_SFULL + t));
+      };
+      // O_t += P_t(j) V_j over K = 128 keys: k-step i reads TMEM columns 8i.. of P and
+      // rows 16i.. of V (2048 bytes per step in its MN-major 128B-swizzled layout)
+      auto issue_pv = [&](int t, int j) {
+        const int st = j % STAGES;
+        const uint64_t vd = smem_desc(vbase + st * L::TILE, BOX, 1024);
+#pragma unroll
+        for (int i = 0; i < KT / 16; ++i)
+          umma_ts(tmem + o_col(t), tmem + s_col(t) + 8 * i, vd + (uint64_t)(i * 128), idesc_o,
+                  (j > 0 || i > 0) ? 1u : 0u);
+        umma_commit(bar(B_ODONE + t));
+      };
+      if (!bwait(bar(B_QFULL), 0u, abort_flag) || !bwait(bar(B_KVFULL), 0u, abort_flag)) {
+        ok = false;
+      } else {
+        tc_fence_after();
+        issue_s(0, 0);                                 // Q tile A starts below s
+        if (nt1 > 0) issue_s(1, 0);
+        issued = true;
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j % STAGES;
+        bool next_ready = false;                       // K/V of tile j + 1 waited for
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int nt = t ? nt1 : nt0;
+          if (j >= nt) continue;
+          if (!bwait(bar(B_PFULL + t), (uint32_t)(j & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nt) {
+            if (!next_ready) {
+              const int sn = (j + 1) % STAGES;
+              if (!bwait(bar(B_KVFULL + sn), (uint32_t)(((j + 1) / STAGES) & 1), abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              next_ready = true;
+            }
+            issue_s(t, j + 1);
+          }
+        }
+        umma_commit(bar(B_KVFREE + st));                // K_j, V_j read by every MMA above
+      }
+      // the CTA frees TMEM only after every MMA issued here has completed
+      if (issued) {
+        umma_commit(bar(B_DRAIN));
+        drain_wait(bar(B_DRAIN), 0u);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax of one Q tile
+    const int t = (warp < SM_B0) ? 0 : 1;
+    const int nt = t ? nt1 : nt0;
+    const int quarter = warp & 3;                      // TMEM lanes 32 quarter ..
+    const int m = 32 * quarter + lane;                 // row within the Q tile
+    const int qi = q0 + t * QT + m;                    // query position in the sequence
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const float sl2 = pa.scale_log2;
+    float m_ref = -INFINITY, l_sum = 0.0f;
+    bool ok = true;
+    // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
+    // decided for the whole warp, waits included (a lane that gave up takes its warp along)
+    for (int j = 0; j < nt; ++j) {
+      const bool got = bwait(bar(B_SFULL + t), (uint32_t)(j & 1), abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[KT];
+#pragma unroll
+      for (int c = 0; c < KT / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, v + 32 * c);
+      tmem_wait_ld();
+      // scale to base 2; mask keys past the row (diagonal tile) or past the sequence
+      const int k0 = j * KT;
+      const bool masked = (k0 + KT - 1 > q0 + t * QT) || (k0 + KT > s);
+      float mx = -INFINITY;
+      if (masked) {
+        const int lim = min(qi, s - 1) - k0;           // keys k0 .. k0 + lim are visible
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          v[c] = (c <= lim) ? v[c] * sl2 : -INFINITY;
+          mx = fmaxf(mx, v[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          v[c] *= sl2;
+          mx = fmaxf(mx, v[c]);
+        }
+      }
+      // a row past the sequence sees no key: keep it finite (it is never stored)
+      if (mx == -INFINITY) mx = 0.0f;
+      if (__any_sync(0xFFFFFFFFu, mx > m_ref + 8.0f)) {
+        // move the reference maximum of every row of the warp to max(m_ref, mx): O and l scale
+        // by 2^(m_ref - m_new) (1 for rows whose maximum did not grow); O holds P V of the
+        // earlier tiles once their MMAs are done
+        const float m_new = fmaxf(m_ref, mx);
+        const float alpha = ex2(m_ref - m_new);
+        if (j > 0) {
+          const bool done = bwait(bar(B_ODONE + t), (uint32_t)((j - 1) & 1), abort_flag);
+          if (!__all_sync(0xFFFFFFFFu, done)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // 16 columns at a time: the row of S stays in registers meanwhile
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t w[16];
+            tmem_ld16(lane_addr + o_col(t) + 16 * c, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+            tmem_st16(lane_addr + o_col(t) + 16 * c, w);
+          }
+          tmem_wait_st();
+        }
+        l_sum *= alpha;
+        m_ref = m_new;
+      }
+      uint32_t pw[KT / 2];
+      float lsum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < KT; c += 2) {
+        const float p0 = ex2(v[c] - m_ref), p1 = ex2(v[c + 1] - m_ref);
+        lsum += p0 + p1;
+        pw[c / 2] = pack_h2(p0, p1);
+      }
+      l_sum += lsum;
+      // P over the first 64 columns of this row's S (two fp16 per column)
+      tmem_st32(lane_addr + s_col(t), pw);
+      tmem_st32(lane_addr + s_col(t) + 32, pw + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + t));
+    }
+    bool fin = ok && nt > 0;
+    if (fin) fin = bwait(bar(B_ODONE + t), (uint32_t)((nt - 1) & 1), abort_flag);
+    if (__all_sync(0xFFFFFFFFu, fin)) {
+      tc_fence_after();
+      const float inv = 1.0f / l_sum;
+      uint16_t* orow = out + ((int64_t)row_base + qi) * pa.h + hd * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
+        tmem_wait_ld();
+        if (qi < s) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_h2(o[i] * inv, o[i + 1] * inv);
+            w.y = pack_h2(o[i + 2] * inv, o[i + 3] * inv);
+            w.z = pack_h2(o[i + 4] * inv, o[i + 5] * inv);
+            w.w = pack_h2(o[i + 6] * inv, o[i + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + i) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, float scale,
+                     uint16_t* out, cudaStream_t st) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<D>::BYTES);
+  if (attr != cudaSuccess) return attr;
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  const int64_t h = (int64_t)H * D;
+  CUtensorMap tm;
+  e = make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qkv, (uint64_t)(3 * h),
+                  (uint64_t)nseq * s, (uint64_t)(3 * h) * 2, 64, QT, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const int qblocks = (s + QB - 1) / QB;
+  const PArgsA pa{nseq, s, H, (int)h, qblocks, scale * 1.4426950408889634f};
+  const int64_t grid = (int64_t)nseq * H * qblocks;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_pdl(prefill_attn_tc_kernel<D>, dim3((unsigned)grid), dim3(THREADS),
+                    PSmem<D>::BYTES, st, tm, pa, out);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
+                                int32_t d, float scale, uint16_t* out, cudaStream_t st) {
+  if (nseq == 0 || s == 0) return cudaSuccess;
+  return d == 128 ? launch_d<128>(qkv, nseq, s, H, scale, out, st)
+                  : launch_d<64>(qkv, nseq, s, H, scale, out, st);
+}
+
+cudaError_t prefill_read_error(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_prefill_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace fg

@@ -137,6 +137,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
 cudaError_t gemm_read_error(unsigned int* out);
 cudaError_t gemm_stream_read_error(unsigned int* out);
 cudaError_t gemm_pair_read_error(unsigned int* out);
+cudaError_t prefill_read_error(unsigned int* out);
 cudaError_t attn_read_error(unsigned int* out);
 
 // Algorithmic work of one launch (bytes for memory-bound kernels, flops for the GEMM and

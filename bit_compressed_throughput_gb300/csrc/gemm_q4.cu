@@ -513,8 +513,8 @@ gemm_q4_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         for (int i = 32 * (warp & 3) + lane; i < 2 * ntok; i += 128)
           prefetch_l2(ea.residual + (int64_t)(w.t0 + (i >> 1)) * N + w.c0 + (i & 1) * 64);
       }
-      if (!mbar_wait(acc_full(acc), (tl >> 1) & 1, abort_flag)) break;
-      __syncwarp();
+      // the warp-collective TMEM loads below need the whole warp: decide for all its lanes
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(acc), (tl >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       const int64_t ch = w.c0 + ch_in_tile;
       const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;

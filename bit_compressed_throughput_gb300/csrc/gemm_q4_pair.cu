@@ -476,8 +476,8 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         for (int i = 32 * (warp & 3) + lane; i < 2 * ntok; i += 128)
           prefetch_l2(ea.residual + (int64_t)(w.t0 + (i >> 1)) * N + c0 + (i & 1) * 64);
       }
-      if (!pwait(acc_full(acc), (tl >> 1) & 1, abort_flag)) break;
-      __syncwarp();
+      // the warp-collective TMEM loads below need the whole warp: decide for all its lanes
+      if (!__all_sync(0xFFFFFFFFu, pwait(acc_full(acc), (tl >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       const int64_t ch = c0 + ch_in_tile;
       const float bias_f = (!ea.partial && ea.bias) ? h2f(ea.bias[ch]) : 0.0f;

@@ -428,8 +428,8 @@ gemm_q4_stream_kernel(const __grid_constant__ CUtensorMap tmX,
     for (int u = blockIdx.x; u < ka.units; u += gridDim.x, ++tl) {
       const SUnit w = stream_unit(u, ka);
       const int b = tl % ka.nbuf, use = tl / ka.nbuf;
-      if (!swait(acc_full(b), use & 1, abort_flag)) break;
-      __syncwarp();
+      // the warp-collective TMEM loads below need the whole warp: decide for all its lanes
+      if (!__all_sync(0xFFFFFFFFu, swait(acc_full(b), use & 1, abort_flag))) break;
       tc_fence_after();
       // issuer mi accumulated this unit iff one of its k-blocks it .. it + L - 1 is == mi
       // (mod NI)

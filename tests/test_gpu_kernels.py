@@ -648,11 +648,17 @@ def test_decode_attention_topk_kv_workload_sampled(fg):
 # ----------------------------------------------------------------------------- prefill attention
 
 
-@pytest.mark.parametrize("nseq,s,H,d", [(2, 16, 4, 64), (3, 100, 2, 128), (1, 513, 2, 128),
-                                        (2, 64, 3, 64), (1, 1, 2, 128)])
-def test_prefill_attention(fg, nseq, s, H, d):
+@pytest.mark.parametrize("nseq,s,H,d,mag", [
+    (2, 16, 4, 64, 1.5), (3, 100, 2, 128, 1.5), (1, 513, 2, 128, 1.5), (2, 64, 3, 64, 1.5),
+    (1, 1, 2, 128, 1.5),
+    (2, 384, 2, 128, 1.5),       # a full 256-row block and a half one, key tiles shared by both
+    (3, 300, 3, 64, 1.5),        # d = 64, ragged second block
+    (1, 1024, 1, 128, 1.5),      # four blocks, up to eight key tiles per Q tile
+    (2, 640, 2, 128, 4.0),       # large scores: the reference maximum moves many times
+])
+def test_prefill_attention(fg, nseq, s, H, d, mag):
     h = H * d
-    qkv16 = fg_synth.random_fp16((nseq * s, 3 * h), seed=nseq * 10 + s, scale=1.5)
+    qkv16 = fg_synth.random_fp16((nseq * s, 3 * h), seed=nseq * 10 + s, scale=mag)
     out = torch.empty((nseq * s, h), dtype=torch.float16, device="cuda")
     fg.fg_prefill_attn(dev(qkv16), nseq, s, H, d, 1.0 / math.sqrt(d), out)
     x = qkv16.reshape(nseq, s, 3 * h)
