@@ -327,9 +327,9 @@ int run_decode_attn(const uint16_t* q, int64_t q_stride, const fg_kvcache& kv, i
 namespace {
 
 int run_prefill_attn(const uint16_t* qkv, int nseq, int s, int H, int d, float scale,
-                     uint16_t* out, cudaStream_t st) {
+                     uint16_t* out, int sms, cudaStream_t st) {
   Span sp(st);
-  cudaError_t e = launch_prefill_attn(qkv, nseq, s, H, d, scale, out, st);
+  cudaError_t e = launch_prefill_attn(qkv, nseq, s, H, d, scale, out, sms, st);
   if (e != cudaSuccess) return set_cuda_error(e);
   sp.stop(FG_K_PREFILL_ATTN, work_prefill_attn(nseq, s, (int64_t)H * d));
   return FG_OK;
@@ -584,9 +584,10 @@ int fg_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, int
   if (!(scale > 0.0f) || !isfinite(scale)) return FG_ERR_ARG;
   if (nseq == 0 || s == 0) return FG_OK;
   if (!qkv || !out || !aligned16(qkv) || !aligned16(out)) return FG_ERR_ARG;
-  int rc = check_device(nullptr);
+  int sms = 0;
+  int rc = check_device(&sms);
   if (rc) return rc;
-  return run_prefill_attn(qkv, nseq, s, H, d, scale, out, static_cast<cudaStream_t>(stream));
+  return run_prefill_attn(qkv, nseq, s, H, d, scale, out, sms, static_cast<cudaStream_t>(stream));
 }
 
 int fg_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* gamma,
@@ -673,7 +674,7 @@ int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const
     if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st)))
       return rc;
     if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, s, 0, kvk, st))) return rc;
-    if ((rc = run_prefill_attn(qkv, g, s, dm->H, dm->d, scale, att, st))) return rc;
+    if ((rc = run_prefill_attn(qkv, g, s, dm->H, dm->d, scale, att, sms, st))) return rc;
     if (dm->f > 0) {
       // O projection + residual into h1, then LN2(h1) (fused into a split-K reduce)
       if ((rc = run_gemm_ln(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, h1, L->ln2_g, L->ln2_b,

@@ -26,7 +26,8 @@
 //   warps 2-5   softmax of Q tile A (warp w owns TMEM lanes 32 (w % 4) ..)
 //   warps 6-9   softmax of Q tile B
 // A Q tile sees key tiles 0 .. (its last row) / 128; tiles wholly above its rows are skipped.
-// The CTAs of the last query blocks, which see the most keys, are scheduled first.
+// The kernel is persistent (one CTA per SM over the blocks, heaviest first), so the next block's
+// loads and first products overlap the current block's softmax and output.
 //
 // Every mbarrier wait is bounded; on timeout the CTA sets the device error word (read by
 // fg_check_device_error), drains its copies and MMAs and frees TMEM.
@@ -61,13 +62,16 @@ struct PSmem {
   static constexpr int Q_OFF = 0;                      // Q_A, Q_B
   static constexpr int K_OFF = 2 * TILE;               // K stages
   static constexpr int V_OFF = K_OFF + STAGES * TILE;  // V stages
-  static constexpr int BAR_OFF = V_OFF + STAGES * TILE;
+  static constexpr int O_OFF = V_OFF + STAGES * TILE;  // one output box per Q tile
+  static constexpr int BAR_OFF = O_OFF + 2 * BOX;
   static constexpr int BYTES = BAR_OFF + 256 + 1024;   // barriers; 1024 for alignment
 };
+static_assert(PSmem<128>::BYTES <= 227 * 1024, "shared memory per CTA");
 
-// barriers: q_full, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2], drain
-constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVFREE = 3, B_SFULL = 5, B_PFULL = 7, B_ODONE = 9,
-              B_DRAIN = 11, NBARS = 12;
+// barriers: q_full, q_free, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2],
+// o_staged[2], o_stage_free[2], drain
+constexpr int B_QFULL = 0, B_QFREE = 1, B_KVFULL = 2, B_KVFREE = 4, B_SFULL = 6, B_PFULL = 8,
+              B_ODONE = 10, B_OSTAGED = 12, B_OSFREE = 14, B_DRAIN = 16, NBARS = 17;
 static_assert(NBARS * 8 + 8 <= 256, "barrier space");
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -92,6 +96,34 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
       return;
     }
   }
+}
+
+// Tiled TMA store of a shared-memory box to global coordinates (x, y, z), tracked by the
+// issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 // D[tmem_d] (+)= A[tmem_a] * B[bdesc], A read from tensor memory.
@@ -151,6 +183,23 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe, for a share of the exponentials so that the special-function unit
+// (one ex2 per element otherwise, as much time per key tile as the tensor core's) is not the
+// bottleneck.  Range reduction to the nearest integer n (x = n + f, |f| <= 1/2; adding
+// 1.5 * 2^23 rounds x to an integer), a cubic for 2^f whose coefficients were fitted for this
+// kernel (relative error at most 1.1e-4 on [-1/2, 1/2], below half an fp16 step of P), and 2^n
+// added into the exponent field.  x is clamped at -64: P is rounded to fp16, where anything
+// below 2^-25 is zero.
+__device__ __forceinline__ float exp2_poly(float x) {
+  constexpr float kC1 = 0x1.62f5fap-1f, kC2 = 0x1.f00c4ep-3f, kC3 = 0x1.c2a216p-5f;
+  x = fmaxf(x, -64.0f);
+  const float t = x + 12582912.0f;
+  const float n = t - 12582912.0f;
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(kC3, f, kC2), f, kC1), f, 1.0f);
+  return __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
+}
+
 // instruction descriptors: D f32, A and B f16, M = 128.  S = Q K^T: both operands K-major,
 // N = 128 keys.  O += P V: A (P, in TMEM) K-major, B (V) MN-major, N = d.
 constexpr uint32_t kIdescS = (1u << 4) | ((uint32_t)(KT >> 3) << 17) | ((uint32_t)(QT >> 4) << 24);
@@ -163,10 +212,38 @@ struct PArgsA {
   float scale_log2;
 };
 
+// A work item: a block of 256 query rows of one (sequence, head).  Items run heaviest first
+// (the last query blocks see the most keys): item i is query block qblocks - 1 - i / (nseq H)
+// of (sequence, head) i % (nseq H).
+struct Item {
+  int b, hd, q0, nt0, nt1, nkv;
+};
+__device__ __forceinline__ Item item_of(int i, const PArgsA& pa) {
+  const int bhn = pa.nseq * pa.H;
+  Item it;
+  const int qb = pa.qblocks - 1 - i / bhn;
+  const int bh = i % bhn;
+  it.b = bh / pa.H;
+  it.hd = bh % pa.H;
+  it.q0 = qb * QB;
+  // key tiles each Q tile sees (0 when the tile lies past the sequence)
+  const int r1 = it.q0 + QT;
+  it.nt0 = (min(pa.s, it.q0 + QT) + KT - 1) / KT;    // >= 1: the block starts below s
+  it.nt1 = (r1 < pa.s) ? (min(pa.s, r1 + QT) + KT - 1) / KT : 0;
+  it.nkv = max(it.nt0, it.nt1);
+  return it;
+}
+
+// Persistent: CTA c takes items c, c + gridDim, ...  The producer loads the next item's Q as
+// soon as the current item's last S product is done and streams K/V through the ring across
+// items; the MMA issuer starts the next item's S products while the softmax warps normalise
+// and store the current item's O.  The next item's first P V product, which overwrites O_t,
+// waits for P_t of that item, which the same softmax warps write only after they have read
+// O_t, so O needs no barrier of its own.
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA pa,
-                       uint16_t* __restrict__ out) {
+prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
+                       const __grid_constant__ CUtensorMap tmO, const PArgsA pa) {
   using L = PSmem<D>;
   constexpr int NB = D / 64;                           // 64-column boxes per tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -179,22 +256,12 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest blocks first: block index counts down through the query blocks
-  const int qb = pa.qblocks - 1 - (int)(blockIdx.x % pa.qblocks);
-  const int bh = (int)(blockIdx.x / pa.qblocks);
-  const int b = bh / pa.H, hd = bh % pa.H;
-  const int q0 = qb * QB;
+  const int nitems = pa.nseq * pa.H * pa.qblocks;
   const int s = pa.s;
-  // key tiles each Q tile sees (0 when the tile lies past the sequence)
-  auto ntile_of = [&](int t) {
-    const int r0 = q0 + t * QT;
-    return (r0 < s) ? (min(s, r0 + QT) + KT - 1) / KT : 0;
-  };
-  const int nt0 = ntile_of(0), nt1 = ntile_of(1);
-  const int nkv = max(nt0, nt1);                       // >= 1: the block starts below s
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QFREE), 1);
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bar(B_KVFULL + i), 1);
       mbar_init(bar(B_KVFREE + i), 1);
@@ -203,6 +270,8 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
       mbar_init(bar(B_SFULL + t), 1);
       mbar_init(bar(B_PFULL + t), 4);                  // one arrival per softmax warp
       mbar_init(bar(B_ODONE + t), 1);
+      mbar_init(bar(B_OSTAGED + t), 4);                // one arrival per softmax warp
+      mbar_init(bar(B_OSFREE + t), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -225,30 +294,44 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
   pdl_launch_dependents();
   pdl_wait();
 
-  const int row_base = b * s;                          // first QKV row of the sequence
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(bar(B_QFULL), (uint32_t)(2 * L::TILE));
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < NB; ++c)
-          tma_load_2d(smem_u32(smem + L::Q_OFF + t * L::TILE + c * BOX), &tmQKV,
-                      hd * D + 64 * c, row_base + q0 + t * QT, bar(B_QFULL));
-      int j = 0;
-      for (; j < nkv; ++j) {
-        const int st = j % STAGES;
-        if (j >= STAGES && !bwait(bar(B_KVFREE + st), ((j / STAGES) & 1) ^ 1, abort_flag)) break;
-        mbar_expect_tx(bar(B_KVFULL + st), (uint32_t)(2 * L::TILE));
-        for (int c = 0; c < NB; ++c) {
-          tma_load_2d(smem_u32(smem + L::K_OFF + st * L::TILE + c * BOX), &tmQKV,
-                      pa.h + hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
-          tma_load_2d(smem_u32(smem + L::V_OFF + st * L::TILE + c * BOX), &tmQKV,
-                      2 * pa.h + hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
+      int kvg = 0, qn = 0;                             // K/V tiles, Q pairs issued
+      bool ok = true;
+      for (int i = blockIdx.x; i < nitems && ok; i += gridDim.x) {
+        const Item it = item_of(i, pa);
+        const int row_base = it.b * s;
+        // the previous item's S products are done with the Q tiles
+        if (qn > 0 && !bwait(bar(B_QFREE), (uint32_t)((qn - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(bar(B_QFULL), (uint32_t)(2 * L::TILE));
+        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < NB; ++c)
+            tma_load_2d(smem_u32(smem + L::Q_OFF + t * L::TILE + c * BOX), &tmQKV,
+                        it.hd * D + 64 * c, row_base + it.q0 + t * QT, bar(B_QFULL));
+        ++qn;
+        for (int j = 0; j < it.nkv; ++j, ++kvg) {
+          const int st = kvg % STAGES;
+          if (kvg >= STAGES &&
+              !bwait(bar(B_KVFREE + st), (uint32_t)(((kvg / STAGES) & 1) ^ 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(B_KVFULL + st), (uint32_t)(2 * L::TILE));
+          for (int c = 0; c < NB; ++c) {
+            tma_load_2d(smem_u32(smem + L::K_OFF + st * L::TILE + c * BOX), &tmQKV,
+                        pa.h + it.hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
+            tma_load_2d(smem_u32(smem + L::V_OFF + st * L::TILE + c * BOX), &tmQKV,
+                        2 * pa.h + it.hd * D + 64 * c, row_base + j * KT, bar(B_KVFULL + st));
+          }
         }
       }
       // every issued copy has landed before the CTA exits
-      drain_wait(bar(B_QFULL), 0u);
-      for (int i = max(0, j - STAGES); i < j; ++i)
+      if (qn > 0) drain_wait(bar(B_QFULL), (uint32_t)((qn - 1) & 1));
+      for (int i = max(0, kvg - STAGES); i < kvg; ++i)
         drain_wait(bar(B_KVFULL + i % STAGES), (uint32_t)((i / STAGES) & 1));
     }
   } else if (warp == 1) {
@@ -258,9 +341,12 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
                      vbase = smem_u32(smem + L::V_OFF);
       const uint32_t idesc_o = idesc_pv(D);
       bool ok = true, issued = false;
-      // S_t(j) = Q_t K_j^T over K = D: k-step i reads 16 columns, 32 bytes into box i / 4
-      auto issue_s = [&](int t, int j) {
-        const int st = j % STAGES;
+      int kvg = 0, qn = 0;                             // K/V tiles, items consumed
+      int pc[2] = {0, 0};                              // P V products per Q tile
+      // S_t = Q_t K^T of K/V tile g over K = D: k-step i reads 16 columns, 32 bytes into box
+      // i / 4
+      auto issue_s = [&](int t, int g) {
+        const int st = g % STAGES;
         const uint64_t qd = smem_desc(qbase + t * L::TILE, 16, 1024);
         const uint64_t kd = smem_desc(kbase + st * L::TILE, 16, 1024);
 #pragma unroll
@@ -270,51 +356,60 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
         }
         umma_commit(bar(B_SFULL + t));
       };
-      // O_t += P_t(j) V_j over K = 128 keys: k-step i reads TMEM columns 8i.. of P and
-      // rows 16i.. of V (2048 bytes per step in its MN-major 128B-swizzled layout)
-      auto issue_pv = [&](int t, int j) {
-        const int st = j % STAGES;
+      // O_t (+)= P_t V of K/V tile g over K = 128 keys: k-step i reads TMEM columns 8i.. of
+      // P and rows 16i.. of V (2048 bytes per step in its MN-major 128B-swizzled layout)
+      auto issue_pv = [&](int t, int g, bool first) {
+        const int st = g % STAGES;
         const uint64_t vd = smem_desc(vbase + st * L::TILE, BOX, 1024);
 #pragma unroll
         for (int i = 0; i < KT / 16; ++i)
           umma_ts(tmem + o_col(t), tmem + s_col(t) + 8 * i, vd + (uint64_t)(i * 128), idesc_o,
-                  (j > 0 || i > 0) ? 1u : 0u);
+                  (!first || i > 0) ? 1u : 0u);
         umma_commit(bar(B_ODONE + t));
       };
-      if (!bwait(bar(B_QFULL), 0u, abort_flag) || !bwait(bar(B_KVFULL), 0u, abort_flag)) {
-        ok = false;
-      } else {
-        tc_fence_after();
-        issue_s(0, 0);                                 // Q tile A starts below s
-        if (nt1 > 0) issue_s(1, 0);
-        issued = true;
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % STAGES;
-        bool next_ready = false;                       // K/V of tile j + 1 waited for
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nt = t ? nt1 : nt0;
-          if (j >= nt) continue;
-          if (!bwait(bar(B_PFULL + t), (uint32_t)(j & 1), abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < nt) {
-            if (!next_ready) {
-              const int sn = (j + 1) % STAGES;
-              if (!bwait(bar(B_KVFULL + sn), (uint32_t)(((j + 1) / STAGES) & 1), abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              next_ready = true;
-            }
-            issue_s(t, j + 1);
-          }
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++qn) {
+        const Item it = item_of(item, pa);
+        const int nt[2] = {it.nt0, it.nt1};
+        if (!bwait(bar(B_QFULL), (uint32_t)(qn & 1), abort_flag) ||
+            !bwait(bar(B_KVFULL + kvg % STAGES), (uint32_t)((kvg / STAGES) & 1), abort_flag)) {
+          ok = false;
+          break;
         }
-        umma_commit(bar(B_KVFREE + st));                // K_j, V_j read by every MMA above
+        tc_fence_after();
+        issue_s(0, kvg);
+        if (it.nt1 > 0) issue_s(1, kvg);
+        issued = true;
+        if (it.nkv == 1) umma_commit(bar(B_QFREE));    // every S product of the item issued
+        for (int j = 0; j < it.nkv && ok; ++j) {
+          const int g = kvg + j;
+          bool next_ready = false;                     // K/V of tile g + 1 waited for
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= nt[t]) continue;
+            if (!bwait(bar(B_PFULL + t), (uint32_t)(pc[t] & 1), abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, g, j == 0);
+            ++pc[t];
+            if (j + 1 < nt[t]) {
+              if (!next_ready) {
+                const int gn = g + 1;
+                if (!bwait(bar(B_KVFULL + gn % STAGES), (uint32_t)((gn / STAGES) & 1),
+                           abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                next_ready = true;
+              }
+              issue_s(t, g + 1);
+            }
+          }
+          if (j == it.nkv - 2) umma_commit(bar(B_QFREE));   // the item's last S products
+          umma_commit(bar(B_KVFREE + g % STAGES));     // K/V tile g read by every MMA above
+        }
+        kvg += it.nkv;
       }
       // the CTA frees TMEM only after every MMA issued here has completed
       if (issued) {
@@ -325,116 +420,154 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
   } else {
     // ------------------------------------------------------------ softmax of one Q tile
     const int t = (warp < SM_B0) ? 0 : 1;
-    const int nt = t ? nt1 : nt0;
     const int quarter = warp & 3;                      // TMEM lanes 32 quarter ..
     const int m = 32 * quarter + lane;                 // row within the Q tile
-    const int qi = q0 + t * QT + m;                    // query position in the sequence
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     const float sl2 = pa.scale_log2;
-    float m_ref = -INFINITY, l_sum = 0.0f;
+    int sc = 0;                                        // S products of this Q tile consumed
+    int nst = 0;                                       // output boxes stored
     bool ok = true;
+    const bool leader = (warp == 2 + 4 * t) && lane == 0;   // issues this tile's stores
+    const uint32_t stage = smem_u32(smem + L::O_OFF + t * BOX);
     // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
     // decided for the whole warp, waits included (a lane that gave up takes its warp along)
-    for (int j = 0; j < nt; ++j) {
-      const bool got = bwait(bar(B_SFULL + t), (uint32_t)(j & 1), abort_flag);
-      if (!__all_sync(0xFFFFFFFFu, got)) {
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+      const Item it = item_of(item, pa);
+      const int nt = t ? it.nt1 : it.nt0;
+      if (nt == 0) continue;
+      const int qi = it.q0 + t * QT + m;               // query position in the sequence
+      float m_ref = -INFINITY, l_sum = 0.0f;
+      for (int j = 0; j < nt; ++j, ++sc) {
+        const bool got = bwait(bar(B_SFULL + t), (uint32_t)(sc & 1), abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float v[KT];
+#pragma unroll
+        for (int c = 0; c < KT / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, v + 32 * c);
+        tmem_wait_ld();
+        // mask keys past the row (diagonal tile) or past the sequence; the row maximum in
+        // base 2 (scale > 0, so scaling after the maximum is the same)
+        const int k0 = j * KT;
+        const bool masked = (k0 + KT - 1 > it.q0 + t * QT) || (k0 + KT > s);
+        if (masked) {
+          const int lim = min(qi, s - 1) - k0;         // keys k0 .. k0 + lim are visible
+#pragma unroll
+          for (int c = 0; c < KT; ++c) v[c] = (c <= lim) ? v[c] : -INFINITY;
+        }
+        // eight independent running maxima, so that the reduction is not one long chain
+        float m8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) m8[c] = v[c];
+#pragma unroll
+        for (int c = 8; c < KT; ++c) m8[c & 7] = fmaxf(m8[c & 7], v[c]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // a row that sees no key keeps a finite maximum (such rows lie past the sequence and
+        // are never stored)
+        mx = (mx == -INFINITY) ? 0.0f : mx * sl2;
+        if (__any_sync(0xFFFFFFFFu, mx > m_ref + 8.0f)) {
+          // move the reference maximum of every row of the warp to max(m_ref, mx): O and l
+          // scale by 2^(m_ref - m_new) (1 for rows whose maximum did not grow); O holds P V of
+          // the item's earlier tiles once their MMAs are done
+          const float m_new = fmaxf(m_ref, mx);
+          const float alpha = ex2(m_ref - m_new);
+          if (j > 0) {
+            const bool done = bwait(bar(B_ODONE + t), (uint32_t)((sc - 1) & 1), abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, done)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // 16 columns at a time: the row of S stays in registers meanwhile
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t w[16];
+              tmem_ld16(lane_addr + o_col(t) + 16 * c, w);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+              tmem_st16(lane_addr + o_col(t) + 16 * c, w);
+            }
+            tmem_wait_st();
+          }
+          l_sum *= alpha;
+          m_ref = m_new;
+        }
+        uint32_t pw[KT / 2];
+        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};       // four partial row sums
+        // p = 2^(s * scale - m_ref): one element in four on the FMA pipe, the rest on ex2
+#pragma unroll
+        for (int c = 0; c < KT; c += 2) {
+          const float x0 = fmaf(v[c], sl2, -m_ref), x1 = fmaf(v[c + 1], sl2, -m_ref);
+          const float p0 = ex2(x0);
+          const float p1 = ((c & 3) == 2) ? exp2_poly(x1) : ex2(x1);
+          ls[(c >> 1) & 3] += p0 + p1;
+          pw[c / 2] = pack_h2(p0, p1);
+        }
+        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P over the first 64 columns of this row's S (two fp16 per column)
+        tmem_st32(lane_addr + s_col(t), pw);
+        tmem_st32(lane_addr + s_col(t) + 32, pw + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + t));
+      }
+      if (!ok) break;
+      // the item's O: wait for its last P V product, normalise, store
+      const bool fin = bwait(bar(B_ODONE + t), (uint32_t)((sc - 1) & 1), abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, fin)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float v[KT];
-#pragma unroll
-      for (int c = 0; c < KT / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, v + 32 * c);
-      tmem_wait_ld();
-      // scale to base 2; mask keys past the row (diagonal tile) or past the sequence
-      const int k0 = j * KT;
-      const bool masked = (k0 + KT - 1 > q0 + t * QT) || (k0 + KT > s);
-      float mx = -INFINITY;
-      if (masked) {
-        const int lim = min(qi, s - 1) - k0;           // keys k0 .. k0 + lim are visible
-#pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          v[c] = (c <= lim) ? v[c] * sl2 : -INFINITY;
-          mx = fmaxf(mx, v[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          v[c] *= sl2;
-          mx = fmaxf(mx, v[c]);
-        }
-      }
-      // a row past the sequence sees no key: keep it finite (it is never stored)
-      if (mx == -INFINITY) mx = 0.0f;
-      if (__any_sync(0xFFFFFFFFu, mx > m_ref + 8.0f)) {
-        // move the reference maximum of every row of the warp to max(m_ref, mx): O and l scale
-        // by 2^(m_ref - m_new) (1 for rows whose maximum did not grow); O holds P V of the
-        // earlier tiles once their MMAs are done
-        const float m_new = fmaxf(m_ref, mx);
-        const float alpha = ex2(m_ref - m_new);
-        if (j > 0) {
-          const bool done = bwait(bar(B_ODONE + t), (uint32_t)((j - 1) & 1), abort_flag);
-          if (!__all_sync(0xFFFFFFFFu, done)) {
+      const float inv = 1.0f / l_sum;
+      // O / l in 64-column boxes staged in shared memory (the 128B-swizzled layout of the
+      // output map: 16-byte chunk k of row m at chunk k ^ (m % 8)) and stored by TMA; rows
+      // past the sequence lie outside the map and are not written
+#pragma unroll 1
+      for (int hb = 0; hb < D / 64; ++hb, ++nst) {
+        if (nst > 0) {
+          // the box is free once the previous store has read it
+          if (leader) {
+            bulk_wait_read();
+            mbar_arrive(bar(B_OSFREE + t));
+          }
+          const bool fr = bwait(bar(B_OSFREE + t), (uint32_t)((nst - 1) & 1), abort_flag);
+          if (!__all_sync(0xFFFFFFFFu, fr)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          // 16 columns at a time: the row of S stays in registers meanwhile
-#pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t w[16];
-            tmem_ld16(lane_addr + o_col(t) + 16 * c, w);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-            tmem_st16(lane_addr + o_col(t) + 16 * c, w);
-          }
-          tmem_wait_st();
         }
-        l_sum *= alpha;
-        m_ref = m_new;
-      }
-      uint32_t pw[KT / 2];
-      float lsum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < KT; c += 2) {
-        const float p0 = ex2(v[c] - m_ref), p1 = ex2(v[c + 1] - m_ref);
-        lsum += p0 + p1;
-        pw[c / 2] = pack_h2(p0, p1);
-      }
-      l_sum += lsum;
-      // P over the first 64 columns of this row's S (two fp16 per column)
-      tmem_st32(lane_addr + s_col(t), pw);
-      tmem_st32(lane_addr + s_col(t) + 32, pw + 32);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + t));
-    }
-    bool fin = ok && nt > 0;
-    if (fin) fin = bwait(bar(B_ODONE + t), (uint32_t)((nt - 1) & 1), abort_flag);
-    if (__all_sync(0xFFFFFFFFu, fin)) {
-      tc_fence_after();
-      const float inv = 1.0f / l_sum;
-      uint16_t* orow = out + ((int64_t)row_base + qi) * pa.h + hd * D;
+        for (int c = 0; c < 2; ++c) {
+          float o[32];
+          tmem_ld32(lane_addr + o_col(t) + 64 * hb + 32 * c, o);
+          tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
-        tmem_wait_ld();
-        if (qi < s) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_h2(o[i] * inv, o[i + 1] * inv);
-            w.y = pack_h2(o[i + 2] * inv, o[i + 3] * inv);
-            w.z = pack_h2(o[i + 4] * inv, o[i + 5] * inv);
-            w.w = pack_h2(o[i + 6] * inv, o[i + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * c + i) = w;
+          for (int i = 0; i < 4; ++i) {
+            const int k = 4 * c + i;
+            const float* e = o + 8 * i;
+            st_shared_v4(stage + 128 * m + ((k ^ (m & 7)) << 4), pack_h2(e[0] * inv, e[1] * inv),
+                         pack_h2(e[2] * inv, e[3] * inv), pack_h2(e[4] * inv, e[5] * inv),
+                         pack_h2(e[6] * inv, e[7] * inv));
           }
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OSTAGED + t));
+        if (leader && bwait(bar(B_OSTAGED + t), (uint32_t)(nst & 1), abort_flag)) {
+          tma_store_3d(&tmO, stage, it.hd * D + 64 * hb, it.q0 + t * QT, it.b);
+          bulk_commit();
+        }
+        __syncwarp();
       }
     }
+    // the CTA's shared memory stays valid until its stores have completed
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -448,32 +581,38 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const PArgsA p
 
 template <int D>
 cudaError_t launch_d(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, float scale,
-                     uint16_t* out, cudaStream_t st) {
+                     uint16_t* out, int nsm, cudaStream_t st) {
   static cudaError_t attr = cudaFuncSetAttribute(
       prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<D>::BYTES);
   if (attr != cudaSuccess) return attr;
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   const int64_t h = (int64_t)H * D;
-  CUtensorMap tm;
+  CUtensorMap tm, tmo;
   e = make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qkv, (uint64_t)(3 * h),
                   (uint64_t)nseq * s, (uint64_t)(3 * h) * 2, 64, QT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
+  // the output as [nseq][s][h]: a box never spills into the next sequence's rows
+  e = make_map_3d(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, out, (uint64_t)h, (uint64_t)s,
+                  (uint64_t)nseq, (uint64_t)h * 2, (uint64_t)s * h * 2, 64, QT,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
   const int qblocks = (s + QB - 1) / QB;
   const PArgsA pa{nseq, s, H, (int)h, qblocks, scale * 1.4426950408889634f};
-  const int64_t grid = (int64_t)nseq * H * qblocks;
-  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const int64_t items = (int64_t)nseq * H * qblocks;
+  if (items > 0x7FFFFFFF || (int64_t)nseq * s > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const int64_t grid = std::min<int64_t>(items, std::max(1, nsm));   // one CTA per SM
   return launch_pdl(prefill_attn_tc_kernel<D>, dim3((unsigned)grid), dim3(THREADS),
-                    PSmem<D>::BYTES, st, tm, pa, out);
+                    PSmem<D>::BYTES, st, tm, tmo, pa);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
-                                int32_t d, float scale, uint16_t* out, cudaStream_t st) {
+                                int32_t d, float scale, uint16_t* out, int nsm, cudaStream_t st) {
   if (nseq == 0 || s == 0) return cudaSuccess;
-  return d == 128 ? launch_d<128>(qkv, nseq, s, H, scale, out, st)
-                  : launch_d<64>(qkv, nseq, s, H, scale, out, st);
+  return d == 128 ? launch_d<128>(qkv, nseq, s, H, scale, out, nsm, st)
+                  : launch_d<64>(qkv, nseq, s, H, scale, out, nsm, st);
 }
 
 cudaError_t prefill_read_error(unsigned int* out) {

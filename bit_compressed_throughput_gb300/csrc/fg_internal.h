@@ -24,7 +24,7 @@ cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64
 cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* g,
                              const uint16_t* b, float eps, uint16_t* y, cudaStream_t st);
 cudaError_t launch_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H,
-                                int32_t d, float scale, uint16_t* out, cudaStream_t st);
+                                int32_t d, float scale, uint16_t* out, int nsm, cudaStream_t st);
 
 // Launch with programmatic stream serialisation (see pdl_wait in fg_common.cuh).
 template <typename... KArgs, typename... Args>

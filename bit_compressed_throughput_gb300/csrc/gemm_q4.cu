@@ -811,6 +811,19 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 }
 
 
+cudaError_t make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t mid, uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
+                        uint32_t box_inner, uint32_t box_mid, CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[3] = {inner, mid, outer};
+  const cuuint64_t strides[2] = {mid_bytes, outer_bytes};
+  const cuuint32_t box[3] = {box_inner, box_mid, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Weight-streaming plan (M <= 128): one token tile, 128-channel tiles, K split so that the
 // busiest persistent CTA (units taken round-robin) has the fewest k-blocks, counting about
 // two k-blocks of pipeline ramp per unit and 24 (~6 us) for a split's partials and reduce

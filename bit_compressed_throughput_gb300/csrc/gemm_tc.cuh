@@ -202,6 +202,11 @@ cudaError_t get_encode();
 cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                         uint32_t box_outer, CUtensorMapSwizzle swz);
+// A 3-D map over [outer][mid][inner] elements (strides in bytes); boxes are one deep in the
+// outer dimension.
+cudaError_t make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t mid, uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
+                        uint32_t box_inner, uint32_t box_mid, CUtensorMapSwizzle swz);
 
 // Weight-streaming GEMM for M <= 128 tokens: enqueues the main kernel on `st` (the caller
 // launches the split-K reduce when p.splits > 1).  tmX is the tiled kernel's X map (64 k x

@@ -4,6 +4,7 @@ one hot-path kernel at a workload's shape, inputs larger than L2 and a few GB at
     python -m bit_compressed_throughput_gb300.profile_cases gemm-fc1-opt67b
     python -m bit_compressed_throughput_gb300.profile_cases decode-attn-opt67b
     python -m bit_compressed_throughput_gb300.profile_cases decode-attn-kv
+    python -m bit_compressed_throughput_gb300.profile_cases prefill-attn-opt67b
 
 Inputs are seeded random device tensors (no parity check here; the tests do that).
 """
@@ -59,6 +60,18 @@ def attn_case(B, H, d, length, reps, topk=0):
     torch.cuda.synchronize()
 
 
+def prefill_case(nseq, s, H, d, reps):
+    import torch
+    from bit_compressed_throughput_gb300 import fg
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    qkv = torch.randn((nseq * s, 3 * H * d), generator=g, device="cuda").half()
+    out = torch.empty((nseq * s, H * d), dtype=torch.float16, device="cuda")
+    for _ in range(1 + reps):
+        fg.fg_prefill_attn(qkv, nseq, s, H, d, 1.0 / math.sqrt(d), out)
+    fg.fg_check_device_error()
+
+
 CASES = {
     # 6.7B prefill FC1 of one GPU batch: M = 16*512, K = 4096, N = 16384, ReLU
     "gemm-fc1-opt67b": lambda r: gemm_case(8192, 4096, 16384, 1, r),
@@ -74,6 +87,10 @@ CASES = {
     "decode-attn-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r),
     # top-K sparse attention on the quarter KV workload: the top 10% (106 of 1056 positions)
     "decode-attn-topk-kv-quarter": lambda r: attn_case(128, 56, 128, 1056, r, topk=106),
+    # 6.7B prefill attention of one GPU batch: 16 sequences x 32 heads x 512 (201 MB of QKV)
+    "prefill-attn-opt67b": lambda r: prefill_case(16, 512, 32, 128, r),
+    # KV-workload prefill attention, a quarter of one GPU batch: 32 x 56 heads x 1024 (1.3 GB)
+    "prefill-attn-kv-quarter": lambda r: prefill_case(32, 1024, 56, 128, r),
     # top-K on the full KV workload (launch lists only: 4.3 GB of cache)
     "decode-attn-topk-kv": lambda r: attn_case(512, 56, 128, 1056, r, topk=106),
 }

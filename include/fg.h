@@ -233,7 +233,9 @@ size_t fg_decode_attn_topk_workspace_bytes(const fg_kvcache* kv, int32_t len);
 
 /* Causal prefill attention over fp16 Q/K/V read from a QKV buffer qkv[nseq*s][3h]
  * (columns q | k | v, head hd at hd*d): out[nseq*s][h] fp16, position i attends over
- * positions 0..i of its own sequence, scores scaled by `scale`.  d in {64, 128}.
+ * positions 0..i of its own sequence, scores scaled by `scale`.  d in {64, 128}, scale > 0,
+ * nseq <= 65535, nseq * s < 2^31; qkv and out device pointers, 16-byte aligned (FG_ERR_ARG
+ * otherwise).  nseq == 0 or s == 0 is a no-op.
  * [FlexGen paper explainer, Figure 2: the prefill step processes all prompt tokens] */
 int fg_prefill_attn(const uint16_t* qkv, int32_t nseq, int32_t s, int32_t H, int32_t d,
                     float scale, uint16_t* out, void* stream);
