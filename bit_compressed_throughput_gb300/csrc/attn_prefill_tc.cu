@@ -14,17 +14,22 @@
 //                 the diagonal tile and past the sequence, online base-2 softmax with a lazily
 //                 moved reference maximum (rescale only when a row's maximum grows by more
 //                 than 2^8), P = 2^(s - m) rounded to fp16 and written back over the first 64
-//                 columns of the row's S (two fp16 per column)
+//                 columns of the row's S (two fp16 per column).  Two passes over the row (the
+//                 maximum, then P 64 columns at a time) keep a thread within 128 registers.
 //   O += P V      tcgen05.mma with A = P read from TMEM (K = 128 keys), B = the V tile
 //                 (MN-major: keys are its K, the head dimension its N); O (fp32) in TMEM
 // The two Q tiles ping-pong: while one tile's softmax warps work on S, the tensor core runs the
 // other tile's products.  TMEM: S of A and B (128 columns each), O of A and B (d columns each).
-//   warp 0      TMA producer: the two Q tiles once, then K/V tiles into a 2-stage ring
+//   warp 0      TMA producer: the two Q tiles of a block, then its K/V tiles into a 2-stage ring
 //   warp 1      MMA issuer: S_A(0), S_B(0); then per key tile j and Q tile t: P_t(j) V_j into
 //               O_t, then S_t(j + 1) (the tensor core runs one thread's MMAs in issue order, so
 //               S_t(j + 1) overwrites the columns of P_t(j) only after P_t(j) V_j has read them)
-//   warps 2-5   softmax of Q tile A (warp w owns TMEM lanes 32 (w % 4) ..)
-//   warps 6-9   softmax of Q tile B
+//   warps 4-7   softmax of Q tile A (warp w owns TMEM lanes 32 (w % 4) ..)
+//   warps 8-11  softmax of Q tile B
+//   warps 12-15 output: O_t / l of a finished block from TMEM, fp16, staged in shared memory,
+//               stored by TMA; a block's first P V product into O_t waits until they have
+//               read the previous block's O_t, so the softmax warps go on to the next block
+//               while the output is written
 // A Q tile sees key tiles 0 .. (its last row) / 128; tiles wholly above its rows are skipped.
 // The kernel is persistent (one CTA per SM over the blocks, heaviest first), so the next block's
 // loads and first products overlap the current block's softmax and output.
@@ -50,8 +55,9 @@ constexpr int QT = 128;                     // query rows per Q tile (MMA M, TME
 constexpr int KT = 128;                     // keys per K/V tile
 constexpr int QB = 2 * QT;                  // query rows per CTA
 constexpr int STAGES = 2;                   // K/V ring
-constexpr int THREADS = 10 * 32;
-constexpr int SM_B0 = 6;                    // first softmax warp of Q tile B (A: warp 2)
+constexpr int THREADS = 16 * 32;           // 128 registers a thread
+constexpr int W_SM_A = 4, W_SM_B = 8;      // first softmax warp of Q tile A, of Q tile B
+constexpr int W_OUT = 12;                   // first output warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int BOX = QT * 128;               // bytes of one 64-column x 128-row box
@@ -62,16 +68,18 @@ struct PSmem {
   static constexpr int Q_OFF = 0;                      // Q_A, Q_B
   static constexpr int K_OFF = 2 * TILE;               // K stages
   static constexpr int V_OFF = K_OFF + STAGES * TILE;  // V stages
-  static constexpr int O_OFF = V_OFF + STAGES * TILE;  // one output box per Q tile
-  static constexpr int BAR_OFF = O_OFF + 2 * BOX;
+  static constexpr int O_OFF = V_OFF + STAGES * TILE;  // two output boxes
+  static constexpr int L_OFF = O_OFF + 2 * BOX;        // row sums l of A and B (fp32)
+  static constexpr int BAR_OFF = L_OFF + 2 * QT * 4;
   static constexpr int BYTES = BAR_OFF + 256 + 1024;   // barriers; 1024 for alignment
 };
 static_assert(PSmem<128>::BYTES <= 227 * 1024, "shared memory per CTA");
 
-// barriers: q_full, q_free, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2],
-// o_staged[2], o_stage_free[2], drain
+// barriers: q_full, q_free, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2], o_free[2],
+// l_full[2], o_staged, o_stage_free, drain
 constexpr int B_QFULL = 0, B_QFREE = 1, B_KVFULL = 2, B_KVFREE = 4, B_SFULL = 6, B_PFULL = 8,
-              B_ODONE = 10, B_OSTAGED = 12, B_OSFREE = 14, B_DRAIN = 16, NBARS = 17;
+              B_ODONE = 10, B_OFREE = 12, B_LFULL = 14, B_OSTAGED = 16, B_OSFREE = 17,
+              B_DRAIN = 18, NBARS = 19;
 static_assert(NBARS * 8 + 8 <= 256, "barrier space");
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -111,9 +119,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// the shared-memory sources of this thread's bulk stores have been read
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// the shared-memory sources of all but this thread's latest bulk store have been read
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // this thread's bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() {
@@ -151,17 +159,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -169,6 +166,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
+      : "memory");
+}
+// Waits for this thread's TMEM loads and ties the 32 values of one to the wait, so that no
+// use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+        "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
+        "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
+        "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+      :
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
@@ -183,21 +193,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for a share of the exponentials so that the special-function unit
-// (one ex2 per element otherwise, as much time per key tile as the tensor core's) is not the
-// bottleneck.  Range reduction to the nearest integer n (x = n + f, |f| <= 1/2; adding
-// 1.5 * 2^23 rounds x to an integer), a cubic for 2^f whose coefficients were fitted for this
-// kernel (relative error at most 1.1e-4 on [-1/2, 1/2], below half an fp16 step of P), and 2^n
-// added into the exponent field.  x is clamped at -64: P is rounded to fp16, where anything
-// below 2^-25 is zero.
-__device__ __forceinline__ float exp2_poly(float x) {
-  constexpr float kC1 = 0x1.62f5fap-1f, kC2 = 0x1.f00c4ep-3f, kC3 = 0x1.c2a216p-5f;
-  x = fmaxf(x, -64.0f);
-  const float t = x + 12582912.0f;
-  const float n = t - 12582912.0f;
-  const float f = x - n;
-  const float p = fmaf(fmaf(fmaf(kC3, f, kC2), f, kC1), f, 1.0f);
-  return __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
+// Blackwell's three-input maximum and packed two-lane fp32 arithmetic (one instruction for two
+// elements).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // instruction descriptors: D f32, A and B f16, M = 128.  S = Q K^T: both operands K-major,
@@ -236,10 +257,8 @@ __device__ __forceinline__ Item item_of(int i, const PArgsA& pa) {
 
 // Persistent: CTA c takes items c, c + gridDim, ...  The producer loads the next item's Q as
 // soon as the current item's last S product is done and streams K/V through the ring across
-// items; the MMA issuer starts the next item's S products while the softmax warps normalise
-// and store the current item's O.  The next item's first P V product, which overwrites O_t,
-// waits for P_t of that item, which the same softmax warps write only after they have read
-// O_t, so O needs no barrier of its own.
+// items; the MMA issuer starts the next item's S products while the current item's last P V
+// products run, and the output warps store an item's O while the softmax warps work on the next.
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
@@ -252,6 +271,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* l_buf = reinterpret_cast<float*>(smem + L::L_OFF);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
@@ -270,9 +290,11 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
       mbar_init(bar(B_SFULL + t), 1);
       mbar_init(bar(B_PFULL + t), 4);                  // one arrival per softmax warp
       mbar_init(bar(B_ODONE + t), 1);
-      mbar_init(bar(B_OSTAGED + t), 4);                // one arrival per softmax warp
-      mbar_init(bar(B_OSFREE + t), 1);
+      mbar_init(bar(B_OFREE + t), 4);                  // one arrival per output warp
+      mbar_init(bar(B_LFULL + t), 4);                  // one arrival per softmax warp
     }
+    mbar_init(bar(B_OSTAGED), 4);                      // one arrival per output warp
+    mbar_init(bar(B_OSFREE), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -342,7 +364,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
       const uint32_t idesc_o = idesc_pv(D);
       bool ok = true, issued = false;
       int kvg = 0, qn = 0;                             // K/V tiles, items consumed
-      int pc[2] = {0, 0};                              // P V products per Q tile
+      int pc[2] = {0, 0}, uses[2] = {0, 0};            // P V products; items, per Q tile
       // S_t = Q_t K^T of K/V tile g over K = D: k-step i reads 16 columns, 32 bytes into box
       // i / 4
       auto issue_s = [&](int t, int g) {
@@ -389,6 +411,12 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
               ok = false;
               break;
             }
+            // the first product of an item overwrites O_t: the output warps have read it
+            if (j == 0 && uses[t] > 0 &&
+                !bwait(bar(B_OFREE + t), (uint32_t)((uses[t] - 1) & 1), abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             issue_pv(t, g, j == 0);
             ++pc[t];
@@ -409,6 +437,8 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           if (j == it.nkv - 2) umma_commit(bar(B_QFREE));   // the item's last S products
           umma_commit(bar(B_KVFREE + g % STAGES));     // K/V tile g read by every MMA above
         }
+        uses[0] += (it.nt0 > 0);
+        uses[1] += (it.nt1 > 0);
         kvg += it.nkv;
       }
       // the CTA frees TMEM only after every MMA issued here has completed
@@ -417,18 +447,16 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         drain_wait(bar(B_DRAIN), 0u);
       }
     }
-  } else {
+  } else if (warp >= W_SM_A && warp < W_OUT) {
     // ------------------------------------------------------------ softmax of one Q tile
-    const int t = (warp < SM_B0) ? 0 : 1;
+    const int t = (warp < W_SM_B) ? 0 : 1;
     const int quarter = warp & 3;                      // TMEM lanes 32 quarter ..
     const int m = 32 * quarter + lane;                 // row within the Q tile
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t srow = lane_addr + s_col(t);
     const float sl2 = pa.scale_log2;
-    int sc = 0;                                        // S products of this Q tile consumed
-    int nst = 0;                                       // output boxes stored
+    int sc = 0, uses = 0;                              // S products consumed, items finished
     bool ok = true;
-    const bool leader = (warp == 2 + 4 * t) && lane == 0;   // issues this tile's stores
-    const uint32_t stage = smem_u32(smem + L::O_OFF + t * BOX);
     // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
     // decided for the whole warp, waits included (a lane that gave up takes its warp along)
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
@@ -444,29 +472,41 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           break;
         }
         tc_fence_after();
-        float v[KT];
-#pragma unroll
-        for (int c = 0; c < KT / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, v + 32 * c);
-        tmem_wait_ld();
-        // mask keys past the row (diagonal tile) or past the sequence; the row maximum in
-        // base 2 (scale > 0, so scaling after the maximum is the same)
+        // keys past the row (diagonal tile) or past the sequence are masked: keys k0 .. k0 +
+        // lim are visible
         const int k0 = j * KT;
-        const bool masked = (k0 + KT - 1 > it.q0 + t * QT) || (k0 + KT > s);
-        if (masked) {
-          const int lim = min(qi, s - 1) - k0;         // keys k0 .. k0 + lim are visible
+        const bool masked = (k0 + KT - 1 > it.q0 + t * QT) || (k0 + KT > s);   // warp-uniform
+        const int lim = min(qi, s - 1) - k0;
+        // pass 1: the row maximum, 32 columns at a time (the next chunk's TMEM load in flight
+        // meanwhile), four independent running maxima
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        auto max_chunk = [&](float (&v)[32], int c4) {
+          if (masked) {
 #pragma unroll
-          for (int c = 0; c < KT; ++c) v[c] = (c <= lim) ? v[c] : -INFINITY;
+            for (int c = 0; c < 32; ++c) v[c] = (32 * c4 + c <= lim) ? v[c] : -INFINITY;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], v[c], v[c + 1]);
+        };
+        {
+          float va[32], vb[32];
+          tmem_ld32(srow, va);
+          tmem_wait_ld_dep(va);
+          tmem_ld32(srow + 32, vb);
+          max_chunk(va, 0);
+          tmem_wait_ld_dep(vb);
+          tmem_ld32(srow + 64, va);
+          max_chunk(vb, 1);
+          tmem_wait_ld_dep(va);
+          tmem_ld32(srow + 96, vb);
+          max_chunk(va, 2);
+          tmem_wait_ld_dep(vb);
+          max_chunk(vb, 3);
         }
-        // eight independent running maxima, so that the reduction is not one long chain
-        float m8[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) m8[c] = v[c];
-#pragma unroll
-        for (int c = 8; c < KT; ++c) m8[c & 7] = fmaxf(m8[c & 7], v[c]);
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        // a row that sees no key keeps a finite maximum (such rows lie past the sequence and
-        // are never stored)
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // in base 2 (scale > 0, so scaling after the maximum is the same); a row that sees no
+        // key keeps a finite maximum (such rows lie past the sequence and are never stored)
         mx = (mx == -INFINITY) ? 0.0f : mx * sl2;
         if (__any_sync(0xFFFFFFFFu, mx > m_ref + 8.0f)) {
           // move the reference maximum of every row of the warp to max(m_ref, mx): O and l
@@ -481,7 +521,6 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
               break;
             }
             tc_fence_after();
-            // 16 columns at a time: the row of S stays in registers meanwhile
 #pragma unroll
             for (int c = 0; c < D / 16; ++c) {
               uint32_t w[16];
@@ -496,74 +535,133 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           l_sum *= alpha;
           m_ref = m_new;
         }
-        uint32_t pw[KT / 2];
-        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};       // four partial row sums
-        // p = 2^(s * scale - m_ref): one element in four on the FMA pipe, the rest on ex2
+        // pass 2: p = 2^(s * scale - m_ref), 32 columns at a time (the scaling and the row sums
+        // two elements per instruction), packed to fp16 over columns 16 c4 .. of the row's S
+        // (S columns that have been read)
+        const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m_ref, -m_ref);
+        uint64_t ls2[2] = {f2pack(0.0f, 0.0f), f2pack(0.0f, 0.0f)};
+        auto p_chunk = [&](float (&v)[32], int c4) {
+          if (masked) {
 #pragma unroll
-        for (int c = 0; c < KT; c += 2) {
-          const float x0 = fmaf(v[c], sl2, -m_ref), x1 = fmaf(v[c + 1], sl2, -m_ref);
-          const float p0 = ex2(x0);
-          const float p1 = ((c & 3) == 2) ? exp2_poly(x1) : ex2(x1);
-          ls[(c >> 1) & 3] += p0 + p1;
-          pw[c / 2] = pack_h2(p0, p1);
+            for (int c = 0; c < 32; ++c) v[c] = (32 * c4 + c <= lim) ? v[c] : -INFINITY;
+          }
+          uint32_t pw[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = f2unpack(ffma2(f2pack(v[c], v[c + 1]), sl2x2, negm2));
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            ls2[(c >> 1) & 1] = fadd2(ls2[(c >> 1) & 1], f2pack(p0, p1));
+            pw[c / 2] = pack_h2(p0, p1);
+          }
+          tmem_st16(srow + 16 * c4, pw);
+        };
+        {
+          float va[32], vb[32];
+          tmem_ld32(srow, va);
+          tmem_wait_ld_dep(va);
+          tmem_ld32(srow + 32, vb);
+          p_chunk(va, 0);
+          tmem_wait_ld_dep(vb);
+          tmem_ld32(srow + 64, va);
+          p_chunk(vb, 1);
+          tmem_wait_ld_dep(va);
+          tmem_ld32(srow + 96, vb);
+          p_chunk(va, 2);
+          tmem_wait_ld_dep(vb);
+          p_chunk(vb, 3);
         }
-        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // P over the first 64 columns of this row's S (two fp16 per column)
-        tmem_st32(lane_addr + s_col(t), pw);
-        tmem_st32(lane_addr + s_col(t) + 32, pw + 32);
         tmem_wait_st();
+        const float2 la = f2unpack(fadd2(ls2[0], ls2[1]));
+        l_sum += la.x + la.y;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_PFULL + t));
       }
       if (!ok) break;
-      // the item's O: wait for its last P V product, normalise, store
-      const bool fin = bwait(bar(B_ODONE + t), (uint32_t)((sc - 1) & 1), abort_flag);
-      if (!__all_sync(0xFFFFFFFFu, fin)) {
-        ok = false;
-        break;
+      // the item's row sums for the output warps, once they have taken the previous item's
+      if (uses > 0) {
+        const bool fr = bwait(bar(B_OFREE + t), (uint32_t)((uses - 1) & 1), abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, fr)) {
+          ok = false;
+          break;
+        }
       }
-      tc_fence_after();
-      const float inv = 1.0f / l_sum;
-      // O / l in 64-column boxes staged in shared memory (the 128B-swizzled layout of the
-      // output map: 16-byte chunk k of row m at chunk k ^ (m % 8)) and stored by TMA; rows
-      // past the sequence lie outside the map and are not written
+      l_buf[t * QT + m] = l_sum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_LFULL + t));
+      ++uses;
+    }
+  } else if (warp >= W_OUT) {
+    // ------------------------------------------------------------ output of both Q tiles
+    const int quarter = warp & 3;
+    const int m = 32 * quarter + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const bool leader = (warp == W_OUT) && lane == 0;  // issues the stores
+    int cum[2] = {0, 0}, uses[2] = {0, 0}, nbox = 0;   // P V products, items, boxes stored
+    bool ok = true;
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+      const Item it = item_of(item, pa);
+      for (int t = 0; t < 2 && ok; ++t) {
+        const int nt = t ? it.nt1 : it.nt0;
+        if (nt == 0) continue;
+        cum[t] += nt;
+        // the row sums, then the item's last P V product into O_t
+        bool got = bwait(bar(B_LFULL + t), (uint32_t)(uses[t] & 1), abort_flag);
+        got = got && bwait(bar(B_ODONE + t), (uint32_t)((cum[t] - 1) & 1), abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        ++uses[t];
+        const float inv = 1.0f / l_buf[t * QT + m];
+        // O / l in 64-column boxes, staged in shared memory (the 128B-swizzled layout of the
+        // output map: 16-byte chunk k of row m at chunk k ^ (m % 8)) and stored by TMA; rows
+        // past the sequence lie outside the map and are not written
 #pragma unroll 1
-      for (int hb = 0; hb < D / 64; ++hb, ++nst) {
-        if (nst > 0) {
-          // the box is free once the previous store has read it
-          if (leader) {
-            bulk_wait_read();
-            mbar_arrive(bar(B_OSFREE + t));
+        for (int hb = 0; hb < NB; ++hb, ++nbox) {
+          const uint32_t stage = smem_u32(smem + L::O_OFF + (nbox & 1) * BOX);
+          if (nbox >= 2) {
+            // the box is free once the store issued from it two boxes ago has read it
+            if (leader) {
+              bulk_wait_read_1();
+              mbar_arrive(bar(B_OSFREE));
+            }
+            const bool fr = bwait(bar(B_OSFREE), (uint32_t)((nbox - 2) & 1), abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, fr)) {
+              ok = false;
+              break;
+            }
           }
-          const bool fr = bwait(bar(B_OSFREE + t), (uint32_t)((nst - 1) & 1), abort_flag);
-          if (!__all_sync(0xFFFFFFFFu, fr)) {
-            ok = false;
-            break;
-          }
-        }
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float o[32];
-          tmem_ld32(lane_addr + o_col(t) + 64 * hb + 32 * c, o);
-          tmem_wait_ld();
+          for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tmem_ld32(lane_addr + o_col(t) + 64 * hb + 32 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int k = 4 * c + i;
-            const float* e = o + 8 * i;
-            st_shared_v4(stage + 128 * m + ((k ^ (m & 7)) << 4), pack_h2(e[0] * inv, e[1] * inv),
-                         pack_h2(e[2] * inv, e[3] * inv), pack_h2(e[4] * inv, e[5] * inv),
-                         pack_h2(e[6] * inv, e[7] * inv));
+            for (int i = 0; i < 4; ++i) {
+              const int k = 4 * c + i;
+              const float* e = o + 8 * i;
+              st_shared_v4(stage + 128 * m + ((k ^ (m & 7)) << 4),
+                           pack_h2(e[0] * inv, e[1] * inv), pack_h2(e[2] * inv, e[3] * inv),
+                           pack_h2(e[4] * inv, e[5] * inv), pack_h2(e[6] * inv, e[7] * inv));
+            }
           }
+          if (hb == NB - 1) {
+            // O_t has been read: the next item's first P V product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_OFREE + t));
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_OSTAGED));
+          if (leader && bwait(bar(B_OSTAGED), (uint32_t)(nbox & 1), abort_flag)) {
+            tma_store_3d(&tmO, stage, it.hd * D + 64 * hb, it.q0 + t * QT, it.b);
+            bulk_commit();
+          }
+          __syncwarp();
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OSTAGED + t));
-        if (leader && bwait(bar(B_OSTAGED + t), (uint32_t)(nst & 1), abort_flag)) {
-          tma_store_3d(&tmO, stage, it.hd * D + 64 * hb, it.q0 + t * QT, it.b);
-          bulk_commit();
-        }
-        __syncwarp();
       }
     }
     // the CTA's shared memory stays valid until its stores have completed
