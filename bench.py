@@ -338,11 +338,37 @@ def merged_gemm(prof):
     return "+".join(kinds) or TENSOR_GEMMS[0], rec
 
 
+def prefill_attn_roof(wl, rec, pk, steps):
+    """Causal prefill attention against the roof that binds at its arithmetic intensity: a
+    launch reads Q, K and V (3h fp16 columns per token of its g sequences) and writes the
+    output (h columns), 8*g*s*h bytes, for 2*g*h*s*(s+1) flops.  At s = 512 that is s/4 = 128
+    flop per byte, below the ridge of the measured peaks (~265), so the HBM floor is the
+    higher one; the tensor fraction is reported beside it."""
+    if not rec or not rec["launches"] or not rec["ms"]:
+        return None
+    nbytes = 8.0 * wl.g * wl.s * wl.h * rec["launches"]
+    flops = rec["work"]
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_sustained"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    tensor = roof("prefill_attn", rec, pk, "tensor", steps)
+    if bound == "tensor":
+        r = tensor
+    else:
+        r = roof("prefill_attn", dict(rec, work=nbytes), pk, "hbm", steps)
+        r["tensor_frac"] = tensor["frac"]
+        r["tensor_achieved_tflops"] = tensor["achieved"]
+    r["flop_per_byte"] = round(flops / nbytes, 1)
+    r["ridge_flop_per_byte"] = round(pk["bf16_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9), 1)
+    r["bytes_per_launch"] = int(8 * wl.g * wl.s * wl.h)
+    return r
+
+
 def phase_rooflines(wl, pre, dec, pk, psteps):
     """Rooflines of the prefill and decode kernels of one workload."""
     pname, prec = merged_gemm(pre)
     out = {"prefill_gemm": roof(pname, prec, pk, "tensor", psteps),
-           "prefill_attn": roof("prefill_attn", pre["prefill_attn"], pk, "tensor", psteps),
+           "prefill_attn": prefill_attn_roof(wl, pre["prefill_attn"], pk, psteps),
            "decode_attn": roof("q4kv_decode_attn", dec["q4kv_decode_attn"], pk, "hbm", psteps,
                                {"lengths": f"{wl.s + 1}..{wl.s + wl.n - 1}",
                                 "sequences_x_heads": wl.B * wl.H})}

@@ -122,7 +122,6 @@ static_assert((RG & (RG - 1)) == 0, "stage positions by mask");
 // on those of it - r.
 static_assert(TMEM_COLS == 512, "TMEM budget: two 256-column accumulators");
 constexpr long long kWaitCycles = 1ll << 32;
-constexpr int SWZ_GROUP = 8;                // token tiles per raster group
 
 // instruction descriptor: D f32, A and B f16, A MN-major, B K-major, M = 256 (the pair),
 // N = tn (both CTAs' tokens)
@@ -184,26 +183,6 @@ struct PUnit {
   int t0, c0, split, kb_begin, kb_end;     // c0: the pair's first channel
 };
 
-// Work unit u -> token tile, channel pair and k-block range; SWZ_GROUP token tiles share a
-// wave of channel pairs.
-__device__ __forceinline__ PUnit pair_unit(int u, int tn, int tiles_t, int pairs, int kblocks,
-                                           int kb_per_split) {
-  PUnit r;
-  const int tiles = tiles_t * pairs;
-  r.split = u / tiles;
-  const int lin = u - r.split * tiles;
-  const int group_span = SWZ_GROUP * pairs;
-  const int grp = lin / group_span;
-  const int first_t = grp * SWZ_GROUP;
-  const int gt = min(SWZ_GROUP, tiles_t - first_t);
-  const int within = lin - grp * group_span;
-  r.t0 = (first_t + within % gt) * tn;
-  r.c0 = (within / gt) * (2 * TCH);
-  r.kb_begin = r.split * kb_per_split;
-  r.kb_end = min(kblocks, r.kb_begin + kb_per_split);
-  return r;
-}
-
 struct PArgs {
   int M, N, K;
   int tiles_t, pairs, kblocks, kb_per_split, units;
@@ -212,7 +191,31 @@ struct PArgs {
   int rc;              // code ring depth in stages, <= RC_MAX (a multiple of RG when sk = 1)
   int sk;              // k-blocks per code stage: 1, or RG (whole stages in every unit)
   int xslot;           // bytes per X slot: tnh * 128 rounded up to 1024
+  int grp;             // token tiles per raster group
 };
+
+// Work unit u -> split, token tile, channel pair and k-block range.  Within a split the
+// units run in raster groups of `grp` token tiles x every channel pair, token tile fastest:
+// the clusters working at one time (76 on a GB300) cover grp token tiles and 76 / grp
+// channel pairs, so each k-block of X is read from HBM once for 76 / grp clusters and each
+// k-block of codes once for grp.
+__device__ __forceinline__ PUnit pair_unit(int u, int tn, const PArgs& ka) {
+  PUnit r;
+  const int tiles = ka.tiles_t * ka.pairs;
+  r.split = u / tiles;
+  const int lin = u - r.split * tiles;
+  const int span = ka.grp * ka.pairs;
+  const int g = lin / span;
+  const int first = g * ka.grp;
+  const int gn = min(ka.grp, ka.tiles_t - first);
+  const int within = lin - g * span;
+  r.t0 = (first + within % gn) * tn;
+  r.c0 = (within / gn) * (2 * TCH);
+  r.kb_begin = r.split * ka.kb_per_split;
+  r.kb_end = min(ka.kblocks, r.kb_begin + ka.kb_per_split);
+  return r;
+}
+
 
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
@@ -287,7 +290,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       int it = 0, s = 0;                              // loads issued; slot
       uint32_t ph = 0;                                // lap parity of slot s
       for (int u = cl; u < ka.units; u += ncl) {
-        const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+        const PUnit w = pair_unit(u, TN, ka);
         const int c0 = w.c0 + (int)rank * TCH;
         bool ok = true;
         for (int kb = w.kb_begin; kb < w.kb_end; kb += step, ++it) {
@@ -331,7 +334,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       uint32_t ph = 0;
       bool ok = true, issued = false;
       for (int u = cl; u < ka.units && ok; u += ncl, ++tl) {
-        const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+        const PUnit w = pair_unit(u, TN, ka);
         const int acc = tl & 1;
         if (tl >= 2 && !pwait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
@@ -391,7 +394,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint32_t phc = 0, phr = 0;
     bool ok = true;
     for (int u = cl; u < ka.units && ok; u += ncl) {
-      const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+      const PUnit w = pair_unit(u, TN, ka);
       const int g0 = ((w.c0 + (int)rank * TCH) >> 6) & 3;   // first group in the stats box
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
         // code stage c holds SK consecutive k-blocks of the unit; this is its j-th.  With
@@ -468,7 +471,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const uint32_t empty_cl[2] = {mapa_shared(acc_empty(0), 0), mapa_shared(acc_empty(1), 0)};
     int tl = 0;
     for (int u = cl; u < ka.units; u += ncl, ++tl) {
-      const PUnit w = pair_unit(u, TN, ka.tiles_t, ka.pairs, ka.kblocks, ka.kb_per_split);
+      const PUnit w = pair_unit(u, TN, ka);
       const int c0 = w.c0 + (int)rank * TCH;
       const int acc = tl & 1;
       const int ntok = min(TN, ka.M - w.t0);
@@ -620,6 +623,16 @@ static bool pair_rings(const GemmPlan& p, int tnh, int* r_out, int* rc_out, int*
   return true;
 }
 
+// Raster group: X is 3.6x the bytes of the 4-bit codes per k-block and tile, so the clusters
+// working at one time should span many channel pairs and few token tiles; up to 4 token tiles,
+// fewer when the group's X would pass 64 MB (half the L2), e.g. 2 at K = 49152.  Measured at
+// the OPT-175B prefill shapes (18432 tokens): 4 (2 at K = 49152) is 3.5-4% faster than 8,
+// 16 or groups of channel pairs; at the 6.7B shapes the group size makes no difference.
+static int pair_raster_group(const GemmPlan& p) {
+  const double x_tile = (double)p.tn * p.K * 2.0;
+  return (int)std::max(1.0, std::min(4.0, 64e6 / x_tile));
+}
+
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,
                              const EpiArgs& ea, cudaStream_t st) {
   const int maxcl = pair_max_clusters();
@@ -642,8 +655,8 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
                   (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, (uint32_t)(BK * sk),
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  const PArgs ka{(int)p.M, (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
-                 p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot};
+  const PArgs ka{(int)p.M,  (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
+                 p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot, pair_raster_group(p)};
   const int64_t clusters = std::min<int64_t>(p.units, maxcl);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config((unsigned)(2 * clusters), st, attr);

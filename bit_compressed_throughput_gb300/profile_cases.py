@@ -5,6 +5,7 @@ one hot-path kernel at a workload's shape, inputs larger than L2 and a few GB at
     python -m bit_compressed_throughput_gb300.profile_cases decode-attn-opt67b
     python -m bit_compressed_throughput_gb300.profile_cases decode-attn-kv
     python -m bit_compressed_throughput_gb300.profile_cases prefill-attn-opt67b
+    python -m bit_compressed_throughput_gb300.profile_cases gemm-prefill-opt175b --reps 0
 
 Inputs are seeded random device tensors (no parity check here; the tests do that).
 """
@@ -34,6 +35,16 @@ def gemm_case(M, K, N, epi, reps):
     for _ in range(1 + reps):
         fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
     fg.fg_check_device_error()
+
+
+def gemm_shapes(shapes, reps):
+    """Several GEMM shapes one after the other, each with its own tensors (freed before the
+    next shape is allocated)."""
+    import torch
+    for M, K, N, epi in shapes:
+        gemm_case(M, K, N, epi, reps)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
 
 
 def attn_case(B, H, d, length, reps, topk=0):
@@ -77,6 +88,12 @@ CASES = {
     "gemm-fc1-opt67b": lambda r: gemm_case(8192, 4096, 16384, 1, r),
     # 6.7B prefill QKV: N = 3*4096
     "gemm-qkv-opt67b": lambda r: gemm_case(8192, 4096, 12288, 0, r),
+    # OPT-175B prefill projections of one GPU batch (36 sequences x 512 = 18432 tokens):
+    # QKV, O, FC1 (ReLU), FC2 in layer order, at most 2.6 GB on the device at a time
+    "gemm-prefill-opt175b": lambda r: gemm_shapes(((18432, 12288, 36864, 0),
+                                                   (18432, 12288, 12288, 0),
+                                                   (18432, 12288, 49152, 1),
+                                                   (18432, 49152, 12288, 0)), r),
     # 6.7B decode FC1 (M = B = 64, split K)
     "gemm-fc1-decode-opt67b": lambda r: gemm_case(64, 4096, 16384, 1, r),
     # 6.7B decode attention at the last step: 64 sequences x 32 heads x 543 positions
