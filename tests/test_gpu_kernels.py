@@ -655,6 +655,10 @@ def test_decode_attention_topk_kv_workload_sampled(fg):
     (3, 300, 3, 64, 1.5),        # d = 64, ragged second block
     (1, 1024, 1, 128, 1.5),      # four blocks, up to eight key tiles per Q tile
     (2, 640, 2, 128, 4.0),       # large scores: the reference maximum moves many times
+    # more blocks than SMs: every persistent CTA takes several blocks (next block's loads and
+    # first products during the previous block's output), ragged last blocks
+    (3, 700, 24, 128, 1.5),
+    (4, 520, 20, 64, 1.5),
 ])
 def test_prefill_attention(fg, nseq, s, H, d, mag):
     h = H * d
