@@ -331,7 +331,7 @@ def kernel_table(prof, steps):
             for k, v in prof.items() if v["launches"]}
 
 
-TENSOR_GEMMS = ("q4_dequant_gemm_pair", "q4_dequant_gemm_tc")
+TENSOR_GEMMS = ("gemm_f16w_pair", "q4_dequant_gemm_pair", "q4_dequant_gemm_tc")
 
 
 def merged_gemm(prof):

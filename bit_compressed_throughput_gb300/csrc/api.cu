@@ -233,16 +233,25 @@ KvOut kv_out(const fg_kvcache& kv, int T, int pos) {
 
 // ---------------------------------------------------------------- timed launches
 // kv: the QKV projection's K/V append in the GEMM epilogue (null: none).
+// Profiler kind of a plan's main kernel.
+int gemm_kind(const GemmPlan& p, const uint16_t* w16) {
+  if (p.kind == kGemmStream) return FG_K_GEMM_STREAM;
+  if (p.kind == kGemmPair) return w16 ? FG_K_GEMM_PAIR_F16W : FG_K_GEMM_PAIR;
+  return FG_K_GEMM;
+}
+
+// w16 (nullable): W restored to fp16 [K][N], used by a CTA-pair plan instead of the codes.
 int run_gemm(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bias, int epi,
              const uint16_t* residual, uint16_t* Y, void* ws, int sms, cudaStream_t st,
-             const KvOut* kv = nullptr) {
+             const KvOut* kv = nullptr, const uint16_t* w16 = nullptr) {
   const GemmPlan p = gemm_plan(M, W.K, W.N, sms, kv == nullptr);
+  if (p.kind != kGemmPair) w16 = nullptr;
   Span sp(st);
   cudaEvent_t mid = (p.splits > 1) ? sp.mid_event() : nullptr;
-  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, kv);
+  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, kv, nullptr, w16);
   if (e != cudaSuccess) return set_cuda_error(e);
   const bool stream = (p.kind == kGemmStream);
-  const int kind = stream ? FG_K_GEMM_STREAM : (p.kind == kGemmPair ? FG_K_GEMM_PAIR : FG_K_GEMM);
+  const int kind = gemm_kind(p, w16);
   // the streaming kernel's work is bytes: with the append, also the 4-bit K/V written
   const double w = stream ? work_gemm_stream(M, W.N, W.K) + (kv ? 2.0 * M * kv->h * 0.5625 : 0.0)
                           : work_gemm(M, W.N, W.K);
@@ -252,6 +261,16 @@ int run_gemm(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bi
   } else {
     sp.stop(kind, w);
   }
+  return FG_OK;
+}
+
+// W restored to fp16 [K][N] for the CTA-pair GEMM's fp16-weight mode: the values of
+// fg_dequant_g64, each run of 8 channels in the GEMM's A-tile order (0,4,1,5,2,6,3,7).
+int run_restore(const fg_q4mat& W, uint16_t* y, cudaStream_t st) {
+  Span sp(st);
+  cudaError_t e = launch_dequant_pairperm(W.codes, W.ab, W.K, W.N, y, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  sp.stop(FG_K_DEQUANT, work_dequant((double)W.K * W.N));
   return FG_OK;
 }
 
@@ -269,20 +288,22 @@ int run_layernorm(const uint16_t* x, int64_t rows, int h, const uint16_t* g, con
 // LayerNorm kernel.
 int run_gemm_ln(const uint16_t* X, int64_t M, const fg_q4mat& W, const uint16_t* bias, int epi,
                 const uint16_t* residual, uint16_t* Y, const uint16_t* g, const uint16_t* b,
-                float eps, uint16_t* y_ln, void* ws, int sms, cudaStream_t st) {
+                float eps, uint16_t* y_ln, void* ws, int sms, cudaStream_t st,
+                const uint16_t* w16 = nullptr) {
   const GemmPlan p = gemm_plan(M, W.K, W.N, sms);
+  if (p.kind != kGemmPair) w16 = nullptr;
   if (p.splits == 1) {
-    int rc = run_gemm(X, M, W, bias, epi, residual, Y, ws, sms, st);
+    int rc = run_gemm(X, M, W, bias, epi, residual, Y, ws, sms, st, nullptr, w16);
     if (rc) return rc;
     return run_layernorm(Y, M, (int)W.N, g, b, eps, y_ln, st);
   }
   Span sp(st);
   cudaEvent_t mid = sp.mid_event();
   const LnOut ln{g, b, eps, y_ln};
-  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, nullptr, &ln);
+  cudaError_t e = launch_gemm(p, X, W, bias, epi, residual, Y, ws, st, mid, nullptr, &ln, w16);
   if (e != cudaSuccess) return set_cuda_error(e);
   const bool stream = (p.kind == kGemmStream);
-  const int kind = stream ? FG_K_GEMM_STREAM : (p.kind == kGemmPair ? FG_K_GEMM_PAIR : FG_K_GEMM);
+  const int kind = gemm_kind(p, w16);
   const double w = stream ? work_gemm_stream(M, W.N, W.K) : work_gemm(M, W.N, W.K);
   if (mid) {
     sp.close(kind, w, mid);
@@ -337,8 +358,13 @@ int run_prefill_attn(const uint16_t* qkv, int nseq, int s, int H, int d, float s
 
 // ---------------------------------------------------------------- layer workspace
 struct LayerWs {
-  size_t ln, qkv, att, h1, mid, gemm, attn, total;
+  size_t ln, qkv, att, h1, mid, gemm, attn, w16, total;
 };
+
+// Prefill restores a layer's weights to fp16 once per call when its GEMMs run on CTA pairs
+// (M > 128): the restore is then done once for all m GPU batches, and the GEMMs load their A
+// tiles by TMA instead of restoring every tile once per token tile (M / 256 times).
+bool prefill_restores(int64_t M) { return M > 128; }
 
 LayerWs layer_ws(const fg_dims& dm, int64_t M, const fg_kvcache* kv_for_decode, int len) {
   LayerWs w{};
@@ -356,7 +382,11 @@ LayerWs layer_ws(const fg_dims& dm, int64_t M, const fg_kvcache* kv_for_decode, 
   }
   w.gemm = round_up(g);
   w.attn = kv_for_decode ? round_up(decode_attn_ws_bytes(*kv_for_decode, len, kMaxSms)) : 0;
-  w.total = w.ln + w.qkv + w.att + w.h1 + w.mid + w.gemm + w.attn;
+  // the four restored matrices (QKV h x 3h, O h x h, FC1 h x f, FC2 f x h)
+  w.w16 = (!kv_for_decode && prefill_restores(M))
+              ? round_up((size_t)(4 * h * h) * 2) + round_up((size_t)(2 * h * f) * 2)
+              : 0;
+  w.total = w.ln + w.qkv + w.att + w.h1 + w.mid + w.gemm + w.attn + w.w16;
   return w;
 }
 
@@ -660,9 +690,25 @@ int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const
   uint16_t* att = reinterpret_cast<uint16_t*>(p); p += w.att;
   uint16_t* h1 = reinterpret_cast<uint16_t*>(p); p += w.h1;
   uint16_t* mid = reinterpret_cast<uint16_t*>(p); p += w.mid;
-  void* gws = p;
+  void* gws = p; p += w.gemm;
   const int h = dm->h;
   const float scale = 1.0f / sqrtf((float)dm->d);
+  // weights restored to fp16 once for the m GPU batches (CTA-pair GEMMs only)
+  const uint16_t *wqkv16 = nullptr, *wo16 = nullptr, *w116 = nullptr, *w216 = nullptr;
+  if (w.w16) {
+    uint16_t* q16 = reinterpret_cast<uint16_t*>(p);
+    uint16_t* o16 = q16 + (int64_t)3 * h * h;
+    uint16_t* f16a = o16 + (int64_t)h * h;
+    uint16_t* f16b = f16a + (int64_t)h * dm->f;
+    if ((rc = run_restore(L->wqkv, q16, st)) || (rc = run_restore(L->wo, o16, st))) return rc;
+    wqkv16 = q16;
+    wo16 = o16;
+    if (dm->f > 0) {
+      if ((rc = run_restore(L->w1, f16a, st)) || (rc = run_restore(L->w2, f16b, st))) return rc;
+      w116 = f16a;
+      w216 = f16b;
+    }
+  }
   for (int k = 0; k < m; ++k) {
     const uint16_t* xk = x + (int64_t)k * M * h;
     uint16_t* yk = y + (int64_t)k * M * h;
@@ -671,18 +717,24 @@ int fg_layer_prefill(const fg_dims* dm, const fg_layer* L, fg_kvcache* kv, const
     // QKV projection, then the 4-bit K/V of positions 0 .. s-1.  The append stays a kernel
     // of its own: quantising in the GEMM epilogue (fg_dequant_gemm_q4_kv) measured slower,
     // the epilogue warps becoming the bottleneck of the K/V tiles
-    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st)))
+    if ((rc = run_gemm(ln, M, L->wqkv, L->bqkv, FG_EPI_NONE, nullptr, qkv, gws, sms, st,
+                       nullptr, wqkv16)))
       return rc;
     if ((rc = run_kv_append(qkv + h, qkv + 2 * h, 3 * h, s, 0, kvk, st))) return rc;
     if ((rc = run_prefill_attn(qkv, g, s, dm->H, dm->d, scale, att, sms, st))) return rc;
     if (dm->f > 0) {
       // O projection + residual into h1, then LN2(h1) (fused into a split-K reduce)
       if ((rc = run_gemm_ln(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, h1, L->ln2_g, L->ln2_b,
-                            dm->ln_eps, ln, gws, sms, st)))
+                            dm->ln_eps, ln, gws, sms, st, wo16)))
         return rc;
-      if ((rc = run_gemm(ln, M, L->w1, L->b1, FG_EPI_RELU, nullptr, mid, gws, sms, st))) return rc;
-      if ((rc = run_gemm(mid, M, L->w2, L->b2, FG_EPI_RESIDUAL, h1, yk, gws, sms, st))) return rc;
-    } else if ((rc = run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, yk, gws, sms, st))) {
+      if ((rc = run_gemm(ln, M, L->w1, L->b1, FG_EPI_RELU, nullptr, mid, gws, sms, st, nullptr,
+                         w116)))
+        return rc;
+      if ((rc = run_gemm(mid, M, L->w2, L->b2, FG_EPI_RESIDUAL, h1, yk, gws, sms, st, nullptr,
+                         w216)))
+        return rc;
+    } else if ((rc = run_gemm(att, M, L->wo, L->bo, FG_EPI_RESIDUAL, xk, yk, gws, sms, st,
+                              nullptr, wo16))) {
       return rc;
     }
   }
@@ -761,7 +813,8 @@ const char* fg_kernel_name(int kind) {
   static const char* names[FG_K_COUNT] = {
       "q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
       "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn",
-      "layernorm", "q4_dequant_gemm_stream", "q4kv_decode_attn_topk", "q4_dequant_gemm_pair"};
+      "layernorm", "q4_dequant_gemm_stream", "q4kv_decode_attn_topk", "q4_dequant_gemm_pair",
+      "gemm_f16w_pair"};
   return (kind >= 0 && kind < FG_K_COUNT) ? names[kind] : "unknown";
 }
 

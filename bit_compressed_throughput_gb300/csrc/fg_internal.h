@@ -19,6 +19,10 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, uint8
                             uint32_t* ab, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64_t cols,
                            uint16_t* y, cudaStream_t st);
+// The same values with each run of 8 channels stored as 0,4,1,5,2,6,3,7: the A-tile order of
+// the CTA-pair GEMM, whose fp16-weight mode loads these instead of restoring.
+cudaError_t launch_dequant_pairperm(const uint8_t* codes, const uint32_t* ab, int64_t rows,
+                                    int64_t cols, uint16_t* y, cudaStream_t st);
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,
                              int32_t T, int32_t pos, const fg_kvcache& kv, cudaStream_t st);
 cudaError_t launch_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* g,
@@ -128,11 +132,13 @@ struct LnOut {
   uint16_t* y;
 };
 // kv: K/V append in the epilogue (null or k_codes == null: none).  ln: LayerNorm in the
-// split-K reduce (only for a split plan; null: none).
+// split-K reduce (only for a split plan; null: none).  w16: W already restored to fp16
+// [K][N] (only the CTA-pair plan uses it; null: restore in the GEMM).
 cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
                         void* ws, cudaStream_t st, cudaEvent_t mid_event,
-                        const KvOut* kv = nullptr, const LnOut* ln = nullptr);
+                        const KvOut* kv = nullptr, const LnOut* ln = nullptr,
+                        const uint16_t* w16 = nullptr);
 // Device error words of the bounded waits (GEMM, decode attention): read-and-clear.
 cudaError_t gemm_read_error(unsigned int* out);
 cudaError_t gemm_stream_read_error(unsigned int* out);
@@ -153,6 +159,7 @@ inline double work_gemm_reduce(int64_t M, int64_t N, int splits) {
   return (double)splits * M * N * 4.0 + 2.0 * M * N;
 }
 inline double work_quantize(double elems) { return elems * (2.0 + 0.5625); }
+inline double work_dequant(double elems) { return elems * (0.5625 + 2.0); }
 inline double work_decode_attn(int64_t B, int64_t len, int64_t h) {
   return 2.0 * B * len * h * 0.5625 + 4.0 * B * h;
 }

@@ -958,7 +958,7 @@ static cudaError_t launch_reduce(const GemmPlan& p, void* ws, const EpiArgs& ea,
 cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
                         const uint16_t* bias, int epi, const uint16_t* residual, uint16_t* Y,
                         void* ws, cudaStream_t st, cudaEvent_t mid_event, const KvOut* kv,
-                        const LnOut* ln) {
+                        const LnOut* ln, const uint16_t* w16) {
   if (p.M == 0) return cudaSuccess;
   if (ln && p.splits == 1) return cudaErrorInvalidValue;     // the caller runs LayerNorm
   cudaError_t e = get_encode();
@@ -986,7 +986,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
   if (p.kind == kGemmPair) {
     if (kv && kv->k_codes) return cudaErrorInvalidValue;   // the append lives in kind 0/1
-    e = launch_gemm_pair(p, W, X, ea, st);
+    e = launch_gemm_pair(p, W, X, ea, st, w16);
     if (e != cudaSuccess || p.splits == 1) return e;
     if (mid_event) cudaEventRecord(mid_event, st);
     return launch_reduce(p, ws, final_ea, ln, st);

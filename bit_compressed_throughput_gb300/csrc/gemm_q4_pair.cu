@@ -95,12 +95,13 @@ constexpr int C_BYTES = BK * TCH / 2;       // 4 KB of codes (64-byte rows)
 constexpr int S_BYTES = BK * 4 * 4;         // 1 KB: (a, b) words of 4 groups x 64 k-rows
 constexpr int CS_BYTES = C_BYTES + S_BYTES; // one code stage
 constexpr int SMEM_BYTES = 232448;          // the whole per-CTA budget
-constexpr int BAR_BYTES = 512;
+constexpr int BAR_BYTES = 1024;
 constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 // barriers: full[R] (CTA 0: the k-block's A and X halves of both CTAs), xfull[R] (this CTA's
 // X half landed), mma_done[R] (the k-block's MMAs done: slot reusable), full_c[RC], free_c[RC],
-// acc_full[2], acc_empty[2] (CTA 0: both CTAs' epilogues read the accumulator), drain
-constexpr int NBARS = 3 * R_MAX + 2 * RC_MAX + 5;
+// acc_full[2], acc_empty[2] (CTA 0: both CTAs' epilogues read the accumulator), drain, and
+// with fp16 weights afull[2][R] (this CTA's two 64-channel halves of the A slot landed)
+constexpr int NBARS = 5 * R_MAX + 2 * RC_MAX + 5;
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;   // two accumulator buffers of 256 columns
 constexpr int FULL_ARRIVALS = 2 * (RTG / 32);   // one per restore warp of a group, both CTAs
 constexpr int EMPTY_ARRIVALS = 2 * 4;           // one per epilogue warp, both CTAs
@@ -192,6 +193,7 @@ struct PArgs {
   int sk;              // k-blocks per code stage: 1, or RG (whole stages in every unit)
   int xslot;           // bytes per X slot: tnh * 128 rounded up to 1024
   int grp;             // token tiles per raster group
+  int w16;             // 1: A slots are loaded by TMA from restored fp16 weights (no restore)
 };
 
 // Work unit u -> split, token tile, channel pair and k-block range.  Within a split the
@@ -219,7 +221,8 @@ __device__ __forceinline__ PUnit pair_unit(int u, int tn, const PArgs& ka) {
 
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
-                    const __grid_constant__ CUtensorMap tmS, const PArgs ka, const EpiArgs ea) {
+                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmA,
+                    const PArgs ka, const EpiArgs ea) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -244,12 +247,15 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   auto acc_full = [&](int a) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + a); };
   auto acc_empty = [&](int a) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 2 + a); };
   const uint32_t drain = bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 4);
+  auto afull = [&](int hf, int r) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 5 + hf * R_MAX + r); };
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < R; ++r) {
-      mbar_init(full(r), FULL_ARRIVALS);
+      mbar_init(full(r), ka.w16 ? 2 : FULL_ARRIVALS);   // fp16 weights: one relay per CTA
       mbar_init(xfull(r), 1);
       mbar_init(mma_done(r), 1);
+      mbar_init(afull(0, r), 1);
+      mbar_init(afull(1, r), 1);
     }
     for (int c = 0; c < RC; ++c) {
       mbar_init(full_c(c), 1);
@@ -286,10 +292,11 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (lane == 0) {
       const bool is_x = (warp == kXWarp);
       const int depth = is_x ? R : RC;
+      const int nunits = (is_x || !ka.w16) ? ka.units : 0;   // fp16 weights: no code copies
       const int step = is_x ? 1 : SK;                 // k-blocks per load (X) or stage (codes)
       int it = 0, s = 0;                              // loads issued; slot
       uint32_t ph = 0;                                // lap parity of slot s
-      for (int u = cl; u < ka.units; u += ncl) {
+      for (int u = cl; u < nunits; u += ncl) {
         const PUnit w = pair_unit(u, TN, ka);
         const int c0 = w.c0 + (int)rank * TCH;
         bool ok = true;
@@ -368,6 +375,50 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         umma2_commit_mc(drain, (uint16_t)0x1);
         drain_wait(drain, 0u);
       }
+    }
+  } else if (restore_index(warp) >= 0 && ka.w16) {
+    // ------------------------------------------------------------ fp16 weights
+    // Restore warp 0 relays, restore warps 1 and 2 load the two 64-channel halves of this
+    // CTA's 128 channels x 64 k of restored weights into the A slot (the layout the restore
+    // writes: two 8 KB halves, k-rows of 128 bytes, 128B swizzle), each copy on a barrier of
+    // its own; a slot is refilled once the MMAs of k-block it - R are done.  The relay
+    // arrives on CTA 0's barrier of a k-block once this CTA's X half and both A halves landed.
+    const int ri = restore_index(warp);
+    if (lane == 0 && ri <= 2) {
+      int it = 0, r = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = cl; u < ka.units && ok; u += ncl) {
+        const PUnit w = pair_unit(u, TN, ka);
+        const int c0 = w.c0 + (int)rank * TCH;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+          if (ri == 0) {
+            if (!pwait(xfull(r), ph, abort_flag) || !pwait(afull(0, r), ph, abort_flag) ||
+                !pwait(afull(1, r), ph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(mapa_shared(full(r), 0));
+          } else {
+            const int hf = ri - 1;
+            if (it >= R && !pwait(mma_done(r), ph ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(afull(hf, r), (uint32_t)(W_BYTES / 2));
+            tma_load_2d(smem_u32(sW + r * W_BYTES + hf * (W_BYTES / 2)), &tmA, c0 + 64 * hf,
+                        kb * BK, afull(hf, r));
+          }
+          if (++r == R) {
+            r = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // every copy this thread issued lands on this CTA's own barrier before the CTA exits
+      if (ri > 0)
+        for (int i = max(0, it - R); i < it; ++i)
+          drain_wait(afull(ri - 1, i % R), (uint32_t)((i / R) & 1));
     }
   } else if (restore_index(warp) >= 0) {
     // ------------------------------------------------------------ restore codes -> A
@@ -634,7 +685,7 @@ static int pair_raster_group(const GemmPlan& p) {
 }
 
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,
-                             const EpiArgs& ea, cudaStream_t st) {
+                             const EpiArgs& ea, cudaStream_t st, const uint16_t* w16) {
   const int maxcl = pair_max_clusters();
   if (maxcl <= 0) return cudaErrorInvalidConfiguration;
   const int tnh = p.tn / 2;
@@ -655,12 +706,20 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
                   (uint64_t)p.K, (uint64_t)(p.N / 64) * 4, 4, (uint32_t)(BK * sk),
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
+  // restored fp16 weights [K][N]: boxes of 64 channels x 64 k-rows (or the code map again)
+  CUtensorMap tmA = tmC;
+  if (w16) {
+    e = make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w16, (uint64_t)p.N, (uint64_t)p.K,
+                    (uint64_t)p.N * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
   const PArgs ka{(int)p.M,  (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
-                 p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot, pair_raster_group(p)};
+                 p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot, pair_raster_group(p),
+                 w16 ? 1 : 0};
   const int64_t clusters = std::min<int64_t>(p.units, maxcl);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config((unsigned)(2 * clusters), st, attr);
-  return cudaLaunchKernelEx(&cfg, gemm_q4_pair_kernel, tmX, tmC, tmS, ka, ea);
+  return cudaLaunchKernelEx(&cfg, gemm_q4_pair_kernel, tmX, tmC, tmS, tmA, ka, ea);
 }
 
 cudaError_t gemm_pair_read_error(unsigned int* out) {

@@ -133,6 +133,9 @@ kv_append_rows_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __rest
 }
 
 // Standalone restoration: fp16(a + q * ((b - a) / 15)), one rounding per binary32 op.
+// kPerm: each run of 8 channels is stored in the order 0,4,1,5,2,6,3,7 (the order in which
+// the CTA-pair GEMM's restore writes its A tiles, so that the GEMM can load them instead).
+template <bool kPerm>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ ab,
                int64_t ngroups, uint16_t* __restrict__ y) {
@@ -145,14 +148,15 @@ dequant_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ a
   const uint32_t abw = ab[grp];
   const float af = h2f((uint16_t)(abw & 0xFFFFu)), bf = h2f((uint16_t)(abw >> 16));
   const float s = __fdiv_rn(__fsub_rn(bf, af), 15.0f);
+  uint16_t xh[8];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+    xh[n] = f2h(__fadd_rn(af, __fmul_rn((float)((c >> (4 * n)) & 0xF), s)));
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float q0 = (float)((c >> (8 * i)) & 0xF), q1 = (float)((c >> (8 * i + 4)) & 0xF);
-    const float x0 = __fadd_rn(af, __fmul_rn(q0, s));
-    const float x1 = __fadd_rn(af, __fmul_rn(q1, s));
-    o[i] = (uint32_t)f2h(x0) | ((uint32_t)f2h(x1) << 16);
-  }
+  for (int i = 0; i < 4; ++i)
+    o[i] = kPerm ? ((uint32_t)xh[i] | ((uint32_t)xh[i + 4] << 16))
+                 : ((uint32_t)xh[2 * i] | ((uint32_t)xh[2 * i + 1] << 16));
   reinterpret_cast<uint4*>(y + grp * 64)[sub] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -173,7 +177,16 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint32_t* ab, int64_t row
                            uint16_t* y, cudaStream_t st) {
   const int64_t ng = rows * (cols / 64);
   if (ng == 0) return cudaSuccess;
-  return launch_pdl(dequant_kernel, dim3(grid_for(ng)), dim3(kThreads), 0, st, codes, ab, ng, y);
+  return launch_pdl(dequant_kernel<false>, dim3(grid_for(ng)), dim3(kThreads), 0, st, codes, ab,
+                    ng, y);
+}
+
+cudaError_t launch_dequant_pairperm(const uint8_t* codes, const uint32_t* ab, int64_t rows,
+                                    int64_t cols, uint16_t* y, cudaStream_t st) {
+  const int64_t ng = rows * (cols / 64);
+  if (ng == 0) return cudaSuccess;
+  return launch_pdl(dequant_kernel<true>, dim3(grid_for(ng)), dim3(kThreads), 0, st, codes, ab,
+                    ng, y);
 }
 
 cudaError_t launch_kv_append(const uint16_t* k_new, const uint16_t* v_new, int64_t row_stride,

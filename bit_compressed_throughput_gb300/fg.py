@@ -24,9 +24,11 @@ FG_ERR_CUDA, FG_ERR_ARCH, FG_ERR_CAPACITY, FG_ERR_TIMEOUT = -4, -5, -6, -7
 FG_EPI_NONE, FG_EPI_RELU, FG_EPI_RESIDUAL = 0, 1, 2
 KINDS = ["q4g64_quantize", "q4g64_dequant", "q4_dequant_gemm_tc", "gemm_splitk_reduce",
          "q4kv_append", "q4kv_decode_attn", "decode_attn_combine", "prefill_attn", "layernorm",
-         "q4_dequant_gemm_stream", "q4kv_decode_attn_topk", "q4_dequant_gemm_pair"]
+         "q4_dequant_gemm_stream", "q4kv_decode_attn_topk", "q4_dequant_gemm_pair",
+         "gemm_f16w_pair"]
 K_QUANT, K_DEQUANT, K_GEMM, K_GEMM_REDUCE, K_KV_APPEND, K_DECODE_ATTN, K_DECODE_COMBINE, \
-    K_PREFILL_ATTN, K_LAYERNORM, K_GEMM_STREAM, K_DECODE_ATTN_TOPK, K_GEMM_PAIR = range(12)
+    K_PREFILL_ATTN, K_LAYERNORM, K_GEMM_STREAM, K_DECODE_ATTN_TOPK, K_GEMM_PAIR, \
+    K_GEMM_PAIR_F16W = range(13)
 
 
 class fg_q4mat(C.Structure):

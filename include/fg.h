@@ -302,7 +302,9 @@ enum {
   FG_K_GEMM_STREAM = 9,   /* the weight-streaming GEMM (M <= 128): work counted in bytes */
   FG_K_DECODE_ATTN_TOPK = 10,   /* both kernels of the top-K attention: bytes */
   FG_K_GEMM_PAIR = 11,   /* the tiled GEMM on CTA pairs (many tokens): flops */
-  FG_K_COUNT = 12
+  FG_K_GEMM_PAIR_F16W = 12,   /* the CTA-pair GEMM on weights restored to fp16 (layer
+                                 prefill): flops */
+  FG_K_COUNT = 13
 };
 int fg_prof_enable(int on);
 int fg_prof_reset(void);
