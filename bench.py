@@ -390,6 +390,42 @@ def phase_rooflines(wl, pre, dec, pk, psteps):
     return out
 
 
+def fused_gemm_probe(fg, wl, layer, device, pk, reps=3):
+    """The dequant-fused GEMM (4-bit codes restored inside the mainloop, C-ABI
+    fg_dequant_gemm_q4) at this workload's prefill FC1 shape (QKV without an FFN), timed
+    alone with CUDA events.  The layer's prefill restores each layer's weights once and runs
+    the fp16-weight mode of the same kernel instead; this line keeps the fused kernel
+    measured at the prefill shape."""
+    import torch
+    W, epi = (layer.w1, 1) if wl.f else (layer.wqkv, 0)
+    M, K, N = wl.g * wl.s, W.K, W.N
+    gen = torch.Generator(device=device)
+    gen.manual_seed(11)
+    X = torch.randn((M, K), generator=gen, device=device).half()
+    Y = torch.empty((M, N), dtype=torch.float16, device=device)
+    bias = torch.zeros(N, dtype=torch.float16, device=device)
+    wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device) if wsb else None
+    fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fg.fg_dequant_gemm_q4(X, W, bias, epi, None, Y, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    fg.fg_check_device_error()
+    ms = e0.elapsed_time(e1) / reps
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    del X, Y, ws
+    return {"kernel": "q4_dequant_gemm_pair", "shape": f"M={M} K={K} N={N}", "bound": "tensor",
+            "achieved": round(tf, 1), "unit": "TFLOP/s", "ms_per_launch": round(ms, 3),
+            "peak": pk["bf16"], "frac": round(tf / pk["bf16"], 4),
+            "frac_of_sustained": round(tf / pk["bf16_sustained"], 4),
+            "peak_source": f"{pk['source']} bf16 burst (timed alone, {reps} launches)",
+            "frac_of_nominal": round(tf / NOMINAL_F16_TFLOPS, 4)}
+
+
 def run_config(wl, device, steps, warmup, dist=None, rank=0, full=False, pk=None):
     """Build one workload's stack on the device and time it: the graph-replayed pass,
     eager per-kernel profiles of prefill and decode, and (full) the e2e pass with host I/O."""
@@ -452,6 +488,7 @@ def run_config(wl, device, steps, warmup, dist=None, rank=0, full=False, pk=None
             "copies": "every step's inputs in and outputs out on copy streams, overlapped "
                       "with the neighbouring steps' compute (two buffer sets)"}
         del run_b
+        extra["fused_prefill_gemm"] = fused_gemm_probe(fg, wl, layers[0], device, pk)
     del run, layers, x, xs
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -530,6 +567,7 @@ def run_gpu(args, wl):
         "decode_attn_roofline": rl["decode_attn"],
         "decode_attn_hbm_kv_workload": attn_kv,
         "prefill_attn_roofline": rl["prefill_attn"],
+        "dequant_fused_prefill_gemm": extra.get("fused_prefill_gemm"),
         "kernels": main["kernels"],
         "cost_model": main["cost_model"],
         "eager_ms_per_step": main["eager_ms_per_step"],
