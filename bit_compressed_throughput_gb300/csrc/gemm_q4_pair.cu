@@ -680,11 +680,13 @@ static bool pair_rings(const GemmPlan& p, int tnh, int* r_out, int* rc_out, int*
 // the OPT-175B prefill shapes (18432 tokens): 4 (2 at K = 49152) is 3.5-4% faster than 8,
 // 16 or groups of channel pairs; at the 6.7B shapes the group size makes no difference.
 // With fp16 weights a channel pair's A tiles are as many bytes as a token tile of X, and the
-// DRAM bytes per wave, g X tiles + 76 / g weight tiles, are least near g = 8: up to 8 token
-// tiles there (1% faster than 4 in the OPT-175B bench, A/B in one call).
+// DRAM bytes per wave, g X tiles + 76 / g weight tiles, are least near g = 8, whatever K:
+// 8 token tiles there (in the OPT-175B bench 1% faster than 4, and another 1% faster than
+// capping the group at 64 MB of X, which gave 2 at K = 49152; A/B runs in one call).
 static int pair_raster_group(const GemmPlan& p, bool w16) {
+  if (w16) return 8;
   const double x_tile = (double)p.tn * p.K * 2.0;
-  return (int)std::max(1.0, std::min(w16 ? 8.0 : 4.0, 64e6 / x_tile));
+  return (int)std::max(1.0, std::min(4.0, 64e6 / x_tile));
 }
 
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,

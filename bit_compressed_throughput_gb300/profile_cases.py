@@ -6,6 +6,7 @@ one hot-path kernel at a workload's shape, inputs larger than L2 and a few GB at
     python -m bit_compressed_throughput_gb300.profile_cases decode-attn-kv
     python -m bit_compressed_throughput_gb300.profile_cases prefill-attn-opt67b
     python -m bit_compressed_throughput_gb300.profile_cases gemm-prefill-opt175b --reps 0
+    python -m bit_compressed_throughput_gb300.profile_cases layer-prefill-opt175b --reps 0
 
 Inputs are seeded random device tensors (no parity check here; the tests do that).
 """
@@ -83,6 +84,31 @@ def prefill_case(nseq, s, H, d, reps):
     fg.fg_check_device_error()
 
 
+def layer_prefill_case(h, H, f, g, s, reps):
+    """One decoder layer's prefill over one GPU batch (g sequences of s tokens): the layer
+    restores its weights to fp16 once, then runs LN, the four projections (the CTA-pair GEMM
+    in its fp16-weight mode), the K/V append and prefill attention."""
+    import torch
+    from bit_compressed_throughput_gb300 import fg
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    params = {}
+    for name, (K, N) in {"wqkv": (h, 3 * h), "wo": (h, h), "w1": (h, f), "w2": (f, h)}.items():
+        params[name] = (torch.randn((K, N), generator=gen, device="cuda") * 0.02).half()
+    params.update({"bqkv": torch.zeros(3 * h), "bo": torch.zeros(h), "ln1_g": torch.ones(h),
+                   "ln1_b": torch.zeros(h), "ln2_g": torch.ones(h), "ln2_b": torch.zeros(h),
+                   "b1": torch.zeros(f), "b2": torch.zeros(h)})
+    layer = fg.LayerQ4.from_fp16(params, H)
+    del params
+    torch.cuda.empty_cache()
+    eng = fg.StackEngine([layer], g, 1, s, s)
+    x = torch.randn((g, s, h), generator=gen, device="cuda").half()
+    y = torch.empty_like(x)
+    for _ in range(1 + reps):
+        eng.prefill(x, y, s)
+    fg.fg_check_device_error()
+
+
 CASES = {
     # 6.7B prefill FC1 of one GPU batch: M = 16*512, K = 4096, N = 16384, ReLU
     "gemm-fc1-opt67b": lambda r: gemm_case(8192, 4096, 16384, 1, r),
@@ -94,6 +120,8 @@ CASES = {
                                                    (18432, 12288, 12288, 0),
                                                    (18432, 12288, 49152, 1),
                                                    (18432, 49152, 12288, 0)), r),
+    # one OPT-175B layer's prefill over one GPU batch (36 x 512 tokens): ~9 GB on the device
+    "layer-prefill-opt175b": lambda r: layer_prefill_case(12288, 96, 49152, 36, 512, r),
     # 6.7B decode FC1 (M = B = 64, split K)
     "gemm-fc1-decode-opt67b": lambda r: gemm_case(64, 4096, 16384, 1, r),
     # 6.7B decode attention at the last step: 64 sequences x 32 heads x 543 positions
