@@ -52,15 +52,16 @@ SUB_CONFIGS = ("opt-6.7b", "opt-30b", "kv-decode")
 # fp16/bf16 tensor 2.25 PFLOP/s
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_F16_TFLOPS = 2250.0
-# DRAM bytes (read + write) per launch of the tiled GEMM, by workload: from one-kernel ncu
-# captures (dram__bytes_read.sum + dram__bytes_write.sum, one pass) of the workload's prefill
-# GEMM shapes at full size, averaged over one pass's launch mix; a workload without a capture
-# of the current kernel reports null.  opt-175b: the QKV, O, FC1 and FC2 projections of one
-# GPU batch (18432 tokens; equal launch counts per pass) read + wrote 9.31, 3.16, 13.68 and
-# 24.90 GB (profile case gemm-prefill-opt175b); their algorithmic bytes (X, 4-bit weights
-# with statistics, Y, and the residual read of O and FC2) are 2.07, 1.44, 2.60 and 3.06 GB.
-GEMM_TRAFFIC_PER_LAUNCH = {"opt-175b": 12762526144}
-GEMM_ALGORITHMIC_BYTES_PER_LAUNCH = {"opt-175b": 2293235712}
+# DRAM bytes (read + write) per launch of the prefill GEMM, by workload: from one-kernel ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum, one pass) at full size, averaged over
+# one pass's launch mix; a workload without a capture of the current kernel reports null.
+# opt-175b: the QKV, O, FC1 and FC2 projections of one GPU batch (18432 tokens, equal launch
+# counts per pass) in the fp16-weight mode of the layer prefill (profile case
+# layer-prefill-opt175b) read + wrote 45.06, 14.04, 61.50 and 76.83 GB; their algorithmic
+# bytes (X, the fp16 weights, Y, and the residual read of O and FC2) are 2.72, 1.66, 3.47 and
+# 3.93 GB.
+GEMM_TRAFFIC_PER_LAUNCH = {"opt-175b": 49360370816}
+GEMM_ALGORITHMIC_BYTES_PER_LAUNCH = {"opt-175b": 2944401408}
 
 
 def peaks():
@@ -538,8 +539,9 @@ def run_gpu(args, wl):
         gemm.pop("ms_per_step", None)
         gemm["traffic"] = GEMM_TRAFFIC_PER_LAUNCH.get(wl.name)
         gemm["traffic_note"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch "
-                                "(mean of the four prefill projection shapes); the weights are "
-                                "re-read from HBM once per raster group of token tiles"
+                                "(mean of the four prefill projection shapes, fp16-weight mode); "
+                                "the weights are re-read from HBM per raster group of token "
+                                "tiles and when the clusters sharing a k-block drift apart"
                                 if gemm["traffic"] else
                                 "no one-kernel capture of the current GEMM at this workload")
         if gemm["traffic"]:
