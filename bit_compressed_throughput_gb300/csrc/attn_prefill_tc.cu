@@ -10,23 +10,27 @@
 // QKV buffer by TMA (boxes of 64 columns x 128 rows, 128B swizzle; d = 128 takes two).
 //   S = Q K^T     tcgen05.mma kind::f16, M = 128 query rows, N = 128 keys, K = d: A = the Q
 //                 tile and B = the K tile, both K-major in shared memory; S (fp32) in TMEM
-//   softmax       one thread per query row (TMEM lane): the row of S from TMEM, causal mask on
-//                 the diagonal tile and past the sequence, online base-2 softmax with a lazily
-//                 moved reference maximum (rescale only when a row's maximum grows by more
-//                 than 2^8), P = 2^(s - m) rounded to fp16 and written back over the first 64
-//                 columns of the row's S (two fp16 per column).  Two passes over the row (the
-//                 maximum, then P 64 columns at a time) keep a thread within 128 registers.
-//   O += P V      tcgen05.mma with A = P read from TMEM (K = 128 keys), B = the V tile
-//                 (MN-major: keys are its K, the head dimension its N); O (fp32) in TMEM
+//   softmax       two threads per query row (TMEM lane), each over one half of the 128 key
+//                 columns: causal mask on the diagonal tile and past the sequence, the row
+//                 maximum exchanged between the halves through shared memory, online base-2
+//                 softmax with a lazily moved reference maximum (rescale only when a row's
+//                 maximum grows by more than 2^8), P = 2^(s - m) rounded to fp16 and written
+//                 back over the first 32 of the half's 64 S columns (two fp16 per column).
+//                 Two passes over the half (the maximum, then P) keep a thread within 80
+//                 registers.
+//   O += P V      tcgen05.mma with A = P read from TMEM (K = 128 keys, in two blocks of 32
+//                 columns), B = the V tile (MN-major: keys are its K, the head dimension its
+//                 N); O (fp32) in TMEM
 // The two Q tiles ping-pong: while one tile's softmax warps work on S, the tensor core runs the
 // other tile's products.  TMEM: S of A and B (128 columns each), O of A and B (d columns each).
 //   warp 0      TMA producer: the two Q tiles of a block, then its K/V tiles into a 2-stage ring
 //   warp 1      MMA issuer: S_A(0), S_B(0); then per key tile j and Q tile t: P_t(j) V_j into
 //               O_t, then S_t(j + 1) (the tensor core runs one thread's MMAs in issue order, so
 //               S_t(j + 1) overwrites the columns of P_t(j) only after P_t(j) V_j has read them)
-//   warps 4-7   softmax of Q tile A (warp w owns TMEM lanes 32 (w % 4) ..)
-//   warps 8-11  softmax of Q tile B
-//   warps 12-15 output: O_t / l of a finished block from TMEM, fp16, staged in shared memory,
+//   warps 2-9   softmax of Q tile A: warp w owns TMEM lanes 32 (w % 4) .. and key half
+//               ((w - 2) / 4) & 1
+//   warps 10-17 softmax of Q tile B
+//   warps 18-21 output: O_t / l of a finished block from TMEM, fp16, staged in shared memory,
 //               stored by TMA; a block's first P V product into O_t waits until they have
 //               read the previous block's O_t, so the softmax warps go on to the next block
 //               while the output is written
@@ -55,9 +59,10 @@ constexpr int QT = 128;                     // query rows per Q tile (MMA M, TME
 constexpr int KT = 128;                     // keys per K/V tile
 constexpr int QB = 2 * QT;                  // query rows per CTA
 constexpr int STAGES = 2;                   // K/V ring
-constexpr int THREADS = 16 * 32;           // 128 registers a thread
-constexpr int W_SM_A = 4, W_SM_B = 8;      // first softmax warp of Q tile A, of Q tile B
-constexpr int W_OUT = 12;                   // first output warp
+constexpr int THREADS = 22 * 32;
+constexpr int W_SM = 2;                     // softmax warps 2..17: Q tile (w - 2) / 8, key half
+                                            // ((w - 2) / 4) & 1, TMEM lane quarter w % 4
+constexpr int W_OUT = 18;                   // first output warp (18..21)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr long long kWaitCycles = 1ll << 32;
 constexpr int BOX = QT * 128;               // bytes of one 64-column x 128-row box
@@ -68,18 +73,20 @@ struct PSmem {
   static constexpr int Q_OFF = 0;                      // Q_A, Q_B
   static constexpr int K_OFF = 2 * TILE;               // K stages
   static constexpr int V_OFF = K_OFF + STAGES * TILE;  // V stages
-  static constexpr int O_OFF = V_OFF + STAGES * TILE;  // two output boxes
-  static constexpr int L_OFF = O_OFF + 2 * BOX;        // row sums l of A and B (fp32)
-  static constexpr int BAR_OFF = L_OFF + 2 * QT * 4;
+  static constexpr int O_OFF = V_OFF + STAGES * TILE;  // one output box
+  static constexpr int L_OFF = O_OFF + BOX;            // row sums l [tile][key half][row]
+  static constexpr int MX_OFF = L_OFF + 2 * 2 * QT * 4;  // row maxima [parity][tile][half][row]
+  static constexpr int BAR_OFF = MX_OFF + 2 * 2 * 2 * QT * 4;
   static constexpr int BYTES = BAR_OFF + 256 + 1024;   // barriers; 1024 for alignment
 };
 static_assert(PSmem<128>::BYTES <= 227 * 1024, "shared memory per CTA");
 
 // barriers: q_full, q_free, kv_full[2], kv_free[2], s_full[2], p_full[2], o_done[2], o_free[2],
-// l_full[2], o_staged, o_stage_free, drain
+// l_full[2], o_staged, o_stage_free, drain, mx_ready[tile][quarter] (the two key halves of a
+// row have written their maxima)
 constexpr int B_QFULL = 0, B_QFREE = 1, B_KVFULL = 2, B_KVFREE = 4, B_SFULL = 6, B_PFULL = 8,
               B_ODONE = 10, B_OFREE = 12, B_LFULL = 14, B_OSTAGED = 16, B_OSFREE = 17,
-              B_DRAIN = 18, NBARS = 19;
+              B_DRAIN = 18, B_MX = 19, NBARS = 27;
 static_assert(NBARS * 8 + 8 <= 256, "barrier space");
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -119,9 +126,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// the shared-memory sources of all but this thread's latest bulk store have been read
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // this thread's bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() {
@@ -272,6 +279,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* l_buf = reinterpret_cast<float*>(smem + L::L_OFF);
+  float* mx_buf = reinterpret_cast<float*>(smem + L::MX_OFF);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
@@ -288,10 +296,11 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(B_SFULL + t), 1);
-      mbar_init(bar(B_PFULL + t), 4);                  // one arrival per softmax warp
+      mbar_init(bar(B_PFULL + t), 8);                  // one arrival per softmax warp
       mbar_init(bar(B_ODONE + t), 1);
       mbar_init(bar(B_OFREE + t), 4);                  // one arrival per output warp
-      mbar_init(bar(B_LFULL + t), 4);                  // one arrival per softmax warp
+      mbar_init(bar(B_LFULL + t), 8);                  // one arrival per softmax warp
+      for (int q = 0; q < 4; ++q) mbar_init(bar(B_MX + 4 * t + q), 2);   // both key halves
     }
     mbar_init(bar(B_OSTAGED), 4);                      // one arrival per output warp
     mbar_init(bar(B_OSFREE), 1);
@@ -378,15 +387,16 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         }
         umma_commit(bar(B_SFULL + t));
       };
-      // O_t (+)= P_t V of K/V tile g over K = 128 keys: k-step i reads TMEM columns 8i.. of
-      // P and rows 16i.. of V (2048 bytes per step in its MN-major 128B-swizzled layout)
+      // O_t (+)= P_t V of K/V tile g over K = 128 keys: k-step i reads the 8 TMEM columns of
+      // P of keys 16i.. (key half i / 4 keeps its P in the first 32 of its 64 S columns) and
+      // rows 16i.. of V (2048 bytes per step in its MN-major 128B-swizzled layout)
       auto issue_pv = [&](int t, int g, bool first) {
         const int st = g % STAGES;
         const uint64_t vd = smem_desc(vbase + st * L::TILE, BOX, 1024);
 #pragma unroll
         for (int i = 0; i < KT / 16; ++i)
-          umma_ts(tmem + o_col(t), tmem + s_col(t) + 8 * i, vd + (uint64_t)(i * 128), idesc_o,
-                  (!first || i > 0) ? 1u : 0u);
+          umma_ts(tmem + o_col(t), tmem + s_col(t) + 64 * (i >> 2) + 8 * (i & 3),
+                  vd + (uint64_t)(i * 128), idesc_o, (!first || i > 0) ? 1u : 0u);
         umma_commit(bar(B_ODONE + t));
       };
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++qn) {
@@ -447,24 +457,30 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         drain_wait(bar(B_DRAIN), 0u);
       }
     }
-  } else if (warp >= W_SM_A && warp < W_OUT) {
-    // ------------------------------------------------------------ softmax of one Q tile
-    const int t = (warp < W_SM_B) ? 0 : 1;
+  } else if (warp >= W_SM && warp < W_OUT) {
+    // ------------------------------------------------------------ softmax: one key half of
+    // one Q tile's rows.  Two threads per row: half c takes key columns 64c .. 64c + 63 of each
+    // S tile, the row maximum is exchanged through shared memory (mx_ready barrier of the two
+    // warps of a lane quarter), and half c writes its P over the first 32 of its own S columns
+    // and rescales O columns c d/2 ..
+    const int t = (warp - W_SM) >> 3, c = ((warp - W_SM) >> 2) & 1;
     const int quarter = warp & 3;                      // TMEM lanes 32 quarter ..
     const int m = 32 * quarter + lane;                 // row within the Q tile
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-    const uint32_t srow = lane_addr + s_col(t);
+    const uint32_t srow = lane_addr + s_col(t) + 64 * c;
+    const uint32_t mxb = bar(B_MX + 4 * t + quarter);
     const float sl2 = pa.scale_log2;
     int sc = 0, uses = 0;                              // S products consumed, items finished
     bool ok = true;
     // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
-    // decided for the whole warp, waits included (a lane that gave up takes its warp along)
+    // decided for the whole warp, waits included (a lane that gave up takes its warp along);
+    // both halves of a row take the same decisions (the same maximum)
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const Item it = item_of(item, pa);
       const int nt = t ? it.nt1 : it.nt0;
       if (nt == 0) continue;
       const int qi = it.q0 + t * QT + m;               // query position in the sequence
-      float m_ref = -INFINITY, l_sum = 0.0f;
+      float m_ref = -INFINITY, l_sum = 0.0f;           // l over this half's keys
       for (int j = 0; j < nt; ++j, ++sc) {
         const bool got = bwait(bar(B_SFULL + t), (uint32_t)(sc & 1), abort_flag);
         if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -476,18 +492,17 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         // lim are visible
         const int k0 = j * KT;
         const bool masked = (k0 + KT - 1 > it.q0 + t * QT) || (k0 + KT > s);   // warp-uniform
-        const int lim = min(qi, s - 1) - k0;
-        // pass 1: the row maximum, 32 columns at a time (the next chunk's TMEM load in flight
-        // meanwhile), four independent running maxima
+        const int lim = min(qi, s - 1) - k0 - 64 * c;  // within this half's 64 columns
+        // pass 1: this half's maximum, 32 columns at a time (the second load in flight)
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        auto max_chunk = [&](float (&v)[32], int c4) {
+        auto max_chunk = [&](float (&v)[32], int c2) {
           if (masked) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = (32 * c4 + c <= lim) ? v[c] : -INFINITY;
+            for (int e = 0; e < 32; ++e) v[e] = (32 * c2 + e <= lim) ? v[e] : -INFINITY;
           }
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], v[c], v[c + 1]);
+          for (int e = 0; e < 32; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], v[e], v[e + 1]);
         };
         {
           float va[32], vb[32];
@@ -496,22 +511,28 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           tmem_ld32(srow + 32, vb);
           max_chunk(va, 0);
           tmem_wait_ld_dep(vb);
-          tmem_ld32(srow + 64, va);
           max_chunk(vb, 1);
-          tmem_wait_ld_dep(va);
-          tmem_ld32(srow + 96, vb);
-          max_chunk(va, 2);
-          tmem_wait_ld_dep(vb);
-          max_chunk(vb, 3);
         }
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // the row maximum over both halves (slot of this tile's parity: the other half reads
+        // it before either can write the slot again two tiles on)
+        float* mx_slot = mx_buf + (((sc & 1) * 2 + t) * 2) * QT;
+        mx_slot[c * QT + m] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mxb);
+        const bool ex = bwait(mxb, (uint32_t)(sc & 1), abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, ex)) {
+          ok = false;
+          break;
+        }
+        float mx = fmaxf(mx_slot[m], mx_slot[QT + m]);
         // in base 2 (scale > 0, so scaling after the maximum is the same); a row that sees no
         // key keeps a finite maximum (such rows lie past the sequence and are never stored)
         mx = (mx == -INFINITY) ? 0.0f : mx * sl2;
         if (__any_sync(0xFFFFFFFFu, mx > m_ref + 8.0f)) {
           // move the reference maximum of every row of the warp to max(m_ref, mx): O and l
           // scale by 2^(m_ref - m_new) (1 for rows whose maximum did not grow); O holds P V of
-          // the item's earlier tiles once their MMAs are done
+          // the item's earlier tiles once their MMAs are done; this half rescales its d/2
+          // columns of O
           const float m_new = fmaxf(m_ref, mx);
           const float alpha = ex2(m_ref - m_new);
           if (j > 0) {
@@ -522,13 +543,14 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
             }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
+            for (int c16 = 0; c16 < D / 32; ++c16) {
               uint32_t w[16];
-              tmem_ld16(lane_addr + o_col(t) + 16 * c, w);
+              const uint32_t oa = lane_addr + o_col(t) + (uint32_t)(c * (D / 2) + 16 * c16);
+              tmem_ld16(oa, w);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-              tmem_st16(lane_addr + o_col(t) + 16 * c, w);
+              for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+              tmem_st16(oa, w);
             }
             tmem_wait_st();
           }
@@ -536,24 +558,24 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           m_ref = m_new;
         }
         // pass 2: p = 2^(s * scale - m_ref), 32 columns at a time (the scaling and the row sums
-        // two elements per instruction), packed to fp16 over columns 16 c4 .. of the row's S
+        // two elements per instruction), packed to fp16 over columns 16 c2 .. of this half's S
         // (S columns that have been read)
         const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m_ref, -m_ref);
         uint64_t ls2[2] = {f2pack(0.0f, 0.0f), f2pack(0.0f, 0.0f)};
-        auto p_chunk = [&](float (&v)[32], int c4) {
+        auto p_chunk = [&](float (&v)[32], int c2) {
           if (masked) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = (32 * c4 + c <= lim) ? v[c] : -INFINITY;
+            for (int e = 0; e < 32; ++e) v[e] = (32 * c2 + e <= lim) ? v[e] : -INFINITY;
           }
           uint32_t pw[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 x = f2unpack(ffma2(f2pack(v[c], v[c + 1]), sl2x2, negm2));
+          for (int e = 0; e < 32; e += 2) {
+            const float2 x = f2unpack(ffma2(f2pack(v[e], v[e + 1]), sl2x2, negm2));
             const float p0 = ex2(x.x), p1 = ex2(x.y);
-            ls2[(c >> 1) & 1] = fadd2(ls2[(c >> 1) & 1], f2pack(p0, p1));
-            pw[c / 2] = pack_h2(p0, p1);
+            ls2[(e >> 1) & 1] = fadd2(ls2[(e >> 1) & 1], f2pack(p0, p1));
+            pw[e / 2] = pack_h2(p0, p1);
           }
-          tmem_st16(srow + 16 * c4, pw);
+          tmem_st16(srow + 16 * c2, pw);
         };
         {
           float va[32], vb[32];
@@ -562,13 +584,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           tmem_ld32(srow + 32, vb);
           p_chunk(va, 0);
           tmem_wait_ld_dep(vb);
-          tmem_ld32(srow + 64, va);
           p_chunk(vb, 1);
-          tmem_wait_ld_dep(va);
-          tmem_ld32(srow + 96, vb);
-          p_chunk(va, 2);
-          tmem_wait_ld_dep(vb);
-          p_chunk(vb, 3);
         }
         tmem_wait_st();
         const float2 la = f2unpack(fadd2(ls2[0], ls2[1]));
@@ -578,7 +594,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         if (lane == 0) mbar_arrive(bar(B_PFULL + t));
       }
       if (!ok) break;
-      // the item's row sums for the output warps, once they have taken the previous item's
+      // this half's row sums for the output warps, once they have taken the previous item's
       if (uses > 0) {
         const bool fr = bwait(bar(B_OFREE + t), (uint32_t)((uses - 1) & 1), abort_flag);
         if (!__all_sync(0xFFFFFFFFu, fr)) {
@@ -586,7 +602,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
           break;
         }
       }
-      l_buf[t * QT + m] = l_sum;
+      l_buf[(t * 2 + c) * QT + m] = l_sum;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_LFULL + t));
       ++uses;
@@ -614,20 +630,20 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQKV,
         }
         tc_fence_after();
         ++uses[t];
-        const float inv = 1.0f / l_buf[t * QT + m];
+        const float inv = 1.0f / (l_buf[(t * 2) * QT + m] + l_buf[(t * 2 + 1) * QT + m]);
         // O / l in 64-column boxes, staged in shared memory (the 128B-swizzled layout of the
         // output map: 16-byte chunk k of row m at chunk k ^ (m % 8)) and stored by TMA; rows
         // past the sequence lie outside the map and are not written
 #pragma unroll 1
         for (int hb = 0; hb < NB; ++hb, ++nbox) {
-          const uint32_t stage = smem_u32(smem + L::O_OFF + (nbox & 1) * BOX);
-          if (nbox >= 2) {
-            // the box is free once the store issued from it two boxes ago has read it
+          const uint32_t stage = smem_u32(smem + L::O_OFF);
+          if (nbox >= 1) {
+            // the box is free once the previous store has read it
             if (leader) {
-              bulk_wait_read_1();
+              bulk_wait_read();
               mbar_arrive(bar(B_OSFREE));
             }
-            const bool fr = bwait(bar(B_OSFREE), (uint32_t)((nbox - 2) & 1), abort_flag);
+            const bool fr = bwait(bar(B_OSFREE), (uint32_t)((nbox - 1) & 1), abort_flag);
             if (!__all_sync(0xFFFFFFFFu, fr)) {
               ok = false;
               break;
