@@ -122,6 +122,9 @@ CASES = {
                                                    (18432, 49152, 12288, 0)), r),
     # one OPT-175B layer's prefill over one GPU batch (36 x 512 tokens): ~9 GB on the device
     "layer-prefill-opt175b": lambda r: layer_prefill_case(12288, 96, 49152, 36, 512, r),
+    # one opt-6.7b layer's prefill over one GPU batch (16 x 512 tokens): ~2 GB on the device,
+    # for multi-pass captures of the fp16-weight GEMM (launches QKV, O, FC1, FC2 in order)
+    "layer-prefill-opt67b": lambda r: layer_prefill_case(4096, 32, 16384, 16, 512, r),
     # 6.7B decode FC1 (M = B = 64, split K)
     "gemm-fc1-decode-opt67b": lambda r: gemm_case(64, 4096, 16384, 1, r),
     # 6.7B decode attention at the last step: 64 sequences x 32 heads x 543 positions
