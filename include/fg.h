@@ -255,10 +255,14 @@ int fg_layernorm(const uint16_t* x, int64_t rows, int32_t h, const uint16_t* gam
 /* Prefill of one layer over a block of m GPU batches of g sequences each, prompt length s:
  * x, y: device fp16 [m][g][s][h] (y may alias x).  GPU batch k is processed in full
  * (M = g*s rows per GEMM) before batch k+1; its K/V are quantised into `kv` positions
- * 0..s-1 of sequences k*g .. k*g+g-1.  kv->B == g*m, s <= kv->cap.
+ * 0..s-1 of sequences k*g .. k*g+g-1.  kv->B == g*m, s <= kv->cap.  When g*s > 128 the
+ * call first restores the layer's four weight matrices to fp16 in `ws` (once for the m GPU
+ * batches) and its GEMMs read those instead of restoring the codes tile by tile; the results
+ * are those of the 4-bit weights either way.
  * ws: device scratch of at least fg_layer_workspace_bytes(dims, g, m, s) bytes.
  * [FlexGen paper explainer, Algorithm 1 (a layer over every GPU batch of the block);
- *  Figure 2 (prefill builds the cache)] */
+ *  Figure 2 (prefill builds the cache); FlexGen review, "4-bit 압축은 정수 연산 가속과
+ *  같은가": weights restored to FP16 before compute] */
 int fg_layer_prefill(const fg_dims* dims, const fg_layer* layer, fg_kvcache* kv,
                      const uint16_t* x, uint16_t* y, int32_t g, int32_t m, int32_t s,
                      void* ws, size_t ws_bytes, void* stream);
@@ -275,8 +279,9 @@ int fg_layer_decode(const fg_dims* dims, const fg_layer* layer, fg_kvcache* kv,
 /* Workspace bytes for fg_layer_prefill with prompts up to s_max and for fg_layer_decode
  * with caches up to s_max positions (the larger of the two uses): per GPU batch of g
  * sequences the LayerNorm output, the [g*s][3h] QKV, the attention output, h1 and the
- * [g*s][f] FFN activation, plus GEMM split-K partials and, for decode over the whole block
- * of g*m sequences, the split-sequence attention partials.  Returns 0 for invalid dims
+ * [g*s][f] FFN activation, plus GEMM split-K partials, the layer's weights restored to fp16
+ * for a prefill of more than 128 rows (2*(4h^2 + 2hf) bytes) and, for decode over the whole
+ * block of g*m sequences, the split-sequence attention partials.  Returns 0 for invalid dims
  * or g, m, s_max <= 0.  A pure host computation (no CUDA call).
  * [FlexGen paper explainer, "Compute Schedule": a layer runs over every GPU batch of the
  *  block, so the scratch is sized by g, m and the sequence length, not by the stack] */
