@@ -104,6 +104,7 @@ struct GemmPlan {
   int64_t units;   // (split, tile) work units
   int grid;        // persistent CTAs: min(units, SMs)
   size_t ws_bytes;
+  size_t sched_off;  // kind 2 with tiles_t >= 2: offset in the workspace of the unit counter
 };
 // K/V append of the QKV projection: columns [h, 2h) of Y are K and [2h, 3h) are V; row
 // r = b*T + t of the GEMM is position pos + t of sequence b.  Each 64-channel group of a

@@ -866,6 +866,8 @@ static void stream_plan(GemmPlan& p, int nsm) {
 // and reduce).  The count is capped independently of the SM count (at most 8, at least 8
 // k-blocks per split, no more units than two rounds of the largest cluster count planned for)
 // and the workspace is sized for the cap, so a workspace sized by the query covers any device.
+// With several token tiles the workspace also holds the 256-byte unit counter of the
+// kernel's dynamic order.
 static bool pair_fits(int64_t M, int64_t N) { return M > 128 && N % 256 == 0; }
 
 static void pair_plan(GemmPlan& p, int nsm) {
@@ -897,6 +899,11 @@ static void pair_plan(GemmPlan& p, int nsm) {
   p.kb_per_split = ((p.kblocks + best - 1) / best + gran - 1) / gran * gran;
   p.splits = (p.kblocks + p.kb_per_split - 1) / p.kb_per_split;
   p.ws_bytes = (cap > 1) ? (size_t)cap * p.M * p.N * sizeof(float) : 0;
+  // several token tiles: the units run in dynamic order from a counter after the partials
+  if (p.tiles_t >= 2) {
+    p.sched_off = (p.ws_bytes + 255) / 256 * 256;
+    p.ws_bytes = p.sched_off + 256;
+  }
   p.units = tiles * p.splits;
   p.grid = (int)(2 * std::min<int64_t>(p.units, ncl));
 }
@@ -986,7 +993,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const uint16_t* X, const fg_q4mat& W,
   if (p.splits > 1) ea.partial = static_cast<float*>(ws);
   if (p.kind == kGemmPair) {
     if (kv && kv->k_codes) return cudaErrorInvalidValue;   // the append lives in kind 0/1
-    e = launch_gemm_pair(p, W, X, ea, st, w16);
+    e = launch_gemm_pair(p, W, X, ea, st, w16, ws);
     if (e != cudaSuccess || p.splits == 1) return e;
     if (mid_event) cudaEventRecord(mid_event, st);
     return launch_reduce(p, ws, final_ea, ln, st);

@@ -101,11 +101,19 @@ constexpr int POOL_BYTES = SMEM_BYTES - 1024 /*align*/ - BAR_BYTES;
 // X half landed), mma_done[R] (the k-block's MMAs done: slot reusable), full_c[RC], free_c[RC],
 // acc_full[2], acc_empty[2] (CTA 0: both CTAs' epilogues read the accumulator), drain, and
 // with fp16 weights afull[2][R] (this CTA's two 64-channel halves of the A slot landed)
-constexpr int NBARS = 5 * R_MAX + 2 * RC_MAX + 5;
+// and uq_full[QD] (a unit-schedule ring entry published: the dynamic order below)
+constexpr int QD = 16;
+constexpr int NBARS = 5 * R_MAX + 2 * RC_MAX + 5 + QD;
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;   // two accumulator buffers of 256 columns
 constexpr int FULL_ARRIVALS = 2 * (RTG / 32);   // one per restore warp of a group, both CTAs
 constexpr int EMPTY_ARRIVALS = 2 * 4;           // one per epilogue warp, both CTAs
-static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier space");
+static_assert(NBARS * 8 + 8 + QD * 4 <= BAR_BYTES, "barriers, TMEM slot, abort flag, schedule");
+// Dynamic order: CTA 0's X producer runs at most R_MAX k-blocks ahead of the MMAs (slot
+// reuse), which run at most 2 units ahead of both CTAs' epilogues (accumulator reuse), and
+// every other role sits between the two; so the producer that publishes schedule entries is
+// fewer than R_MAX + 3 entries (one unit holds at least one k-block) ahead of any reader, and
+// a ring of QD entries is never overwritten before it is read nor waited on a lap early.
+static_assert(QD >= R_MAX + 3, "unit schedule ring depth");
 static_assert(W_BYTES % 1024 == 0, "128B-swizzled slots stay 1024-aligned");
 static_assert(CS_BYTES % 512 == 0, "64B-swizzled code stages stay 512-byte aligned");
 static_assert(RTG * ITEMS * 32 == BK * TCH, "restore coverage: 32 codes per item");
@@ -155,6 +163,38 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Unit schedule (dynamic order): CTA 0 writes an entry of CTA 1's ring and arrives on its
+// barrier with cluster-scope release; readers wait with cluster-scope acquire.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool uwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_try_acq_cluster(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(&g_gemm_pair_error, 4u);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ void transpose8x8_h(uint32_t (&w)[4], int lane) {
   const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
   const uint32_t sel = b0 ? 0x3276u : 0x5410u;
@@ -194,6 +234,8 @@ struct PArgs {
   int xslot;           // bytes per X slot: tnh * 128 rounded up to 1024
   int grp;             // token tiles per raster group
   int w16;             // 1: A slots are loaded by TMA from restored fp16 weights (no restore)
+  unsigned int* ctr;   // dynamic order: the launch's ticket counter (zeroed before the launch);
+                       // null: static order
 };
 
 // Work unit u -> split, token tile, channel pair and k-block range.  Within a split the
@@ -234,6 +276,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + POOL_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* uq = abort_flag + 1;                   // unit schedule ring (QD entries)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -248,6 +291,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   auto acc_empty = [&](int a) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 2 + a); };
   const uint32_t drain = bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 4);
   auto afull = [&](int hf, int r) { return bar0 + 8u * (3 * R_MAX + 2 * RC_MAX + 5 + hf * R_MAX + r); };
+  auto uq_full = [&](int i) { return bar0 + 8u * (5 * R_MAX + 2 * RC_MAX + 5 + i); };
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < R; ++r) {
@@ -266,6 +310,7 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       mbar_init(acc_empty(a), EMPTY_ARRIVALS);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < QD; ++i) mbar_init(uq_full(i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -286,6 +331,40 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   pdl_launch_dependents();
   pdl_wait();
 
+  // Schedule position q -> work unit (ka.units: none left; -1: a wait gave up).  Static
+  // order: cluster cl takes units cl, cl + ncl, ...  Dynamic order (prefill, many token
+  // tiles): CTA 0's X producer takes the launch counter's next ticket when it starts a unit
+  // and publishes it in both CTAs' ring entry q % QD; every role of both CTAs reads the same
+  // sequence.  Tickets follow the raster order, so whatever the clusters' relative speeds
+  // the units in flight stay one window of the raster, the window whose tiles L2 holds; in
+  // static order a cluster that runs ahead drifts into the next raster window, and the
+  // clusters sharing a tile no longer read it at the same time.
+  auto unit_static = [&](int q) -> int {
+    const int64_t u = cl + (int64_t)q * ncl;
+    return u < ka.units ? (int)u : ka.units;
+  };
+  auto unit_fetch = [&](int q) -> int {                // CTA 0's X producer (one thread)
+    if (!ka.ctr) return unit_static(q);
+    const int u = (int)min(atomicAdd(ka.ctr, 1u), (unsigned)ka.units);
+    const int i = q % QD;
+    uq[i] = u;
+    st_cluster_u32(mapa_shared(smem_u32((const void*)(uq + i)), 1), (uint32_t)u);
+    mbar_arrive_release_cluster(mapa_shared(uq_full(i), 1));
+    mbar_arrive(uq_full(i));
+    return u;
+  };
+  auto unit_read = [&](int q) -> int {                 // one thread
+    if (!ka.ctr) return unit_static(q);
+    if (!uwait(uq_full(q % QD), (uint32_t)((q / QD) & 1), abort_flag)) return -1;
+    return uq[q % QD];
+  };
+  auto unit_read_warp = [&](int q) -> int {            // the whole warp
+    if (!ka.ctr) return unit_static(q);
+    if (!__all_sync(0xFFFFFFFFu, uwait(uq_full(q % QD), (uint32_t)((q / QD) & 1), abort_flag)))
+      return -1;
+    return uq[q % QD];
+  };
+
   if (warp == kXWarp || warp == kCodeWarp) {
     // ------------------------------------------------------------ TMA producers
     // this CTA's X half into the k-block ring, or its codes + statistics into the code ring
@@ -296,7 +375,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       const int step = is_x ? 1 : SK;                 // k-blocks per load (X) or stage (codes)
       int it = 0, s = 0;                              // loads issued; slot
       uint32_t ph = 0;                                // lap parity of slot s
-      for (int u = cl; u < nunits; u += ncl) {
+      for (int q = 0; nunits > 0; ++q) {
+        const int u = (is_x && rank == 0) ? unit_fetch(q) : unit_read(q);
+        if (u < 0 || u >= ka.units) break;
         const PUnit w = pair_unit(u, TN, ka);
         const int c0 = w.c0 + (int)rank * TCH;
         bool ok = true;
@@ -340,7 +421,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       int tl = 0, r = 0;
       uint32_t ph = 0;
       bool ok = true, issued = false;
-      for (int u = cl; u < ka.units && ok; u += ncl, ++tl) {
+      for (int q = 0; ok; ++q, ++tl) {
+        const int u = unit_read(q);
+        if (u < 0 || u >= ka.units) break;
         const PUnit w = pair_unit(u, TN, ka);
         const int acc = tl & 1;
         if (tl >= 2 && !pwait(acc_empty(acc), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
@@ -388,7 +471,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       int it = 0, r = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int u = cl; u < ka.units && ok; u += ncl) {
+      for (int q = 0; ok; ++q) {
+        const int u = unit_read(q);
+        if (u < 0 || u >= ka.units) break;
         const PUnit w = pair_unit(u, TN, ka);
         const int c0 = w.c0 + (int)rank * TCH;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
@@ -444,7 +529,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     int it = 0, c = 0, r = 0, rg = 0;
     uint32_t phc = 0, phr = 0;
     bool ok = true;
-    for (int u = cl; u < ka.units && ok; u += ncl) {
+    for (int q = 0; ok; ++q) {
+      const int u = unit_read_warp(q);
+      if (u < 0 || u >= ka.units) break;
       const PUnit w = pair_unit(u, TN, ka);
       const int g0 = ((w.c0 + (int)rank * TCH) >> 6) & 3;   // first group in the stats box
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
@@ -521,7 +608,9 @@ gemm_q4_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const bool add_res = !ea.partial && ea.epi == FG_EPI_RESIDUAL;
     const uint32_t empty_cl[2] = {mapa_shared(acc_empty(0), 0), mapa_shared(acc_empty(1), 0)};
     int tl = 0;
-    for (int u = cl; u < ka.units; u += ncl, ++tl) {
+    for (int q = 0;; ++q, ++tl) {
+      const int u = unit_read_warp(q);
+      if (u < 0 || u >= ka.units) break;
       const PUnit w = pair_unit(u, TN, ka);
       const int c0 = w.c0 + (int)rank * TCH;
       const int acc = tl & 1;
@@ -690,7 +779,7 @@ static int pair_raster_group(const GemmPlan& p, bool w16) {
 }
 
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,
-                             const EpiArgs& ea, cudaStream_t st, const uint16_t* w16) {
+                             const EpiArgs& ea, cudaStream_t st, const uint16_t* w16, void* ws) {
   const int maxcl = pair_max_clusters();
   if (maxcl <= 0) return cudaErrorInvalidConfiguration;
   const int tnh = p.tn / 2;
@@ -718,9 +807,18 @@ cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_
                     (uint64_t)p.N * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
+  // dynamic order for plans of several token tiles: the ticket counter in the workspace,
+  // zeroed on the stream before the launch
+  unsigned int* ctr = nullptr;
+  if (p.tiles_t >= 2) {
+    if (!ws || p.sched_off % 16 != 0) return cudaErrorInvalidValue;
+    ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + p.sched_off);
+    e = cudaMemsetAsync(ctr, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
+  }
   const PArgs ka{(int)p.M,  (int)p.N, (int)p.K, p.tiles_t, p.tiles_c / 2, p.kblocks,
                  p.kb_per_split, (int)p.units, tnh, r, rc, sk, xslot, pair_raster_group(p, w16),
-                 w16 ? 1 : 0};
+                 w16 ? 1 : 0, ctr};
   const int64_t clusters = std::min<int64_t>(p.units, maxcl);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config((unsigned)(2 * clusters), st, attr);

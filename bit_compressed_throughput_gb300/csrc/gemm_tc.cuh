@@ -217,8 +217,10 @@ cudaError_t launch_gemm_stream(const GemmPlan& p, const fg_q4mat& W, const CUten
 // The CTA-pair kernel (p.kind == kGemmPair): enqueues the main kernel on `st` (the caller
 // launches the split-K reduce when p.splits > 1); builds its own tensor maps.  w16 (nullable):
 // the weight already restored to fp16 [K][N]; the kernel then loads its A slots by TMA instead
-// of restoring the codes.
+// of restoring the codes.  ws: the plan's workspace (with several token tiles it holds the
+// unit counter at p.sched_off, zeroed here on `st` before the launch).
 cudaError_t launch_gemm_pair(const GemmPlan& p, const fg_q4mat& W, const uint16_t* X,
-                             const EpiArgs& ea, cudaStream_t st, const uint16_t* w16 = nullptr);
+                             const EpiArgs& ea, cudaStream_t st, const uint16_t* w16,
+                             void* ws);
 
 }  // namespace fg

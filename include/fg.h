@@ -128,7 +128,9 @@ int fg_dequant_g64(const uint8_t* codes, const uint32_t* ab, int64_t rows, int64
  * leading dimensions K (X) and N (Y, residual).  K % 16 == 0, N % 256 == 0 (one output tile
  * of group statistics is one 16-byte row), M >= 0.
  * Y may alias residual.  ws: device scratch of at least fg_gemm_workspace_bytes(M,K,N)
- * bytes (split-K partial sums when M is small); NULL allowed when that is 0.
+ * bytes (split-K partial sums when M is small; with M > 256 a 4-byte unit counter that the
+ * call zeroes on `stream` before its kernel); NULL allowed when that is 0.  Two calls in
+ * flight at once on different streams need workspaces of their own.
  * [FlexGen review (jaehun.me), "4-bit 압축은 정수 연산 가속과 같은가": restore to FP16
  *  before compute, not an INT4 matmul; FlexGen paper explainer, "Cost Model and Policy
  *  Search": the four h x h and two h x h2 weight matrices of a layer] */
@@ -136,8 +138,9 @@ int fg_dequant_gemm_q4(const uint16_t* X, int64_t M, const fg_q4mat* W, const ui
                        int epilogue, const uint16_t* residual, uint16_t* Y, void* ws,
                        size_t ws_bytes, void* stream);
 /* Scratch bytes fg_dequant_gemm_q4 needs for an M x K by K x N product (split-K fp32
- * partials when M is small; 0 when the plan does not split).  Host computation only; the
- * pages have no counterpart (their GEMMs run in PyTorch). */
+ * partials when M is small, and 256 bytes for the unit counter of the many-token plans;
+ * 0 when neither applies).  Host computation only; the pages have no counterpart (their
+ * GEMMs run in PyTorch). */
 size_t fg_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* The QKV projection with the KV quantise-and-append in its epilogue:

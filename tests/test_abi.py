@@ -85,7 +85,9 @@ def test_gemm_validation(fg):
     need = fg.fg_gemm_workspace_bytes(64, 4096, 256)
     assert need > 0                                  # one tile of 256: split K
     assert call(q4(4096, 256), M=64, ws=FAKE, wsb=need - 1) == fg.FG_ERR_WORKSPACE
-    assert fg.fg_gemm_workspace_bytes(8192, 4096, 12288) == 0      # full grid: no split
+    # full grid, no split: only the 256-byte unit counter of the many-token plan
+    assert fg.fg_gemm_workspace_bytes(8192, 4096, 12288) == 256
+    assert fg.fg_gemm_workspace_bytes(200, 64, 49152) == 0         # one token tile, no split
 
 
 def test_fused_gemm_validation(fg):
