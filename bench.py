@@ -57,10 +57,10 @@ NOMINAL_F16_TFLOPS = 2250.0
 # one pass's launch mix; a workload without a capture of the current kernel reports null.
 # opt-175b: the QKV, O, FC1 and FC2 projections of one GPU batch (18432 tokens, equal launch
 # counts per pass) in the fp16-weight mode of the layer prefill (profile case
-# layer-prefill-opt175b) read + wrote 45.06, 14.04, 61.50 and 76.83 GB; their algorithmic
-# bytes (X, the fp16 weights, Y, and the residual read of O and FC2) are 2.72, 1.66, 3.47 and
-# 3.93 GB.
-GEMM_TRAFFIC_PER_LAUNCH = {"opt-175b": 49360370816}
+# layer-prefill-opt175b), units in dynamic order, read + wrote 16.16, 6.77, 21.46 and
+# 42.12 GB; their algorithmic bytes (X, the fp16 weights, Y, and the residual read of O and
+# FC2) are 2.72, 1.66, 3.47 and 3.93 GB.
+GEMM_TRAFFIC_PER_LAUNCH = {"opt-175b": 21629349376}
 GEMM_ALGORITHMIC_BYTES_PER_LAUNCH = {"opt-175b": 2944401408}
 
 
