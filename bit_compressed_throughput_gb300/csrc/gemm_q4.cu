@@ -862,8 +862,9 @@ static void stream_plan(GemmPlan& p, int nsm) {
 // CTA-pair plan: tiles of 256 channels (a pair) x tn tokens, tn = 2 tnh the smallest multiple
 // of 16 that covers M in ceil(M / 256) tiles (M = 144 -> one tile of 144).  K is split when
 // the tiles leave clusters idle: the split count minimises the busiest cluster's k-blocks
-// (units taken round-robin, about two k-blocks of ramp per unit and 24 for a split's partials
-// and reduce).  The count is capped independently of the SM count (at most 8, at least 8
+// (units of equal size taken in turn: round-robin, or the next free ticket in the kernel's
+// dynamic order, which deals the same counts; about two k-blocks of ramp per unit and 24 for
+// a split's partials and reduce).  The count is capped independently of the SM count (at most 8, at least 8
 // k-blocks per split, no more units than two rounds of the largest cluster count planned for)
 // and the workspace is sized for the cap, so a workspace sized by the query covers any device.
 // With several token tiles the workspace also holds the 256-byte unit counter of the
