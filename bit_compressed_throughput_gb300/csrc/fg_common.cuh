@@ -129,6 +129,72 @@ __device__ __forceinline__ uint32_t q4_codes8_checked(const uint32_t (&w)[4], co
   return near ? q4_codes8_exact(make_uint4(w[0], w[1], w[2], w[3]), g.af, g.bma) : c;
 }
 
+// ---- the same fast path two values per instruction (packed binary32 pairs, sm_100 and up):
+// sub / mul / add .rn.f32x2 round each lane as the scalar operations do, so y, t and rint(y)
+// are the same bits as in q4_code_fast.  The tie test takes the largest |y - rint(y)| of the
+// 8 values (max.NaN keeps a NaN, which counts as near, as in q4_code_fast), and the code of a
+// value is byte 0 of t = 1.5 * 2^23 + rint(y): one byte permute gathers four of them.
+__device__ __forceinline__ uint64_t q4_pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void q4_unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t q4_sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t q4_mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t q4_add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float q4_max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t q4_codes8_x2(const uint32_t (&w)[4], const Q4Group& g,
+                                                 bool& near) {
+  if (g.bma == 0.0f) return 0u;                   // constant group
+  const uint64_t a2 = q4_pack2(g.af, g.af), c2 = q4_pack2(g.c15, g.c15);
+  const uint64_t k2 = q4_pack2(12582912.0f, 12582912.0f);
+  uint32_t tb[8];
+  float dmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x2 = unpack_h2(w[i]);
+    const uint64_t y = q4_mul2(q4_sub2(q4_pack2(x2.x, x2.y), a2), c2);
+    const uint64_t t = q4_add2(y, k2);
+    float d0, d1, t0, t1;
+    q4_unpack2(q4_sub2(y, q4_sub2(t, k2)), d0, d1);
+    q4_unpack2(t, t0, t1);
+    dmax = q4_max_nan(dmax, q4_max_nan(fabsf(d0), fabsf(d1)));
+    tb[2 * i] = __float_as_uint(t0);
+    tb[2 * i + 1] = __float_as_uint(t1);
+  }
+  near |= !(dmax <= 0.5f - 0x1p-16f);
+  const uint32_t ev = __byte_perm(__byte_perm(tb[0], tb[2], 0x0040),
+                                  __byte_perm(tb[4], tb[6], 0x0040), 0x5410);
+  const uint32_t od = __byte_perm(__byte_perm(tb[1], tb[3], 0x0040),
+                                  __byte_perm(tb[5], tb[7], 0x0040), 0x5410);
+  return (ev & 0x0F0F0F0Fu) | ((od & 0x0F0F0F0Fu) << 4);
+}
+__device__ __forceinline__ uint32_t q4_codes8_checked_x2(const uint32_t (&w)[4],
+                                                         const Q4Group& g) {
+  bool near = false;
+  const uint32_t c = q4_codes8_x2(w, g, near);
+  return near ? q4_codes8_exact(make_uint4(w[0], w[1], w[2], w[3]), g.af, g.bma) : c;
+}
+
 // Programmatic dependent launch: every library kernel lets the next kernel of the stream
 // launch at once and waits for its predecessor's results (and for its predecessor to have
 // finished reading what this kernel overwrites) before touching global data, so launch and

@@ -29,7 +29,7 @@ __device__ __forceinline__ uint32_t quantize8(const uint4 v, uint32_t* ab_out) {
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) mm = __vminu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
   *ab_out = q4_ab_word(mm);
-  return q4_codes8_checked(w, q4_group(*ab_out));
+  return q4_codes8_checked_x2(w, q4_group(*ab_out));
 }
 
 __global__ void __launch_bounds__(kThreads)
