@@ -88,6 +88,10 @@ def test_gemm_validation(fg):
     # full grid, no split: only the 256-byte unit counter of the many-token plan
     assert fg.fg_gemm_workspace_bytes(8192, 4096, 12288) == 256
     assert fg.fg_gemm_workspace_bytes(200, 64, 49152) == 0         # one token tile, no split
+    # with split partials too: the counter follows them at a 256-byte boundary
+    for M, K, N in ((512, 8192, 256), (18432, 49152, 12288), (300, 512, 2048)):
+        wsb = fg.fg_gemm_workspace_bytes(M, K, N)
+        assert wsb >= 256 and wsb % 256 == 0, (M, K, N, wsb)
 
 
 def test_fused_gemm_validation(fg):
